@@ -1,0 +1,209 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE FFN layer forward.
+ *
+ * The layer is the inference forward of one Mixture-of-Experts FFN layer:
+ *
+ *   router logits -> top-k gating -> regroup tokens by expert -> grouped SwiGLU
+ *   expert FFN over the active experts -> weighted combine back to token order
+ *
+ * Sources (page title, section):
+ *   [Mira]   "Mira: adaptive caching and predictive expert staging for MoE
+ *            inference" (gsyq.cn/news/338825): sec. 4.2 (Top-K gating).
+ *   [CoInf]  "CPU-GPU co-inference for MoE models" (maplevalley.com.cn/news/2111104):
+ *            sec. 2.1 (router and expert cache on the GPU), sec. 2.2 (expert
+ *            slots, S = floor(memory / expert size)), sec. 5.1 (group quantisation).
+ *   [Strata] "125B MoE on an RTX 3090 at 100+ tok/s: a full-stack inference
+ *            optimisation log" (bjdmk.com.cn/news/6009460): sec. 1.1 (top-2 /
+ *            top-1 routing), sec. 2.1 (shared expert always resident; hot-expert
+ *            pool), sec. 3.1 (per-expert int4 scale and zero-point, dequantise
+ *            without a separate pass), sec. 3.2 (expert FFN is a two-layer MLP;
+ *            one grouped GEMM over the active experts), sec. 4.2 (tokens
+ *            regrouped by expert id, contiguous per expert).
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers owned by the caller unless stated otherwise.
+ *     The library never allocates, frees or synchronises (except
+ *     moe_last_device_error, which reads one word back synchronously).
+ *   - bf16 and fp16 tensors are passed as their 16-bit patterns (uint16_t).
+ *     Matrices are row-major; "[rows][cols]" lists the slow index first.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) in call order.  Nothing is launched when a host-side check fails.
+ *   - Every pointer must be 16-byte aligned; workspaces and pools 256-byte aligned.
+ *   - Host-side argument errors return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *     MOE_ERR_WORKSPACE; a failed launch returns MOE_ERR_CUDA.  Device-side
+ *     checks (an expert index outside [0,E), a slot outside [0,n_slots), a
+ *     pipeline wait that exceeds its time limit) never trap: they OR a code into
+ *     the workspace error word, skip the affected work and return; read it with
+ *     moe_last_device_error().  No C++ exception crosses this ABI.
+ *   - Logits must be finite.
+ *
+ * Limits: 1 <= E <= 256, 1 <= k <= min(E, 16), T*k <= 1<<20, d_model and d_ff
+ * multiples of 128 and <= 32768.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t;   /* identical to cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, k outside 1..E */
+  MOE_ERR_UNSUPPORTED = 2,   /* outside the documented limits */
+  MOE_ERR_WORKSPACE = 3,     /* workspace smaller than the *_workspace_bytes() answer */
+  MOE_ERR_CUDA = 4,          /* a CUDA launch or attribute call failed */
+  MOE_ERR_DEVICE = 5         /* moe_last_device_error found a device-side error code */
+} moe_status;
+
+/* Device-side error codes ORed into the workspace error word. */
+enum {
+  MOE_DEVERR_TIMEOUT = 1,       /* a pipeline wait ran past its limit (~2 s) */
+  MOE_DEVERR_EXPERT_RANGE = 2,  /* topk_idx outside [0, E) */
+  MOE_DEVERR_SLOT_RANGE = 4,    /* expert_to_slot[e] outside [0, n_slots) */
+  MOE_DEVERR_OFFSETS = 8        /* offsets not non-decreasing or beyond the row count */
+};
+
+/* Expert weight formats. */
+typedef enum {
+  MOE_W_BF16 = 0,       /* bf16 weights */
+  MOE_W_INT4_G128 = 1   /* int4, asymmetric, one fp16 scale + one fp16 zero (integer 0..15)
+                           per row and group of 128 input elements: w = (q - z) * s
+                           ([Strata] sec. 3.1; [CoInf] sec. 5.1) */
+} moe_wfmt;
+
+/* The expert pool: n_slots equally sized slots in one device allocation, and
+ * the table that maps an expert id to its slot ([CoInf] sec. 2.2 slots;
+ * [Strata] sec. 2.1 resident expert pool).  Described by, not owned by, the
+ * library.  Slot s starts at pool + s * slot_bytes and holds one expert in the
+ * library's prepacked layout (see moe_prepack_expert). */
+typedef struct {
+  int n_experts;                  /* E: entries of expert_to_slot */
+  int n_slots;                    /* slots in the pool */
+  int d_model, d_ff;              /* d and F of every expert in this pool */
+  int fmt;                        /* moe_wfmt */
+  const void* pool;               /* device, 256-byte aligned */
+  size_t slot_bytes;              /* >= moe_slot_bytes(fmt, d_model, d_ff), multiple of 256 */
+  const int32_t* expert_to_slot;  /* device int32 [n_experts], values in [0, n_slots) */
+} moe_pool;
+
+/* Canonical (interchange) weights of one expert, device pointers.
+ * bf16:  w[0] = W_gate [F][d], w[1] = W_up [F][d], w[2] = W_down [d][F]  (bf16)
+ * int4:  w[m] = packed bytes [rows][K/2]: byte j holds element 2j in its low
+ *        nibble and 2j+1 in its high nibble; scale[m], zero[m] = fp16
+ *        [rows][K/128]; (rows, K) = (F, d) for gate/up and (d, F) for down. */
+typedef struct {
+  const void* w[3];
+  const uint16_t* scale[3];   /* int4 only */
+  const uint16_t* zero[3];    /* int4 only */
+} moe_expert_src;
+
+/* ---------------------------------------------------------------- information */
+
+const char* moe_status_str(int status);
+
+/* Bytes one expert occupies in the prepacked slot layout (no padding):
+ * bf16: 6*d*F;  int4: 1.5*d*F + 3*F*(d/128)*4.  0 for unsupported shapes. */
+size_t moe_slot_bytes(int fmt, int d_model, int d_ff);
+
+/* ---------------------------------------------------------------- weight preparation
+ * Not on the hot path.  Rewrites one expert from the canonical layout into the
+ * slot layout the grouped GEMM streams: per (matrix, 128-row tile, K step) one
+ * contiguous block, bf16 tiles pre-swizzled for the tensor core, int4 nibbles
+ * reordered for in-register unpacking with the group's scale and zero beside
+ * them.  slot_dst must hold moe_slot_bytes() bytes. */
+moe_status moe_prepack_expert(int fmt, int d_model, int d_ff, const moe_expert_src* src,
+                              void* slot_dst, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- hot path */
+
+/* Top-k gating ([Mira] sec. 4.2; [Strata] sec. 1.1).
+ * logits: fp32 [T][E].  For each token the k largest logits (the lower expert
+ * index first among equal logits), in descending order -> topk_idx int32 [T][k];
+ * topk_w fp32 [T][k] = softmax over the k selected logits (same as softmax over
+ * all E renormalised over the k). */
+moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                          float* topk_w, moe_stream_t stream);
+
+/* Regroup tokens by expert ([Strata] sec. 4.2): histogram, exclusive scan and a
+ * stable scatter of the A = T*k assignments a = t*k + j.
+ *   counts int32 [E]: assignments per expert;  offsets int32 [E+1], offsets[E] = A;
+ *   row_of_assign int32 [A]: row of assignment a = offsets[e] + number of earlier
+ *     assignments with the same expert e = topk_idx[a];
+ *   token_of_row int32 [A]: token of each row (ascending within an expert);
+ *   x_perm bf16 [A][d]: x_perm[row_of_assign[a]] = x[a / k]  (x is bf16 [T][d]).
+ * ws: moe_permute_workspace_bytes() bytes (holds the error word). */
+size_t moe_permute_workspace_bytes(void);
+moe_status moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int k, int E, int d,
+                       int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
+                       int32_t* token_of_row, uint16_t* x_perm, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/* Grouped SwiGLU expert FFN over the active experts ([Strata] sec. 3.2, 3.1).
+ * Rows [offsets[e], offsets[e+1]) of x_perm (bf16 [A][d]) belong to expert e and
+ * use the weights in slot expert_to_slot[e] of `pool`:
+ *   h = bf16(silu(x W_gate^T) * (x W_up^T))  [rows][F]     (fp32 accumulation)
+ *   y_perm = bf16(h W_down^T)                 bf16 [A][d]
+ * int4 weights are dequantised inside the GEMM main loop; experts with no rows
+ * are never read.  ws: moe_grouped_ffn_workspace_bytes(A, pool) bytes. */
+size_t moe_grouped_ffn_workspace_bytes(int A, const moe_pool* pool);
+moe_status moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int A,
+                           const moe_pool* pool, uint16_t* y_perm, void* ws, size_t ws_bytes,
+                           moe_stream_t stream);
+
+/* Weighted combine back to token order:
+ *   out[t] = bf16( sum_{j<k} topk_w[t][j] * y_perm[row_of_assign[t*k+j]]  + shared_y[t] )
+ * summed in fp32 in the order j = 0..k-1, shared_y (bf16 [T][d]) last; shared_y
+ * may be NULL.  out bf16 [T][d]. */
+moe_status moe_combine(const uint16_t* y_perm, const int32_t* row_of_assign, const float* topk_w,
+                       const uint16_t* shared_y, int T, int k, int d, uint16_t* out,
+                       moe_stream_t stream);
+
+/* The whole layer: route -> permute -> grouped FFN -> combine, with an optional
+ * always-on shared expert ([Strata] sec. 2.1) of weight 1.0 added to every token.
+ * x bf16 [T][d]; logits fp32 [T][E] (E = routed->n_experts); out bf16 [T][d].
+ * shared: NULL, or a pool view with n_experts == 1 and the same d_model, d_ff and
+ * fmt as `routed` (it may point into the same allocation).
+ * ws: moe_layer_workspace_bytes(T, k, routed, shared) bytes; its first word is
+ * the device error word, cleared at the start of every call. */
+size_t moe_layer_workspace_bytes(int T, int k, const moe_pool* routed, const moe_pool* shared);
+moe_status moe_layer_forward(const uint16_t* x, const float* logits, int T, int k,
+                             const moe_pool* routed, const moe_pool* shared, uint16_t* out,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Stage boundaries of moe_layer_forward, for timing with CUDA events. */
+enum {
+  MOE_STAGE_ROUTE = 0,    /* top-k gating */
+  MOE_STAGE_PERMUTE = 1,  /* histogram, scan, stable scatter of the indices */
+  MOE_STAGE_GATHER = 2,   /* x rows copied into expert order */
+  MOE_STAGE_GATE_UP = 3,  /* grouped gate/up GEMM + SwiGLU */
+  MOE_STAGE_DOWN = 4,     /* grouped down GEMM (K-split partial sums) */
+  MOE_STAGE_COMBINE = 5,  /* weighted combine (+ shared expert) */
+  MOE_N_STAGES = 6
+};
+
+/* Same as moe_layer_forward; if stage_events is non-NULL it must point to
+ * MOE_N_STAGES + 1 cudaEvent_t handles, recorded on `stream` before each stage
+ * and after the last one. */
+moe_status moe_layer_forward_timed(const uint16_t* x, const float* logits, int T, int k,
+                                   const moe_pool* routed, const moe_pool* shared, uint16_t* out,
+                                   void* ws, size_t ws_bytes, moe_stream_t stream,
+                                   void* const* stage_events);
+
+/* Kernel launches one moe_layer_forward enqueues for these arguments (0 on error). */
+int moe_layer_launch_count(int T, int k, const moe_pool* routed, const moe_pool* shared);
+
+/* Synchronously reads the device error word of a workspace written by
+ * moe_permute, moe_grouped_ffn or moe_layer_forward (waits for `stream`).
+ * *code = the ORed MOE_DEVERR_* bits; returns MOE_ERR_DEVICE if any bit is set. */
+moe_status moe_last_device_error(const void* ws, int* code, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,264 @@
+"""GB300 (sm_103a) MoE FFN layer forward: Python binding of the C ABI in include/moe.h.
+
+This module only marshals arguments (torch tensors -> device pointers, the
+current torch stream -> cudaStream_t) and calls the CUDA library
+libmoe_gb300.so; every step of the layer runs in the library's kernels.  There
+is no CPU path: if the library is not built, every call raises.
+
+Typical use::
+
+    import moe_expert_layer_03_gb300 as moe
+    pool = moe.ExpertPool(n_slots=8, d_model=4096, d_ff=14336, fmt=moe.W_INT4)
+    for e in range(8):
+        pool.load_expert(e, canonical_weights_of_expert[e])     # device tensors
+    routed = pool.view(expert_to_slot)                          # int32 [E] on the device
+    out = moe.layer_forward(x, logits, k=2, routed=routed)      # bf16 [T, d]
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+from .build import LIB, build  # noqa: F401  (build() compiles the library in-tree)
+
+W_BF16 = 0
+W_INT4 = 1
+FMT = {"bf16": W_BF16, "int4": W_INT4}
+N_STAGES = 6
+STAGES = ("route", "permute", "gather", "gate_up", "down", "combine")
+DEVERR = {1: "timeout", 2: "expert index out of range", 4: "slot out of range", 8: "bad offsets"}
+
+EXPORTS = ("moe_status_str", "moe_slot_bytes", "moe_prepack_expert", "moe_route_topk",
+           "moe_permute_workspace_bytes", "moe_permute", "moe_grouped_ffn_workspace_bytes",
+           "moe_grouped_ffn", "moe_combine", "moe_layer_workspace_bytes", "moe_layer_forward",
+           "moe_layer_forward_timed", "moe_layer_launch_count", "moe_last_device_error")
+
+
+class MoeError(RuntimeError):
+    pass
+
+
+class MoePool(C.Structure):
+    _fields_ = [("n_experts", C.c_int), ("n_slots", C.c_int), ("d_model", C.c_int),
+                ("d_ff", C.c_int), ("fmt", C.c_int), ("pool", C.c_void_p),
+                ("slot_bytes", C.c_size_t), ("expert_to_slot", C.c_void_p)]
+
+
+class ExpertSrc(C.Structure):
+    _fields_ = [("w", C.c_void_p * 3), ("scale", C.c_void_p * 3), ("zero", C.c_void_p * 3)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> C.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB):
+                raise MoeError(f"CUDA library not built ({LIB}); run moe_expert_layer_03_gb300.build()")
+            L = C.CDLL(LIB)
+            P, I, S = C.c_void_p, C.c_int, C.c_size_t
+            L.moe_status_str.restype = C.c_char_p
+            L.moe_status_str.argtypes = [I]
+            L.moe_slot_bytes.restype = S
+            L.moe_slot_bytes.argtypes = [I, I, I]
+            L.moe_prepack_expert.argtypes = [I, I, I, C.POINTER(ExpertSrc), P, P]
+            L.moe_route_topk.argtypes = [P, I, I, I, P, P, P]
+            L.moe_permute_workspace_bytes.restype = S
+            L.moe_permute_workspace_bytes.argtypes = []
+            L.moe_permute.argtypes = [P, P, I, I, I, I, P, P, P, P, P, P, S, P]
+            L.moe_grouped_ffn_workspace_bytes.restype = S
+            L.moe_grouped_ffn_workspace_bytes.argtypes = [I, C.POINTER(MoePool)]
+            L.moe_grouped_ffn.argtypes = [P, P, I, C.POINTER(MoePool), P, P, S, P]
+            L.moe_combine.argtypes = [P, P, P, P, I, I, I, P, P]
+            L.moe_layer_workspace_bytes.restype = S
+            L.moe_layer_workspace_bytes.argtypes = [I, I, C.POINTER(MoePool), C.POINTER(MoePool)]
+            L.moe_layer_forward.argtypes = [P, P, I, I, C.POINTER(MoePool), C.POINTER(MoePool), P,
+                                            P, S, P]
+            L.moe_layer_forward_timed.argtypes = [P, P, I, I, C.POINTER(MoePool),
+                                                  C.POINTER(MoePool), P, P, S, P, P]
+            L.moe_layer_launch_count.argtypes = [I, I, C.POINTER(MoePool), C.POINTER(MoePool)]
+            L.moe_last_device_error.argtypes = [P, C.POINTER(C.c_int), P]
+            _lib = L
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise MoeError(f"{what}: {lib().moe_status_str(status).decode()} (status {status})")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+# ----------------------------------------------------------------------------- expert pool
+class PoolView:
+    """A moe_pool struct plus the tensors it points at (kept alive)."""
+
+    def __init__(self, pool: "ExpertPool", expert_to_slot: torch.Tensor):
+        assert expert_to_slot.dtype == torch.int32 and expert_to_slot.is_cuda
+        self.pool = pool
+        self.e2s = expert_to_slot.contiguous()
+        self.struct = MoePool(self.e2s.numel(), pool.n_slots, pool.d_model, pool.d_ff, pool.fmt,
+                              pool.buf.data_ptr(), pool.slot_bytes, self.e2s.data_ptr())
+
+    @property
+    def ref(self):
+        return C.byref(self.struct)
+
+
+class ExpertPool:
+    """HBM-resident expert pool: n_slots slots of the library's prepacked layout."""
+
+    def __init__(self, n_slots: int, d_model: int, d_ff: int, fmt: int | str, device="cuda"):
+        self.fmt = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+        self.n_slots, self.d_model, self.d_ff = n_slots, d_model, d_ff
+        raw = lib().moe_slot_bytes(self.fmt, d_model, d_ff)
+        if raw == 0:
+            raise MoeError(f"unsupported expert shape d_model={d_model} d_ff={d_ff}")
+        self.slot_bytes = (raw + 255) // 256 * 256
+        self.buf = torch.empty(n_slots * self.slot_bytes, dtype=torch.uint8, device=device)
+        assert self.buf.data_ptr() % 256 == 0
+
+    def slot_ptr(self, slot: int) -> int:
+        return self.buf.data_ptr() + slot * self.slot_bytes
+
+    def load_expert(self, slot: int, weights: dict, stream=None):
+        """Prepack one expert (canonical device tensors, see moe.h) into `slot`."""
+        src = ExpertSrc()
+        keep = []
+        for m, name in enumerate(("gate", "up", "down")):
+            wm = weights[name]
+            if self.fmt == W_BF16:
+                w = wm["w"].contiguous()
+                keep.append(w)
+                src.w[m] = w.data_ptr()
+            else:
+                q, s, z = (wm[k].contiguous() for k in ("q", "scale", "zero"))
+                keep += [q, s, z]
+                src.w[m], src.scale[m], src.zero[m] = q.data_ptr(), s.data_ptr(), z.data_ptr()
+        for t in keep:
+            if not t.is_cuda:
+                raise MoeError("expert weights must be device tensors")
+        _check(lib().moe_prepack_expert(self.fmt, self.d_model, self.d_ff, C.byref(src),
+                                        C.c_void_p(self.slot_ptr(slot)), _stream(stream)),
+               "moe_prepack_expert")
+        torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+
+    def view(self, expert_to_slot: torch.Tensor) -> PoolView:
+        return PoolView(self, expert_to_slot)
+
+
+# ----------------------------------------------------------------------------- workspaces
+def layer_workspace_bytes(T: int, k: int, routed: PoolView, shared: PoolView | None = None) -> int:
+    return lib().moe_layer_workspace_bytes(T, k, routed.ref, shared.ref if shared else None)
+
+
+def grouped_ffn_workspace_bytes(A: int, pool: PoolView) -> int:
+    return lib().moe_grouped_ffn_workspace_bytes(A, pool.ref)
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def last_device_error(ws: torch.Tensor, stream=None) -> int:
+    """The ORed device error code of the last call that used this workspace (syncs)."""
+    code = C.c_int(0)
+    st = lib().moe_last_device_error(_ptr(ws), C.byref(code), _stream(stream))
+    if st not in (0, 5):
+        _check(st, "moe_last_device_error")
+    return code.value
+
+
+# ----------------------------------------------------------------------------- hot path
+def route_topk(logits: torch.Tensor, k: int, idx=None, w=None, stream=None):
+    T, E = logits.shape
+    idx = idx if idx is not None else torch.empty(T, k, dtype=torch.int32, device=logits.device)
+    w = w if w is not None else torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    _check(lib().moe_route_topk(_ptr(logits), T, E, k, _ptr(idx), _ptr(w), _stream(stream)),
+           "moe_route_topk")
+    return idx, w
+
+
+def permute(topk_idx: torch.Tensor, x: torch.Tensor, E: int, ws=None, stream=None):
+    T, k = topk_idx.shape
+    d = x.shape[1]
+    A = T * k
+    dev = x.device
+    out = {
+        "counts": torch.empty(E, dtype=torch.int32, device=dev),
+        "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+        "row_of_assign": torch.empty(A, dtype=torch.int32, device=dev),
+        "token_of_row": torch.empty(A, dtype=torch.int32, device=dev),
+        "x_perm": torch.empty(A, d, dtype=torch.bfloat16, device=dev),
+    }
+    ws = ws if ws is not None else workspace(lib().moe_permute_workspace_bytes(), dev)
+    _check(lib().moe_permute(_ptr(topk_idx), _ptr(x), T, k, E, d, _ptr(out["counts"]),
+                             _ptr(out["offsets"]), _ptr(out["row_of_assign"]),
+                             _ptr(out["token_of_row"]), _ptr(out["x_perm"]), _ptr(ws), ws.numel(),
+                             _stream(stream)), "moe_permute")
+    out["ws"] = ws
+    return out
+
+
+def grouped_ffn(x_perm: torch.Tensor, offsets: torch.Tensor, pool: PoolView, y_perm=None, ws=None,
+                stream=None):
+    A, d = x_perm.shape
+    y_perm = y_perm if y_perm is not None else torch.empty(A, d, dtype=torch.bfloat16,
+                                                           device=x_perm.device)
+    ws = ws if ws is not None else workspace(grouped_ffn_workspace_bytes(A, pool), x_perm.device)
+    _check(lib().moe_grouped_ffn(_ptr(x_perm), _ptr(offsets), A, pool.ref, _ptr(y_perm), _ptr(ws),
+                                 ws.numel(), _stream(stream)), "moe_grouped_ffn")
+    return y_perm, ws
+
+
+def combine(y_perm: torch.Tensor, row_of_assign: torch.Tensor, topk_w: torch.Tensor,
+            shared_y: torch.Tensor | None = None, out=None, stream=None):
+    T, k = topk_w.shape
+    d = y_perm.shape[1]
+    out = out if out is not None else torch.empty(T, d, dtype=torch.bfloat16, device=y_perm.device)
+    _check(lib().moe_combine(_ptr(y_perm), _ptr(row_of_assign), _ptr(topk_w), _ptr(shared_y), T, k,
+                             d, _ptr(out), _stream(stream)), "moe_combine")
+    return out
+
+
+def layer_forward(x: torch.Tensor, logits: torch.Tensor, k: int, routed: PoolView,
+                  shared: PoolView | None = None, out=None, ws=None, events=None, stream=None):
+    """out = MoE layer(x): bf16 [T, d].  `events`: optional N_STAGES+1 torch.cuda.Event."""
+    T, d = x.shape
+    out = out if out is not None else torch.empty(T, d, dtype=torch.bfloat16, device=x.device)
+    need = layer_workspace_bytes(T, k, routed, shared)
+    if need == 0:
+        raise MoeError("moe_layer_workspace_bytes: invalid layer description")
+    ws = ws if ws is not None else workspace(need, x.device)
+    sh = shared.ref if shared is not None else None
+    if events is None:
+        st = lib().moe_layer_forward(_ptr(x), _ptr(logits), T, k, routed.ref, sh, _ptr(out),
+                                     _ptr(ws), ws.numel(), _stream(stream))
+    else:
+        s = stream if stream is not None else torch.cuda.current_stream()
+        for e in events:          # torch creates the CUDA event on its first record
+            if not e.cuda_event:
+                e.record(s)
+        arr = (C.c_void_p * (N_STAGES + 1))(*[e.cuda_event for e in events])
+        st = lib().moe_layer_forward_timed(_ptr(x), _ptr(logits), T, k, routed.ref, sh, _ptr(out),
+                                           _ptr(ws), ws.numel(), _stream(stream), arr)
+    _check(st, "moe_layer_forward")
+    return out, ws
+
+
+def layer_launch_count(T: int, k: int, routed: PoolView, shared: PoolView | None = None) -> int:
+    return lib().moe_layer_launch_count(T, k, routed.ref, shared.ref if shared else None)

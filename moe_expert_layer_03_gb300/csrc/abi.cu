@@ -1,0 +1,408 @@
+// abi.cu -- the extern "C" entry points declared in include/moe.h: host-side
+// argument checks, workspace carve-up, TMA tensor maps and the launch sequence
+//   route -> permute -> gather -> gate/up GEMM -> down GEMM -> combine
+// (one stream, nothing allocated, nothing synchronised).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kernels.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr int MAX_E = 256;
+constexpr int MAX_K = 16;
+constexpr int MAX_A = 1 << 20;
+constexpr int MAX_DIM = 32768;
+constexpr int TARGET_ITEMS = 640;   // down-GEMM work items to aim for when picking a K split
+constexpr int MAX_KSPLIT = 8;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool have_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+inline bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+inline bool al256(const void* p) { return ((uintptr_t)p & 255u) == 0; }
+inline size_t up1k(size_t x) { return (x + 1023) & ~(size_t)1023; }
+
+// bf16 row-major [rows][K] -> TMA map with a {64 x box_rows} box, 128-byte swizzle.
+bool make_row_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
+  if (!have_encoder()) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)KSTEP, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+moe_status check_pool(const moe_pool* p, bool single) {
+  if (!p || !p->pool || !p->expert_to_slot) return MOE_ERR_INVALID_ARG;
+  if (p->fmt != MOE_W_BF16 && p->fmt != MOE_W_INT4_G128) return MOE_ERR_INVALID_ARG;
+  if (p->n_experts < 1 || p->n_slots < 1) return MOE_ERR_INVALID_ARG;
+  if (single && p->n_experts != 1) return MOE_ERR_INVALID_ARG;
+  if (p->n_experts > MAX_E) return MOE_ERR_UNSUPPORTED;
+  if (p->d_model < 128 || p->d_ff < 128 || p->d_model % 128 || p->d_ff % 128)
+    return MOE_ERR_INVALID_ARG;
+  if (p->d_model > MAX_DIM || p->d_ff > MAX_DIM) return MOE_ERR_UNSUPPORTED;
+  if (!al256(p->pool) || p->slot_bytes % 256 ||
+      p->slot_bytes < moe_slot_bytes(p->fmt, p->d_model, p->d_ff))
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(p->expert_to_slot)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// Largest chunk of one expert's rows that one work item covers (the B tile height).
+int choose_bn(int A, int E) {
+  const int mean = (A + E - 1) / E;
+  int bn = 16;
+  while (bn < 2 * mean && bn < 256) bn <<= 1;
+  return bn;
+}
+
+int choose_ksplit(int A, int E, bool has_shared, int bn, int n_mt, int F) {
+  const int active = (A < E ? A : E) + (has_shared ? 1 : 0);
+  const int mean = (A + E - 1) / E;
+  const int nch = mean > bn ? (mean + bn - 1) / bn : 1;
+  const long items = (long)active * n_mt * nch;
+  int s = (int)((TARGET_ITEMS + items - 1) / items);
+  const int G = F / QGROUP;
+  if (s > MAX_KSPLIT) s = MAX_KSPLIT;
+  if (s > G) s = G;
+  return s < 1 ? 1 : s;
+}
+
+struct LayerLayout {
+  int A, Tsh, rows, E, d, F, bn, ksplit;
+  size_t err, idx, w, counts, offsets, roa, tor, xperm, h, part, total;
+};
+
+LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* shared) {
+  LayerLayout L{};
+  L.A = T * k;
+  L.Tsh = shared ? T : 0;
+  L.rows = L.A + L.Tsh;
+  L.E = routed->n_experts;
+  L.d = routed->d_model;
+  L.F = routed->d_ff;
+  L.bn = choose_bn(L.A, L.E);
+  L.ksplit = choose_ksplit(L.A, L.E, shared != nullptr, L.bn, L.d / TILE_M, L.F);
+  size_t o = 0;
+  L.err = o;      o += 1024;
+  L.idx = o;      o = up1k(o + (size_t)L.A * 4);
+  L.w = o;        o = up1k(o + (size_t)L.A * 4);
+  L.counts = o;   o = up1k(o + (size_t)(L.E + 1) * 4);
+  L.offsets = o;  o = up1k(o + (size_t)(L.E + 2) * 4);
+  L.roa = o;      o = up1k(o + (size_t)L.A * 4);
+  L.tor = o;      o = up1k(o + (size_t)L.rows * 4);
+  L.xperm = o;    o = up1k(o + (size_t)L.rows * L.d * 2);
+  L.h = o;        o = up1k(o + (size_t)L.rows * L.F * 2);
+  L.part = o;     o = up1k(o + (size_t)L.ksplit * L.rows * L.d * 4);
+  L.total = o;
+  return L;
+}
+
+GemmArgs base_args(const moe_pool* routed, const moe_pool* shared, int* err) {
+  GemmArgs a{};
+  a.n_routed = routed->n_experts;
+  a.pool_r = (const uint8_t*)routed->pool;
+  a.slot_bytes_r = routed->slot_bytes;
+  a.e2s_r = routed->expert_to_slot;
+  a.n_slots_r = routed->n_slots;
+  if (shared) {
+    a.pool_s = (const uint8_t*)shared->pool;
+    a.slot_bytes_s = shared->slot_bytes;
+    a.e2s_s = shared->expert_to_slot;
+    a.n_slots_s = shared->n_slots;
+  } else {
+    a.pool_s = a.pool_r;
+    a.slot_bytes_s = a.slot_bytes_r;
+    a.e2s_s = a.e2s_r;
+    a.n_slots_s = a.n_slots_r;
+  }
+  a.err = err;
+  return a;
+}
+
+// gate/up (SwiGLU) then down over the row groups described by `offsets`.
+moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups, int rows,
+                   const moe_pool* routed, const moe_pool* shared, int bn, int ksplit, uint16_t* h,
+                   float* part, int* err, cudaStream_t s, cudaEvent_t ev_mid, cudaEvent_t ev_down) {
+  const int d = routed->d_model, F = routed->d_ff, fmt = routed->fmt;
+  const int grid = sm_count();
+  CUtensorMap mx, mh;
+  if (!make_row_map(&mx, x_rows, rows, d, bn) || !make_row_map(&mh, h, rows, F, bn))
+    return MOE_ERR_CUDA;
+  GemmArgs a = base_args(routed, shared, err);
+  a.offsets = offsets;
+  a.n_groups = n_groups;
+  a.bn = bn;
+  a.rows_total = rows;
+
+  GemmArgs g = a;   // gate/up + SwiGLU
+  g.sec_off = 0;
+  g.K = d;
+  g.n_mt = F / TILE_M;
+  g.ksplit = 1;
+  g.out = h;
+  g.out_ld = F;
+  g.out_split_stride = 0;
+  if (launch_grouped_gemm(fmt, true, mx, g, plan_gemm(fmt, true, bn, n_groups), grid, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (ev_mid && cudaEventRecord(ev_mid, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  GemmArgs dn = a;   // down, K-split fp32 partial sums
+  dn.sec_off = gateup_section_bytes(fmt, d, F);
+  dn.K = F;
+  dn.n_mt = d / TILE_M;
+  dn.ksplit = ksplit;
+  dn.out = part;
+  dn.out_ld = d;
+  dn.out_split_stride = (unsigned long long)rows * d;
+  if (launch_grouped_gemm(fmt, false, mh, dn, plan_gemm(fmt, false, bn, n_groups), grid, s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (ev_down && cudaEventRecord(ev_down, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status check_route_args(const float* logits, int T, int E, int k, const void* idx,
+                            const void* w) {
+  if (!logits || !idx || !w) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  if (E > MAX_E || k > MAX_K || (long)T * k > MAX_A) return MOE_ERR_UNSUPPORTED;
+  if (!al16(logits) || !al16(idx) || !al16(w)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int k,
+                              const moe_pool* routed, const moe_pool* shared, uint16_t* out,
+                              void* ws, size_t ws_bytes, cudaStream_t s, void* const* ev) {
+  moe_status st = check_pool(routed, false);
+  if (st != MOE_OK) return st;
+  if (shared) {
+    if ((st = check_pool(shared, true)) != MOE_OK) return st;
+    if (shared->d_model != routed->d_model || shared->d_ff != routed->d_ff ||
+        shared->fmt != routed->fmt)
+      return MOE_ERR_UNSUPPORTED;
+  }
+  if (!x || !logits || !out || !ws) return MOE_ERR_INVALID_ARG;
+  const int E = routed->n_experts;
+  if (T < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  if (k > MAX_K || (long)T * k > MAX_A) return MOE_ERR_UNSUPPORTED;
+  if (!al16(x) || !al16(logits) || !al16(out) || !al256(ws)) return MOE_ERR_INVALID_ARG;
+  const LayerLayout L = layer_layout(T, k, routed, shared);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  uint8_t* W = (uint8_t*)ws;
+  int* err = (int*)(W + L.err);
+  int32_t* idx = (int32_t*)(W + L.idx);
+  float* w = (float*)(W + L.w);
+  int32_t* counts = (int32_t*)(W + L.counts);
+  int32_t* offsets = (int32_t*)(W + L.offsets);
+  int32_t* roa = (int32_t*)(W + L.roa);
+  int32_t* tor = (int32_t*)(W + L.tor);
+  uint16_t* xperm = (uint16_t*)(W + L.xperm);
+  uint16_t* h = (uint16_t*)(W + L.h);
+  float* part = (float*)(W + L.part);
+  auto rec = [&](int i) -> bool {
+    return !ev || !ev[i] || cudaEventRecord((cudaEvent_t)ev[i], s) == cudaSuccess;
+  };
+
+  if (!rec(MOE_STAGE_ROUTE)) return MOE_ERR_CUDA;
+  if (launch_route_topk(logits, T, E, k, idx, w, nullptr, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!rec(MOE_STAGE_PERMUTE)) return MOE_ERR_CUDA;
+  if (launch_permute_index(idx, T, k, E, L.Tsh, counts, offsets, roa, tor, err, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!rec(MOE_STAGE_GATHER)) return MOE_ERR_CUDA;
+  if (launch_gather_rows(x, tor, L.rows, T, L.d, xperm, sm_count(), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!rec(MOE_STAGE_GATE_UP)) return MOE_ERR_CUDA;
+  st = run_ffn(xperm, offsets, E + (shared ? 1 : 0), L.rows, routed, shared, L.bn, L.ksplit, h, part,
+               err, s, ev ? (cudaEvent_t)ev[MOE_STAGE_DOWN] : nullptr,
+               ev ? (cudaEvent_t)ev[MOE_STAGE_COMBINE] : nullptr);
+  if (st != MOE_OK) return st;
+  if (launch_combine_partials(part, L.ksplit, (size_t)L.rows * L.d, roa, w, T, k, L.d,
+                              shared ? L.A : -1, out, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!rec(MOE_N_STAGES)) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+
+// ===================================================================== C ABI
+extern "C" {
+
+const char* moe_status_str(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size or format";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA launch failed";
+    case MOE_ERR_DEVICE: return "device-side error code set";
+    default: return "unknown status";
+  }
+}
+
+size_t moe_slot_bytes(int fmt, int d_model, int d_ff) {
+  if ((fmt != MOE_W_BF16 && fmt != MOE_W_INT4_G128) || d_model < 128 || d_ff < 128 ||
+      d_model % 128 || d_ff % 128)
+    return 0;
+  return gateup_section_bytes(fmt, d_model, d_ff) + down_section_bytes(fmt, d_model, d_ff);
+}
+
+moe_status moe_prepack_expert(int fmt, int d_model, int d_ff, const moe_expert_src* src,
+                              void* slot_dst, moe_stream_t stream) {
+  if (!src || !slot_dst || moe_slot_bytes(fmt, d_model, d_ff) == 0) return MOE_ERR_INVALID_ARG;
+  if (d_model > MAX_DIM || d_ff > MAX_DIM) return MOE_ERR_UNSUPPORTED;
+  if (!al256(slot_dst)) return MOE_ERR_INVALID_ARG;
+  for (int m = 0; m < 3; ++m) {
+    if (!src->w[m] || !al16(src->w[m])) return MOE_ERR_INVALID_ARG;
+    if (fmt == MOE_W_INT4_G128 && (!src->scale[m] || !src->zero[m])) return MOE_ERR_INVALID_ARG;
+  }
+  return launch_prepack(fmt, d_model, d_ff, *src, (uint8_t*)slot_dst, (cudaStream_t)stream) ==
+                 cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                          float* topk_w, moe_stream_t stream) {
+  const moe_status st = check_route_args(logits, T, E, k, topk_idx, topk_w);
+  if (st != MOE_OK) return st;
+  return launch_route_topk(logits, T, E, k, topk_idx, topk_w, nullptr, (cudaStream_t)stream) ==
+                 cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+size_t moe_permute_workspace_bytes(void) { return 1024; }
+
+moe_status moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int k, int E, int d,
+                       int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
+                       int32_t* token_of_row, uint16_t* x_perm, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+  if (!topk_idx || !x || !counts || !offsets || !row_of_assign || !token_of_row || !x_perm || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (T < 1 || E < 1 || k < 1 || k > E || d < 128 || d % 128) return MOE_ERR_INVALID_ARG;
+  if (E > MAX_E || k > MAX_K || (long)T * k > MAX_A || d > MAX_DIM) return MOE_ERR_UNSUPPORTED;
+  if (!al16(topk_idx) || !al16(x) || !al16(x_perm) || !al256(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_permute_workspace_bytes()) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  int* err = (int*)ws;
+  if (launch_permute_index(topk_idx, T, k, E, 0, counts, offsets, row_of_assign, token_of_row, err,
+                           s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_gather_rows(x, token_of_row, T * k, T, d, x_perm, sm_count(), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+size_t moe_grouped_ffn_workspace_bytes(int A, const moe_pool* pool) {
+  if (A < 1 || check_pool(pool, false) != MOE_OK) return 0;
+  const int bn = choose_bn(A, pool->n_experts);
+  const int ks = choose_ksplit(A, pool->n_experts, false, bn, pool->d_model / TILE_M, pool->d_ff);
+  return 1024 + up1k((size_t)A * pool->d_ff * 2) + up1k((size_t)ks * A * pool->d_model * 4);
+}
+
+moe_status moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int A,
+                           const moe_pool* pool, uint16_t* y_perm, void* ws, size_t ws_bytes,
+                           moe_stream_t stream) {
+  moe_status st = check_pool(pool, false);
+  if (st != MOE_OK) return st;
+  if (!x_perm || !offsets || !y_perm || !ws || A < 1) return MOE_ERR_INVALID_ARG;
+  if (A > MAX_A) return MOE_ERR_UNSUPPORTED;
+  if (!al16(x_perm) || !al16(offsets) || !al16(y_perm) || !al256(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_grouped_ffn_workspace_bytes(A, pool)) return MOE_ERR_WORKSPACE;
+  const int bn = choose_bn(A, pool->n_experts);
+  const int ks = choose_ksplit(A, pool->n_experts, false, bn, pool->d_model / TILE_M, pool->d_ff);
+  uint8_t* W = (uint8_t*)ws;
+  int* err = (int*)W;
+  uint16_t* h = (uint16_t*)(W + 1024);
+  float* part = (float*)(W + 1024 + up1k((size_t)A * pool->d_ff * 2));
+  cudaStream_t s = (cudaStream_t)stream;
+  if (launch_clear_word(err, s) != cudaSuccess) return MOE_ERR_CUDA;
+  st = run_ffn(x_perm, offsets, pool->n_experts, A, pool, nullptr, bn, ks, h, part, err, s, nullptr,
+               nullptr);
+  if (st != MOE_OK) return st;
+  return launch_reduce_splits(part, ks, (size_t)A * pool->d_model, A, pool->d_model, y_perm, s) ==
+                 cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+moe_status moe_combine(const uint16_t* y_perm, const int32_t* row_of_assign, const float* topk_w,
+                       const uint16_t* shared_y, int T, int k, int d, uint16_t* out,
+                       moe_stream_t stream) {
+  if (!y_perm || !row_of_assign || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || k < 1 || d < 128 || d % 128) return MOE_ERR_INVALID_ARG;
+  if (k > MAX_K || (long)T * k > MAX_A || d > MAX_DIM) return MOE_ERR_UNSUPPORTED;
+  if (!al16(y_perm) || !al16(out) || (shared_y && !al16(shared_y))) return MOE_ERR_INVALID_ARG;
+  return launch_combine_bf16(y_perm, row_of_assign, topk_w, shared_y, T, k, d, out,
+                             (cudaStream_t)stream) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+size_t moe_layer_workspace_bytes(int T, int k, const moe_pool* routed, const moe_pool* shared) {
+  if (T < 1 || k < 1 || check_pool(routed, false) != MOE_OK) return 0;
+  if (shared && check_pool(shared, true) != MOE_OK) return 0;
+  return layer_layout(T, k, routed, shared).total;
+}
+
+moe_status moe_layer_forward(const uint16_t* x, const float* logits, int T, int k,
+                             const moe_pool* routed, const moe_pool* shared, uint16_t* out,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return layer_forward_impl(x, logits, T, k, routed, shared, out, ws, ws_bytes,
+                            (cudaStream_t)stream, nullptr);
+}
+
+moe_status moe_layer_forward_timed(const uint16_t* x, const float* logits, int T, int k,
+                                   const moe_pool* routed, const moe_pool* shared, uint16_t* out,
+                                   void* ws, size_t ws_bytes, moe_stream_t stream,
+                                   void* const* stage_events) {
+  return layer_forward_impl(x, logits, T, k, routed, shared, out, ws, ws_bytes,
+                            (cudaStream_t)stream, stage_events);
+}
+
+int moe_layer_launch_count(int T, int k, const moe_pool* routed, const moe_pool* shared) {
+  if (moe_layer_workspace_bytes(T, k, routed, shared) == 0) return 0;
+  return 6;   // route, permute, gather, gate/up, down, combine
+}
+
+moe_status moe_last_device_error(const void* ws, int* code, moe_stream_t stream) {
+  if (!ws || !code) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  *code = v;
+  return v ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,147 @@
+// combine.cu -- weighted un-permute back to token order:
+//   out[t] = bf16( sum_{j<k} w[t][j] * y[row_of_assign[t*k+j]]  (+ y_shared[t]) )
+// summed in fp32 in the order j = 0..k-1, the always-on shared expert last
+// ("125B MoE on an RTX 3090 at 100+ tok/s": sec. 4.2 regroup and back, sec. 2.1
+// shared expert).  The expert outputs y are bf16 values: the partial-sum
+// variant rounds the sum of its fp32 K-split partials to bf16 first, exactly as
+// the bf16 y_perm of the standalone path would hold it.
+//
+// One CTA per (token, 1024-column slab); each thread owns 4 consecutive columns
+// (16-byte fp32 / 8-byte bf16 vectors).
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ float bf16_round(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ float4 load_bf16x4(const uint16_t* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  float4 r;
+  r.x = __uint_as_float(u.x << 16);
+  r.y = __uint_as_float(u.x & 0xFFFF0000u);
+  r.z = __uint_as_float(u.y << 16);
+  r.w = __uint_as_float(u.y & 0xFFFF0000u);
+  return r;
+}
+
+__device__ __forceinline__ void store_bf16x4(uint16_t* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// bf16(sum over K splits of the fp32 partial sums) of row r, columns [c, c+4)
+__device__ __forceinline__ float4 y_from_partials(const float* part, int n_split,
+                                                  size_t split_stride, int r, int d, int c) {
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = 0; i < n_split; ++i) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(part + i * split_stride + (size_t)r * d + c));
+    s.x += v.x;
+    s.y += v.y;
+    s.z += v.z;
+    s.w += v.w;
+  }
+  return make_float4(bf16_round(s.x), bf16_round(s.y), bf16_round(s.z), bf16_round(s.w));
+}
+
+__global__ void __launch_bounds__(256)
+    combine_partials_kernel(const float* __restrict__ part, int n_split, size_t split_stride,
+                            const int32_t* __restrict__ row_of_assign,
+                            const float* __restrict__ topk_w, int k, int d, int shared_row0,
+                            uint16_t* __restrict__ out) {
+  const int t = blockIdx.x;
+  const int c = (blockIdx.y * 256 + threadIdx.x) * 4;
+  if (c >= d) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < k; ++j) {
+    const int r = row_of_assign[t * k + j];
+    if (r < 0) continue;   // only after an index error
+    const float w = topk_w[t * k + j];
+    const float4 y = y_from_partials(part, n_split, split_stride, r, d, c);
+    acc.x += w * y.x;
+    acc.y += w * y.y;
+    acc.z += w * y.z;
+    acc.w += w * y.w;
+  }
+  if (shared_row0 >= 0) {
+    const float4 y = y_from_partials(part, n_split, split_stride, shared_row0 + t, d, c);
+    acc.x += y.x;
+    acc.y += y.y;
+    acc.z += y.z;
+    acc.w += y.w;
+  }
+  store_bf16x4(out + (size_t)t * d + c, acc);
+}
+
+__global__ void __launch_bounds__(256)
+    combine_bf16_kernel(const uint16_t* __restrict__ y_perm, const int32_t* __restrict__ row_of_assign,
+                        const float* __restrict__ topk_w, const uint16_t* __restrict__ shared_y,
+                        int k, int d, uint16_t* __restrict__ out) {
+  const int t = blockIdx.x;
+  const int c = (blockIdx.y * 256 + threadIdx.x) * 4;
+  if (c >= d) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < k; ++j) {
+    const int r = row_of_assign[t * k + j];
+    if (r < 0) continue;
+    const float w = topk_w[t * k + j];
+    const float4 y = load_bf16x4(y_perm + (size_t)r * d + c);
+    acc.x += w * y.x;
+    acc.y += w * y.y;
+    acc.z += w * y.z;
+    acc.w += w * y.w;
+  }
+  if (shared_y != nullptr) {
+    const float4 y = load_bf16x4(shared_y + (size_t)t * d + c);
+    acc.x += y.x;
+    acc.y += y.y;
+    acc.z += y.z;
+    acc.w += y.w;
+  }
+  store_bf16x4(out + (size_t)t * d + c, acc);
+}
+
+__global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restrict__ part,
+                                                            int n_split, size_t split_stride,
+                                                            int d, uint16_t* __restrict__ y) {
+  const int r = blockIdx.x;
+  const int c = (blockIdx.y * 256 + threadIdx.x) * 4;
+  if (c >= d) return;
+  store_bf16x4(y + (size_t)r * d + c, y_from_partials(part, n_split, split_stride, r, d, c));
+}
+
+static dim3 grid_rows(int rows, int d) { return dim3((unsigned)rows, (unsigned)((d + 1023) / 1024)); }
+
+cudaError_t launch_combine_partials(const float* part, int n_split, size_t split_stride,
+                                    const int32_t* row_of_assign, const float* topk_w, int T,
+                                    int k, int d, int shared_row0, uint16_t* out, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  combine_partials_kernel<<<grid_rows(T, d), 256, 0, s>>>(part, n_split, split_stride,
+                                                          row_of_assign, topk_w, k, d,
+                                                          shared_row0, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bf16(const uint16_t* y_perm, const int32_t* row_of_assign,
+                                const float* topk_w, const uint16_t* shared_y, int T, int k, int d,
+                                uint16_t* out, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  combine_bf16_kernel<<<grid_rows(T, d), 256, 0, s>>>(y_perm, row_of_assign, topk_w, shared_y, k,
+                                                      d, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_splits(const float* part, int n_split, size_t split_stride, int rows,
+                                 int d, uint16_t* y, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  reduce_splits_kernel<<<grid_rows(rows, d), 256, 0, s>>>(part, n_split, split_stride, d, y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,104 @@
+// kernels.cuh -- internal declarations shared by the library's translation units:
+// the prepacked slot layout, the grouped-GEMM argument block, launch helpers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ slot layout
+// One expert slot = [gate/up section][down section].
+//   bf16: per (128-row tile mt, K step ks of 64) one block of NMAT x 16 KB; each
+//         16 KB is the 128 x 64 bf16 tile in the tensor core's 128-byte-swizzled
+//         K-major image (16-byte chunk j of row r at chunk j ^ (r % 8)).
+//         gate/up blocks hold gate then up for the same rows (NMAT = 2).
+//   int4: per (mt, quantisation group g of 128 K) one block of NMAT x 8704 B:
+//         8192 B of nibbles then 128 x (fp16 scale | fp16 zero << 16).  The
+//         nibbles of row r, half h (K 0-63 / 64-127 of the group), quad j
+//         (32 K each) form 16 bytes at ((h*2 + j)*128 + r)*16; each 32-bit word
+//         w of a quad covers K elements 8w..8w+7 with element 2i in bits
+//         [4i, 4i+4) and element 2i+1 in bits [16+4i, 20+4i).
+constexpr int TILE_M = 128;          // weight rows per MMA tile (the MMA's M)
+constexpr int KSTEP = 64;            // K elements per pipeline stage (one 128-byte row)
+constexpr int QGROUP = 128;          // int4 quantisation group
+constexpr int BF16_TILE_BYTES = TILE_M * KSTEP * 2;          // 16384
+constexpr int I4_PACKED_BYTES = TILE_M * QGROUP / 2;         // 8192
+constexpr int I4_MAT_BYTES = I4_PACKED_BYTES + TILE_M * 4;   // 8704
+
+__host__ __device__ inline size_t gateup_section_bytes(int fmt, int d, int F) {
+  return fmt == MOE_W_INT4_G128
+             ? (size_t)(F / TILE_M) * (d / QGROUP) * (2 * I4_MAT_BYTES)
+             : (size_t)(F / TILE_M) * (d / KSTEP) * (2 * BF16_TILE_BYTES);
+}
+__host__ __device__ inline size_t down_section_bytes(int fmt, int d, int F) {
+  return fmt == MOE_W_INT4_G128 ? (size_t)(d / TILE_M) * (F / QGROUP) * I4_MAT_BYTES
+                                : (size_t)(d / TILE_M) * (F / KSTEP) * BF16_TILE_BYTES;
+}
+
+// ------------------------------------------------------------------ grouped GEMM
+// Row group g (an expert, or the shared expert appended as the last group) owns
+// B-operand rows [offsets[g], offsets[g+1]).  Work items are
+// (group, 128-row output tile, K split, row chunk of <= bn rows).
+struct GemmArgs {
+  const int32_t* offsets;               // [n_groups + 1]
+  int n_groups;                         // groups (routed experts, + 1 shared)
+  int n_routed;                         // groups [0, n_routed) use the routed table
+  const uint8_t* pool_r;                // routed pool
+  unsigned long long slot_bytes_r;
+  const int32_t* e2s_r;                 // routed expert -> slot
+  int n_slots_r;
+  const uint8_t* pool_s;                // shared-expert pool view (group n_routed)
+  unsigned long long slot_bytes_s;
+  const int32_t* e2s_s;
+  int n_slots_s;
+  unsigned long long sec_off;           // byte offset of this GEMM's section in a slot
+  int K;                                // reduction length, multiple of 128
+  int n_mt;                             // 128-row output tiles
+  int ksplit;                           // K splits (whole quantisation groups each)
+  int bn;                               // max rows per item = B tile rows (16..256, % 16 == 0)
+  int rows_total;                       // rows of the B operand
+  void* out;                            // gate/up: bf16 h; down: fp32 partials
+  int out_ld;                           // elements per output row
+  unsigned long long out_split_stride;  // elements between K-split partial buffers
+  int* err;                             // device error word
+  int n_a, n_b, n_raw;                  // pipeline depths
+  uint32_t tmem_cols;                   // TMEM columns (power of two >= 32)
+};
+
+struct GemmPlan {
+  int ndq;            // dequant / epilogue warps
+  int n_a, n_b, n_raw;
+  size_t smem_bytes;
+  uint32_t tmem_cols;
+};
+
+GemmPlan plan_gemm(int fmt, bool gateup, int bn, int n_groups);
+cudaError_t launch_grouped_gemm(int fmt, bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
+                                const GemmPlan& plan, int grid, cudaStream_t stream);
+
+// ------------------------------------------------------------------ other kernels
+// err_clear (nullable): error word zeroed by the first thread (first launch of a forward).
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+                              int* err_clear, cudaStream_t s);
+cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_shared,
+                                 int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
+                                 int32_t* token_of_row, int* err, cudaStream_t s);
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
+                               int d, uint16_t* x_perm, int n_sm, cudaStream_t s);
+cudaError_t launch_combine_partials(const float* part, int n_split, size_t split_stride,
+                                    const int32_t* row_of_assign, const float* topk_w, int T,
+                                    int k, int d, int shared_row0, uint16_t* out, cudaStream_t s);
+cudaError_t launch_combine_bf16(const uint16_t* y_perm, const int32_t* row_of_assign,
+                                const float* topk_w, const uint16_t* shared_y, int T, int k, int d,
+                                uint16_t* out, cudaStream_t s);
+cudaError_t launch_reduce_splits(const float* part, int n_split, size_t split_stride, int rows,
+                                 int d, uint16_t* y, cudaStream_t s);
+cudaError_t launch_clear_word(int* p, cudaStream_t s);
+cudaError_t launch_prepack(int fmt, int d, int F, const moe_expert_src& src, uint8_t* dst,
+                           cudaStream_t s);
+
+}  // namespace moe

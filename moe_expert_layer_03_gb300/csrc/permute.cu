@@ -1,0 +1,161 @@
+// permute.cu -- regroup the token->expert assignments so every expert's rows are
+// contiguous ("125B MoE on an RTX 3090 at 100+ tok/s", sec. 4.2: after routing,
+// tokens are reordered by expert id so one grouped GEMM serves each expert).
+//
+// permute_index_kernel (one CTA of 1024 threads):
+//   1. histogram of the A = T*k expert ids (shared-memory atomics),
+//   2. exclusive scan -> offsets,
+//   3. stable scatter: tiles of 1024 assignments in order; inside a warp the
+//      lanes with the same expert find each other with __match_any_sync and
+//      take their rank from the lanes below them; across warps a per-warp
+//      count table gives each warp its base.  The row of assignment a is
+//      offsets[e] + (number of earlier assignments with expert e) -- unique, so
+//      the result is independent of scheduling.
+// gather_rows_kernel: x_perm[r] = x[token_of_row[r]], one warp per row, 16-byte
+//   vector loads and stores.
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+constexpr int PERM_THREADS = 1024;
+constexpr int PERM_WARPS = PERM_THREADS / 32;
+constexpr int PERM_MAX_E = 256;
+
+__global__ void __launch_bounds__(PERM_THREADS, 1)
+    permute_index_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int t_shared,
+                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                         int32_t* __restrict__ row_of_assign, int32_t* __restrict__ token_of_row,
+                         int* __restrict__ err) {
+  __shared__ int s_cnt[PERM_MAX_E];
+  __shared__ int s_base[PERM_MAX_E];
+  __shared__ int s_wc[PERM_WARPS][PERM_MAX_E];
+  __shared__ int s_total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int A = T * k;
+
+  // first kernel of the pipeline that reports device errors: clear the word
+  if (tid == 0) *err = 0;
+  for (int e = tid; e < E; e += PERM_THREADS) s_cnt[e] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int a = tid; a < A; a += PERM_THREADS) {
+    const int e = idx[a];
+    if (e < 0 || e >= E)
+      bad = true;
+    else
+      atomicAdd(&s_cnt[e], 1);
+  }
+  if (bad) atomicOr(err, MOE_DEVERR_EXPERT_RANGE);
+  __syncthreads();
+
+  // exclusive scan by warp 0: lane l owns experts [8l, 8l+8)
+  if (warp == 0) {
+    int local[8];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      local[i] = e < E ? s_cnt[e] : 0;
+      sum += local[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      if (e < E) {
+        s_base[e] = run;
+        counts[e] = local[i];
+        offsets[e] = run;
+      }
+      run += local[i];
+    }
+    if (lane == 31) {
+      s_total = incl;
+      offsets[E] = incl;
+      if (t_shared > 0) offsets[E + 1] = incl + t_shared;
+    }
+  }
+  __syncthreads();
+
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = 0; base < A; base += PERM_THREADS) {
+    for (int i = tid; i < PERM_WARPS * E; i += PERM_THREADS) s_wc[i / E][i % E] = 0;
+    __syncthreads();
+    const int a = base + tid;
+    int e = a < A ? idx[a] : -1;
+    const bool valid = (e >= 0 && e < E);
+    if (!valid) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    if (valid && rank == 0) s_wc[warp][e] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      int r = s_base[e] + rank;
+      for (int w = 0; w < warp; ++w) r += s_wc[w][e];
+      row_of_assign[a] = r;
+      token_of_row[r] = a / k;
+    } else if (a < A) {
+      row_of_assign[a] = -1;
+    }
+    __syncthreads();
+    for (int ee = tid; ee < E; ee += PERM_THREADS) {
+      int s = 0;
+      for (int w = 0; w < PERM_WARPS; ++w) s += s_wc[w][ee];
+      s_base[ee] += s;
+    }
+    __syncthreads();
+  }
+  // rows of the always-on shared expert follow the routed rows, in token order
+  for (int t = tid; t < t_shared; t += PERM_THREADS) token_of_row[s_total + t] = t;
+}
+
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ token_of_row,
+                                                          int rows, int T, int d,
+                                                          uint16_t* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31;
+  const int nvec = d / 8;   // 16-byte vectors per row
+  for (int r = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); r < rows;
+       r += (int)((gridDim.x * blockDim.x) >> 5)) {
+    const int t = token_of_row[r];
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * d);
+    if (t < 0 || t >= T) {   // only after an index error: keep the row defined
+      for (int i = lane; i < nvec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    for (int i = lane; i < nvec; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
+cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_shared,
+                                 int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
+                                 int32_t* token_of_row, int* err, cudaStream_t s) {
+  permute_index_kernel<<<1, PERM_THREADS, 0, s>>>(idx, T, k, E, t_shared, counts, offsets,
+                                                  row_of_assign, token_of_row, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
+                               int d, uint16_t* x_perm, int n_sm, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  int blocks = (rows + 7) / 8;   // 8 warps (rows) per block
+  if (blocks > 4 * n_sm) blocks = 4 * n_sm;
+  gather_rows_kernel<<<blocks, 256, 0, s>>>(x, token_of_row, rows, T, d, x_perm);
+  return cudaGetLastError();
+}
+
+__global__ void clear_word_kernel(int* p) { *p = 0; }
+cudaError_t launch_clear_word(int* p, cudaStream_t s) {
+  clear_word_kernel<<<1, 1, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,72 @@
+"""Builds one synthetic MoE layer on the GPU (through the library's C ABI) and the
+matching CPU-oracle description of the same seeded inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import moe_expert_layer_03_gb300 as moe
+import moe_synth as ms
+import oracle
+
+TOL = 2e-2   # max|err| <= TOL * RMS(out) for bf16 activations with fp32 accumulation
+
+
+class GpuLayer:
+    def __init__(self, cfg: ms.LayerConfig, device="cuda", logits: np.ndarray | None = None,
+                 e2s: np.ndarray | None = None):
+        self.cfg = cfg
+        self.dev = device
+        self.x = ms.make_x(cfg).to(device)
+        self.logits_np = ms.make_logits(cfg) if logits is None else logits
+        self.logits = torch.from_numpy(self.logits_np).to(device)
+        self.e2s_np = ms.make_slot_table(cfg) if e2s is None else e2s
+        n_slots = cfg.E + (1 if cfg.shared else 0)
+        self.pool = moe.ExpertPool(n_slots, cfg.d, cfg.F, cfg.fmt, device=device)
+        self.weights = {}
+        for e in range(cfg.E):
+            self.weights[e] = ms.expert_weights(cfg, e, device)
+            self.pool.load_expert(int(self.e2s_np[e]), self.weights[e])
+        self.routed = self.pool.view(torch.from_numpy(self.e2s_np.astype(np.int32)).to(device))
+        self.shared = None
+        if cfg.shared:
+            self.weights["shared"] = ms.expert_weights(cfg, "shared", device)
+            self.pool.load_expert(cfg.E, self.weights["shared"])
+            self.shared = self.pool.view(torch.tensor([cfg.E], dtype=torch.int32, device=device))
+        self._refs = {}
+
+    def ref(self, e) -> oracle.ExpertRef:
+        if e not in self._refs:
+            w = self.weights[e]
+            self._refs[e] = oracle.ExpertRef({m: {k: v.cpu() for k, v in w[m].items()} for m in w},
+                                             self.cfg.fmt)
+        return self._refs[e]
+
+    def forward(self, **kw):
+        out, ws = moe.layer_forward(self.x, self.logits, self.cfg.k, self.routed, self.shared, **kw)
+        torch.cuda.synchronize()
+        return out, ws
+
+    def oracle_forward(self, tokens=None):
+        """Oracle output rows (float32) for the listed tokens (all if None)."""
+        cfg = self.cfg
+        toks = list(range(cfg.T)) if tokens is None else list(tokens)
+        idx, _ = oracle.route_topk(self.logits_np[toks], cfg.k)
+        used = sorted(set(int(e) for e in idx.ravel()))
+        refs = [self.ref(used[0])] * cfg.E
+        for e in used:
+            refs[e] = self.ref(e)
+        sh = self.ref("shared") if cfg.shared else None
+        out, _, _ = oracle.layer_forward(self.x.cpu(), self.logits_np, cfg.k, refs, sh, cfg.d,
+                                         cfg.F, tokens=toks)
+        return oracle.bf16_bits_to_float(out)
+
+
+def assert_close_rms(got: np.ndarray, want: np.ndarray, tol: float = TOL, what: str = ""):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    rms = float(np.sqrt(np.mean(want ** 2)))
+    err = float(np.max(np.abs(got - want)))
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    assert err <= tol * rms, f"{what}: max|err| {err:.4e} > {tol} * RMS {rms:.4e}"
+    return err, rms

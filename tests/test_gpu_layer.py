@@ -1,0 +1,143 @@
+"""GPU parity: the grouped SwiGLU FFN, the combine and the whole layer against the
+oracle, within max|err| <= 2e-2 * RMS(out) (bf16 activations, fp32 accumulation).
+
+Small cases run the oracle on every token; the five workload shapes run at full
+size in the bench's launch configuration and compare a sample of tokens."""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_03_gb300 as moe
+import moe_synth as ms
+import oracle
+from layer_setup import GpuLayer, assert_close_rms
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "tiny": ms.CONFIGS["tiny"],
+    "tiny_int4": ms.CONFIGS["tiny"].with_(name="tiny_int4", fmt="int4"),
+    "int4_shared_perm": ms.LayerConfig("int4_shared_perm", T=24, d=384, F=256, E=16, k=4,
+                                       fmt="int4", logits="zipf", zipf_s=1.1, shared=True,
+                                       slot_perm=True),
+    "bf16_multichunk": ms.LayerConfig("bf16_multichunk", T=600, d=256, F=384, E=2, k=1,
+                                      fmt="bf16", seed=3),                 # >256 rows per expert
+    "int4_ragged": ms.LayerConfig("int4_ragged", T=37, d=256, F=640, E=5, k=3, fmt="int4",
+                                  seed=5),                                 # T, F not tile multiples
+    "k_equals_E": ms.LayerConfig("k_equals_E", T=9, d=128, F=128, E=4, k=4, fmt="bf16", seed=2),
+    "single_token": ms.LayerConfig("single_token", T=1, d=256, F=256, E=8, k=2, fmt="int4"),
+    "dense_E1": ms.LayerConfig("dense_E1", T=20, d=256, F=512, E=1, k=1, fmt="int4"),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_layer_small_all_tokens(name):
+    L = GpuLayer(SMALL[name])
+    out, ws = L.forward()
+    assert moe.last_device_error(ws) == 0
+    assert_close_rms(out.float().cpu().numpy(), L.oracle_forward(), what=name)
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_int4", "int4_ragged", "bf16_multichunk"])
+def test_grouped_ffn_and_combine_entry_points(name):
+    """route -> permute -> grouped_ffn -> combine through the separate ABI calls."""
+    L = GpuLayer(SMALL[name])
+    cfg = L.cfg
+    idx, w = moe.route_topk(L.logits, cfg.k)
+    perm = moe.permute(idx, L.x, cfg.E)
+    y_perm, ws = moe.grouped_ffn(perm["x_perm"], perm["offsets"], L.routed)
+    out = moe.combine(y_perm, perm["row_of_assign"], w)
+    torch.cuda.synchronize()
+    assert moe.last_device_error(ws) == 0
+    # y_perm row by row against the oracle's expert FFN of that row's expert
+    tor = perm["token_of_row"].cpu().numpy()
+    offs = perm["offsets"].cpu().numpy()
+    yp = y_perm.float().cpu().numpy()
+    rows = np.linspace(0, cfg.A - 1, min(cfg.A, 24)).astype(int)
+    for r in rows:
+        e = int(np.searchsorted(offs, r, side="right") - 1)
+        _, y = oracle.expert_ffn(L.x[tor[r]].cpu(), L.ref(e), cfg.d, cfg.F)
+        assert_close_rms(yp[r], oracle.bf16_bits_to_float(y), what=f"{name} row {r}")
+    assert_close_rms(out.float().cpu().numpy(), L.oracle_forward(), what=name)
+
+
+def test_combine_with_shared_rows():
+    T, k, d = 5, 3, 256
+    y = torch.randn(T * k, d, device="cuda").to(torch.bfloat16)
+    sh = torch.randn(T, d, device="cuda").to(torch.bfloat16)
+    roa = torch.randperm(T * k, device="cuda").to(torch.int32)
+    w = torch.softmax(torch.randn(T, k, device="cuda"), dim=1)
+    out = moe.combine(y, roa, w, sh).float().cpu().numpy()
+    yc, shc, roac, wc = y.cpu(), sh.cpu(), roa.cpu().numpy(), w.cpu().numpy()
+    for t in range(T):
+        bits = [yc[roac[t * k + j]].view(torch.int16).numpy().view(np.uint16) for j in range(k)]
+        want = oracle.combine_row(bits, wc[t], shc[t].view(torch.int16).numpy().view(np.uint16))
+        assert_close_rms(out[t], oracle.bf16_bits_to_float(want), tol=1e-2, what=f"token {t}")
+
+
+@pytest.mark.parametrize("name", ["mixtral_decode", "phi35_prefill", "fg125b_decode",
+                                  "mixtral_prefill"])
+def test_layer_full_size_sampled(name):
+    cfg = ms.CONFIGS[name]
+    L = GpuLayer(cfg)
+    out, ws = L.forward()
+    assert moe.last_device_error(ws) == 0
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    toks = sorted({0, cfg.T - 1, cfg.T // 2})[: 2 if cfg.d * cfg.F > 30e6 else 3]
+    assert_close_rms(got[toks], L.oracle_forward(toks), what=name)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "int4"])
+def test_one_expert_takes_every_token(fmt):
+    """50 tokens on expert 0 of 16 (B tile of 16 rows -> 4 row chunks), 15 experts idle."""
+    cfg = ms.LayerConfig("skew", T=50, d=256, F=256, E=16, k=1, fmt=fmt, seed=9)
+    lg = ms.make_logits(cfg)
+    lg[:, 0] = 10.0
+    L = GpuLayer(cfg, logits=lg)
+    out, ws = L.forward()
+    assert moe.last_device_error(ws) == 0
+    assert_close_rms(out.float().cpu().numpy(), L.oracle_forward(), what="skew")
+
+
+def test_slot_permutation_is_bit_identical():
+    cfg = SMALL["int4_shared_perm"]
+    a = GpuLayer(cfg)
+    out_a, _ = a.forward()
+    b = GpuLayer(cfg, e2s=np.roll(a.e2s_np, 5))
+    out_b, _ = b.forward()
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+
+
+def test_token_permutation_permutes_rows():
+    cfg = SMALL["int4_ragged"]
+    a = GpuLayer(cfg)
+    out_a, _ = a.forward()
+    perm = np.random.default_rng(1).permutation(cfg.T)
+    b = GpuLayer(cfg, logits=a.logits_np[perm])
+    b.x = a.x[torch.from_numpy(perm).to("cuda")].contiguous()
+    out_b, _ = b.forward()
+    assert torch.equal(out_b.view(torch.int16), out_a[torch.from_numpy(perm).to("cuda")].view(torch.int16))
+
+
+def test_slot_out_of_range_sets_device_error():
+    cfg = SMALL["tiny_int4"]
+    L = GpuLayer(cfg)
+    bad = L.pool.view(torch.tensor([0, 1, 2, 3, 4, 5, 6, 99], dtype=torch.int32, device="cuda"))
+    out, ws = moe.layer_forward(L.x, L.logits, cfg.k, bad)
+    assert moe.last_device_error(ws) & 4
+    out, ws = L.forward()                     # the context is still usable afterwards
+    assert moe.last_device_error(ws) == 0
+
+
+def test_host_side_rejections():
+    cfg = SMALL["tiny"]
+    L = GpuLayer(cfg)
+    need = moe.layer_workspace_bytes(cfg.T, cfg.k, L.routed)
+    with pytest.raises(moe.MoeError, match="workspace"):
+        moe.layer_forward(L.x, L.logits, cfg.k, L.routed, ws=moe.workspace(need - 1024))
+    with pytest.raises(moe.MoeError, match="invalid"):
+        moe.layer_forward(L.x, L.logits, cfg.E + 1, L.routed)
+    xs = torch.empty(cfg.T * cfg.d + 8, dtype=torch.bfloat16, device="cuda")[1:1 + cfg.T * cfg.d]
+    with pytest.raises(moe.MoeError, match="invalid"):
+        moe.layer_forward(xs.view(cfg.T, cfg.d), L.logits, cfg.k, L.routed)
