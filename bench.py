@@ -1,0 +1,402 @@
+"""Benchmark of the MoE FFN layer forward on GB300: tokens/s per layer.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
+
+A step is one pass of the whole layer (route -> permute -> gather -> gate/up
+GEMM + SwiGLU -> down GEMM -> combine) over one batch of seeded synthetic
+tokens.  The default workload is the Mixtral-8x7B-shaped decode layer (T=16,
+d_model=4096, d_ff=14336, E=8, top-2, int4 group-128 weights).  Prints one JSON
+line (rank 0).
+
+--impl ours       the CUDA library (inputs resident in HBM for `value`; `e2e`
+                  adds the pinned host<->device copies of x, logits and out).
+--impl reference  the CPU oracle (test infrastructure) on the host cores, one
+                  thread per token slice (the C oracle releases the GIL), on the
+                  same workload; no GPU work.
+N > 1 (torchrun): independent replicas, one per GPU, no data-path collective
+("scaling": "weak"); a barrier brackets the timed region and the max time over
+ranks is used.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import moe_synth as ms  # noqa: E402
+
+STAGES = ("route", "permute", "gather", "gate_up", "down", "combine")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="mixtral_decode", choices=list(ms.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=4)
+    return ap.parse_args()
+
+
+def describe(cfg: ms.LayerConfig) -> dict:
+    w = {"bf16": "bf16", "int4": "int4 asymmetric group-128 (fp16 scale + zero)"}[cfg.fmt]
+    route = {"normal": "i.i.d. N(0,1) logits", "zipf": f"Zipf(s={cfg.zipf_s}) routing",
+             "reuse": f"{int(cfg.reuse_p * 100)}% of tokens reuse the previous token's experts"}[cfg.logits]
+    return {"workload": f"{cfg.name}: MoE FFN layer forward, T={cfg.T}, d_model={cfg.d}, "
+                        f"d_ff={cfg.F}, E={cfg.E}, top-{cfg.k}, SwiGLU, {w} weights, {route}"
+                        + (", + 1 shared expert" if cfg.shared else ""),
+            "T": cfg.T, "d_model": cfg.d, "d_ff": cfg.F, "experts": cfg.E, "top_k": cfg.k,
+            "weights": cfg.fmt, "shared_expert": cfg.shared}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_init(n: int):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(mx)) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def oracle_refs(cfg, weights_cpu: dict):
+    import oracle
+    refs = {e: oracle.ExpertRef(w, cfg.fmt) for e, w in weights_cpu.items()}
+    return refs
+
+
+def time_oracle(cfg, x_cpu, logits_np, refs: dict, tokens: list[int], threads: int) -> float:
+    """Wall time of the oracle forward of `tokens`, split over `threads` threads."""
+    import oracle
+    first = next(iter(refs))
+    ex = [refs.get(e, refs[first]) for e in range(cfg.E)]
+    sh = refs.get("shared")
+    chunks = [tokens[i::threads] for i in range(threads) if tokens[i::threads]]
+
+    def run(ch):
+        return oracle.layer_forward(x_cpu, logits_np, cfg.k, ex, sh, cfg.d, cfg.F, tokens=ch)
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=len(chunks)) as pool:
+        list(pool.map(run, chunks))
+    return time.perf_counter() - t0
+
+
+def needed_experts(cfg, logits_np, tokens) -> list[int]:
+    top = np.argsort(-logits_np[tokens], axis=1, kind="stable")[:, :cfg.k]
+    return sorted(set(int(e) for e in top.ravel()))
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, cfg):
+    rank, world, _ = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), 0
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    x = ms.make_x(cfg)
+    lg = ms.make_logits(cfg)
+    toks = list(range(cfg.T))
+    used = needed_experts(cfg, lg, toks)
+    w = {e: ms.expert_weights(cfg, e, "cpu") for e in used}
+    if cfg.shared:
+        w["shared"] = ms.expert_weights(cfg, "shared", "cpu")
+    refs = oracle_refs(cfg, w)
+    cores = os.cpu_count() or 1
+    threads = max(1, min(cfg.T, cores))
+    # one step = the whole layer on the T tokens; fewer tokens per step if a
+    # full step would keep the run beyond a few minutes
+    wave = time_oracle(cfg, x, lg, refs, toks[:threads], threads)   # `threads` tokens at once
+    runs = args.steps + args.warmup
+    waves = (cfg.T + threads - 1) // threads
+    budget = 240.0
+    if wave * waves * runs <= budget:
+        n_tok = cfg.T
+    else:
+        n_tok = max(1, min(cfg.T, threads * int(budget / (wave * runs))))
+    step_toks = toks[:n_tok]
+    for _ in range(args.warmup):
+        time_oracle(cfg, x, lg, refs, step_toks, min(threads, n_tok))
+    total = 0.0
+    for _ in range(args.steps):
+        total += time_oracle(cfg, x, lg, refs, step_toks, min(threads, n_tok))
+    value = n_tok * args.steps / total
+    line = {
+        "impl": "reference", "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": describe(cfg),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(threads, n_tok),
+                         "kind": "oracle",
+                         "sample": f"{n_tok} of {cfg.T} tokens per step, all their experts, "
+                                   f"one host thread per token slice"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+def gateup_bytes(cfg, n_active: int, rows: int) -> int:
+    if cfg.fmt == "int4":
+        wb = 2 * (cfg.d * cfg.F // 2 + cfg.F * (cfg.d // 128) * 4)
+    else:
+        wb = 2 * cfg.d * cfg.F * 2
+    return n_active * wb + rows * cfg.d * 2 + rows * cfg.F * 2
+
+
+def layer_bytes(cfg, n_active: int) -> int:
+    return n_active * ms.active_expert_bytes(cfg) + cfg.T * cfg.d * 2 * 2 + cfg.T * cfg.E * 4
+
+
+def load_peaks() -> tuple[float, float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return float(j["hbm_gbs"]), float(j.get("bf16_tflops", 1900.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_traffic(key: str):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    j = json.load(open(p))
+    src = open(os.path.join(ROOT, "moe_expert_layer_03_gb300", "csrc", "gemm.cu"), "rb").read()
+    ent = j.get(key)
+    if not ent or ent.get("gemm_cu_sha256") != hashlib.sha256(src).hexdigest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def run_ours(args, cfg):
+    import moe_expert_layer_03_gb300 as moe
+    rank, world, local = dist_init(args.gpus)
+    moe.build()
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+
+    # ---- the layer, resident in HBM
+    x = ms.make_x(cfg).to(dev)
+    logits_np = ms.make_logits(cfg)
+    logits = torch.from_numpy(logits_np).to(dev)
+    e2s = ms.make_slot_table(cfg)
+    pool = moe.ExpertPool(cfg.E + (1 if cfg.shared else 0), cfg.d, cfg.F, cfg.fmt, device=dev)
+    toks_cpu = list(range(min(cfg.T, args.cpu_sample_tokens)))
+    need_cpu = set(needed_experts(cfg, logits_np, toks_cpu)) if rank == 0 and world == 1 else set()
+    weights_cpu = {}
+    for e in range(cfg.E):
+        w = ms.expert_weights(cfg, e, dev)
+        pool.load_expert(int(e2s[e]), w)
+        if e in need_cpu:
+            weights_cpu[e] = {m: {k: v.cpu() for k, v in w[m].items()} for m in w}
+        del w
+    routed = pool.view(torch.from_numpy(e2s).to(dev))
+    shared = None
+    if cfg.shared:
+        w = ms.expert_weights(cfg, "shared", dev)
+        pool.load_expert(cfg.E, w)
+        if need_cpu:
+            weights_cpu["shared"] = {m: {k: v.cpu() for k, v in w[m].items()} for m in w}
+        shared = pool.view(torch.tensor([cfg.E], dtype=torch.int32, device=dev))
+        del w
+    torch.cuda.synchronize()
+    n_active = len(set(needed_experts(cfg, logits_np, list(range(cfg.T))))) + (1 if cfg.shared else 0)
+
+    out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
+    ws = moe.workspace(moe.layer_workspace_bytes(cfg.T, cfg.k, routed, shared), dev)
+    launches = moe.layer_launch_count(cfg.T, cfg.k, routed, shared)
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+          for _ in range(args.steps)]
+
+    # ---- warm-up and correctness guard (device error word)
+    for _ in range(max(args.warmup, 3)):
+        moe.layer_forward(x, logits, cfg.k, routed, shared, out=out, ws=ws)
+    torch.cuda.synchronize()
+    code = moe.last_device_error(ws)
+    if code:
+        raise SystemExit(f"device error code {code} during warm-up")
+
+    # ---- timed region: K steps, per-stage events on the launching stream
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        moe.layer_forward(x, logits, cfg.k, routed, shared, out=out, ws=ws, events=ev[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = clk.stop()
+    total_ms = max_over_ranks(start.elapsed_time(stop), world)
+    stage_ms = {s: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)]))
+                for j, s in enumerate(STAGES)}
+    if moe.last_device_error(ws):
+        raise SystemExit("device error during the timed region")
+
+    # ---- end to end through the public API: pinned host in, pinned host out
+    x_h = x.cpu().pin_memory()
+    lg_h = logits.cpu().pin_memory()
+    out_h = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    x_d, lg_d = torch.empty_like(x), torch.empty_like(logits)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        moe.layer_forward(x_d, lg_d, cfg.k, routed, shared, out=out, ws=ws)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+
+    ms_step = total_ms / args.steps
+    value = world * cfg.T * args.steps / (total_ms / 1e3)
+    hbm, tflops, peak_kind = load_peaks()
+    rows = cfg.A + (cfg.T if cfg.shared else 0)
+    gu_bytes = gateup_bytes(cfg, n_active, rows)
+    gu_gbs = gu_bytes / (stage_ms["gate_up"] / 1e3) / 1e9
+    lb = layer_bytes(cfg, n_active)
+    line = {
+        "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded), random-init weights of the configured shape",
+        "config": dict(describe(cfg), parallelism=f"replicas x{world}" if world > 1 else "single GPU",
+                       l2="inputs larger than L2: the active experts' weights streamed per step "
+                          f"({lb / 1e6:.0f} MB) exceed the 129 MB L2",
+                       active_experts=n_active),
+        "roofline": {"kernel": "grouped gate/up GEMM + SwiGLU (tcgen05, int4 dequant in the main loop)"
+                     if cfg.fmt == "int4" else "grouped gate/up GEMM + SwiGLU (tcgen05)",
+                     "bound": "hbm", "achieved": gu_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gu_gbs / hbm, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": gu_bytes,
+                     "traffic": kernel_traffic(cfg.name)},
+        "layer_roofline": {"bound": "hbm", "achieved": lb / (ms_step / 1e3) / 1e9, "peak": hbm,
+                           "unit": "GB/s", "frac": lb / (ms_step / 1e3) / 1e9 / hbm,
+                           "algorithmic_bytes_per_step": lb},
+        "stage_ms": stage_ms,
+        "e2e": {"value": world * cfg.T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
+                "d2h_bytes_per_step": out.numel() * 2},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        refs = oracle_refs(cfg, weights_cpu)
+        n = len(toks_cpu)
+        t = time_oracle(cfg, x.cpu(), logits_np, refs, toks_cpu, n)
+        line["cpu_baseline"] = {"value": n / t, "unit": "tokens/s", "cores": n, "kind": "oracle",
+                                "sample": f"{n} of {cfg.T} tokens (their {cfg.k} experts each, full "
+                                          f"d_model x d_ff), one host thread per token"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    cfg = ms.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

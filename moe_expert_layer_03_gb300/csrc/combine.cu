@@ -2,9 +2,9 @@
 //   out[t] = bf16( sum_{j<k} w[t][j] * y[row_of_assign[t*k+j]]  (+ y_shared[t]) )
 // summed in fp32 in the order j = 0..k-1, the always-on shared expert last
 // ("125B MoE on an RTX 3090 at 100+ tok/s": sec. 4.2 regroup and back, sec. 2.1
-// shared expert).  The expert outputs y are bf16 values: the partial-sum
-// variant rounds the sum of its fp32 K-split partials to bf16 first, exactly as
-// the bf16 y_perm of the standalone path would hold it.
+// shared expert).  The partial-sum variant (whole-layer path) adds the fp32
+// K-split partial sums of each expert output and uses them unrounded; the bf16
+// variant reads the bf16 y_perm of the standalone grouped-FFN entry point.
 //
 // One CTA per (token, 1024-column slab); each thread owns 4 consecutive columns
 // (16-byte fp32 / 8-byte bf16 vectors).
@@ -12,10 +12,6 @@
 #include "ptx.cuh"
 
 namespace moe {
-
-__device__ __forceinline__ float bf16_round(float v) {
-  return __bfloat162float(__float2bfloat16_rn(v));
-}
 
 __device__ __forceinline__ float4 load_bf16x4(const uint16_t* p) {
   const uint2 u = *reinterpret_cast<const uint2*>(p);
@@ -36,7 +32,7 @@ __device__ __forceinline__ void store_bf16x4(uint16_t* p, float4 v) {
   *reinterpret_cast<uint2*>(p) = u;
 }
 
-// bf16(sum over K splits of the fp32 partial sums) of row r, columns [c, c+4)
+// sum over K splits of the fp32 partial sums of row r, columns [c, c+4)
 __device__ __forceinline__ float4 y_from_partials(const float* part, int n_split,
                                                   size_t split_stride, int r, int d, int c) {
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -47,7 +43,7 @@ __device__ __forceinline__ float4 y_from_partials(const float* part, int n_split
     s.z += v.z;
     s.w += v.w;
   }
-  return make_float4(bf16_round(s.x), bf16_round(s.y), bf16_round(s.z), bf16_round(s.w));
+  return s;
 }
 
 __global__ void __launch_bounds__(256)

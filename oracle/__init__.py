@@ -53,8 +53,6 @@ def lib():
             P = C.c_void_p
             L.oracle_bf16_to_double.restype = C.c_double
             L.oracle_bf16_to_double.argtypes = [C.c_uint16]
-            L.oracle_bf16_round.restype = C.c_uint16
-            L.oracle_bf16_round.argtypes = [C.c_double]
             L.oracle_fp16_to_double.restype = C.c_double
             L.oracle_fp16_to_double.argtypes = [C.c_uint16]
             L.oracle_weight.restype = C.c_double
@@ -137,10 +135,10 @@ def permute(idx, E: int):
 
 
 def expert_ffn(x_row, expert: ExpertRef, d: int, F: int):
-    """Returns (h bf16-bits [F], y bf16-bits [d]) for one token row."""
+    """Returns (h [F], y [d]) in float64 for one bf16 token row."""
     xr = _np(x_row, np.uint16).reshape(-1)
-    h = np.zeros(F, np.uint16)
-    y = np.zeros(d, np.uint16)
+    h = np.zeros(F, np.float64)
+    y = np.zeros(d, np.float64)
     rc = lib().oracle_expert_ffn(_ptr(xr), d, F, C.byref(expert.struct), _ptr(h), _ptr(y))
     if rc:
         raise ValueError("oracle_expert_ffn: bad arguments")
@@ -153,7 +151,7 @@ def combine_row(y_rows, w, y_shared=None):
     arr = (C.c_void_p * k)(*[_ptr(y).value for y in ys])
     wf = _np(np.asarray(w, np.float32), np.float32)
     sh = _np(y_shared, np.uint16).reshape(-1) if y_shared is not None else None
-    out = np.zeros(d, np.uint16)
+    out = np.zeros(d, np.float64)
     rc = lib().oracle_combine_row(C.cast(arr, C.c_void_p), _ptr(wf), k, d,
                                   _ptr(sh) if sh is not None else None, _ptr(out))
     if rc:
@@ -163,14 +161,14 @@ def combine_row(y_rows, w, y_shared=None):
 
 def layer_forward(x, logits, k: int, experts: list, shared: ExpertRef | None, d: int, F: int,
                   tokens=None):
-    """out bf16-bits [n, d], idx [n, k], w [n, k] for the listed tokens (all if None)."""
+    """out float64 [n, d], idx [n, k], w [n, k] for the listed tokens (all if None)."""
     xb = _np(x, np.uint16)
     lg = _np(logits, np.float32)
     T, E = lg.shape
     arr = (Expert * E)(*[e.struct for e in experts])
     tl = None if tokens is None else np.ascontiguousarray(np.asarray(tokens, np.int32))
     n = T if tl is None else tl.shape[0]
-    out = np.zeros((n, d), np.uint16)
+    out = np.zeros((n, d), np.float64)
     idx = np.zeros((n, k), np.int32)
     w = np.zeros((n, k), np.float32)
     rc = lib().oracle_layer_forward(_ptr(xb), _ptr(lg), T, E, k, d, F, arr,

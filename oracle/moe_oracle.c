@@ -21,26 +21,6 @@ double oracle_bf16_to_double(uint16_t b) {
   return (double)f;
 }
 
-/* Round a double to the nearest bf16 (ties to even) in one step.  bf16 keeps 8
- * significant bits; normal exponents 2^-126 .. 2^127, subnormal quantum 2^-133. */
-uint16_t oracle_bf16_round(double v) {
-  if (v != v) return 0x7FC0;
-  uint16_t sign = signbit(v) ? 0x8000 : 0;
-  double a = fabs(v);
-  if (a == 0.0) return sign;
-  if (isinf(a)) return (uint16_t)(sign | 0x7F80);
-  int e;
-  frexp(a, &e);                  /* a = m * 2^e, m in [0.5, 1) */
-  int qe = e - 8;                /* quantum of an 8-bit significand */
-  if (qe < -133) qe = -133;
-  double r = nearbyint(ldexp(a, -qe)) * ldexp(1.0, qe);   /* default mode: ties to even */
-  if (r >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);
-  float f = (float)r;            /* exact: r has at most 8 significant bits */
-  uint32_t u;
-  memcpy(&u, &f, sizeof u);
-  return (uint16_t)(sign | (uint16_t)((u >> 16) & 0x7FFF));
-}
-
 double oracle_fp16_to_double(uint16_t h) {
   int s = (h >> 15) & 1, ex = (h >> 10) & 0x1F, man = h & 0x3FF;
   double v;
@@ -130,10 +110,10 @@ int oracle_permute(const int32_t* idx, int T, int k, int E, int32_t* counts, int
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 /* SwiGLU two-layer MLP ([Strata] sec. 3.2), no biases:
- *   g_f = sum_c x_c Wg[f][c],  u_f = sum_c x_c Wu[f][c],  h_f = bf16(silu(g_f) u_f)
- *   y_c = bf16(sum_f h_f Wd[c][f]) */
+ *   g_f = sum_c x_c Wg[f][c],  u_f = sum_c x_c Wu[f][c],  h_f = silu(g_f) u_f
+ *   y_c = sum_f h_f Wd[c][f] */
 int oracle_expert_ffn(const uint16_t* x_row, int d, int F, const oracle_expert* ex,
-                      uint16_t* h_out, uint16_t* y_out) {
+                      double* h_out, double* y_out) {
   if (!x_row || !ex || !y_out || d < 1 || F < 1) return -1;
   if (ex->gate.rows != F || ex->gate.cols != d || ex->up.rows != F || ex->up.cols != d ||
       ex->down.rows != d || ex->down.cols != F)
@@ -148,14 +128,13 @@ int oracle_expert_ffn(const uint16_t* x_row, int d, int F, const oracle_expert* 
       g += x[c] * oracle_weight(&ex->gate, f, c);
       u += x[c] * oracle_weight(&ex->up, f, c);
     }
-    uint16_t hb = oracle_bf16_round(silu(g) * u);
-    if (h_out) h_out[f] = hb;
-    h[f] = oracle_bf16_to_double(hb);
+    h[f] = silu(g) * u;
+    if (h_out) h_out[f] = h[f];
   }
   for (int c = 0; c < d; ++c) {
     double y = 0.0;
     for (int f = 0; f < F; ++f) y += h[f] * oracle_weight(&ex->down, c, f);
-    y_out[c] = oracle_bf16_round(y);
+    y_out[c] = y;
   }
   free(x);
   free(h);
@@ -164,15 +143,15 @@ int oracle_expert_ffn(const uint16_t* x_row, int d, int F, const oracle_expert* 
 
 /* ------------------------------------------------------------------ combine */
 
-/* out_c = bf16( sum_{j=0..k-1} w_j * y_j[c]  +  y_shared[c] ), summed in that order. */
+/* out_c = sum_{j=0..k-1} w_j * y_j[c]  +  y_shared[c], summed in that order. */
 int oracle_combine_row(const uint16_t* const* y_rows, const float* w, int k, int d,
-                       const uint16_t* y_shared, uint16_t* out) {
+                       const uint16_t* y_shared, double* out) {
   if (!y_rows || !w || !out || k < 1 || d < 1) return -1;
   for (int c = 0; c < d; ++c) {
     double acc = 0.0;
     for (int j = 0; j < k; ++j) acc += (double)w[j] * oracle_bf16_to_double(y_rows[j][c]);
     if (y_shared) acc += oracle_bf16_to_double(y_shared[c]);
-    out[c] = oracle_bf16_round(acc);
+    out[c] = acc;
   }
   return 0;
 }
@@ -184,30 +163,32 @@ int oracle_combine_row(const uint16_t* const* y_rows, const float* w, int k, int
  * [Strata] sec. 4.2 moves data but does not change any value. */
 int oracle_layer_forward(const uint16_t* x, const float* logits, int T, int E, int k, int d,
                          int F, const oracle_expert* experts, const oracle_expert* shared,
-                         const int32_t* token_list, int n_tokens, uint16_t* out,
+                         const int32_t* token_list, int n_tokens, double* out,
                          int32_t* idx_out, float* w_out) {
   if (!x || !logits || !experts || !out || T < 0 || E < 1 || k < 1 || k > E) return -1;
   int n = token_list ? n_tokens : T;
   int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)k);
   float* w = (float*)malloc(sizeof(float) * (size_t)k);
-  uint16_t* y = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)k * d);
-  uint16_t* ysh = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)d);
-  const uint16_t** yrows = (const uint16_t**)malloc(sizeof(uint16_t*) * (size_t)k);
+  double* y = (double*)malloc(sizeof(double) * (size_t)d);
   int rc = 0;
-  if (!idx || !w || !y || !ysh || !yrows) rc = -1;
+  if (!idx || !w || !y) rc = -1;
   for (int i = 0; i < n && rc == 0; ++i) {
     int t = token_list ? token_list[i] : i;
     if (t < 0 || t >= T) { rc = -1; break; }
+    double* o = out + (size_t)i * d;
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
     rc = oracle_route_topk(logits + (size_t)t * E, 1, E, k, idx, w);
-    for (int j = 0; j < k && rc == 0; ++j) {
-      rc = oracle_expert_ffn(x + (size_t)t * d, d, F, &experts[idx[j]], NULL, y + (size_t)j * d);
-      yrows[j] = y + (size_t)j * d;
+    for (int j = 0; j < k && rc == 0; ++j) {           /* sum_j w_j FFN_{e_j}(x_t), j in order */
+      rc = oracle_expert_ffn(x + (size_t)t * d, d, F, &experts[idx[j]], NULL, y);
+      for (int c = 0; c < d && rc == 0; ++c) o[c] += (double)w[j] * y[c];
     }
-    if (rc == 0 && shared) rc = oracle_expert_ffn(x + (size_t)t * d, d, F, shared, NULL, ysh);
-    if (rc == 0) rc = oracle_combine_row(yrows, w, k, d, shared ? ysh : NULL, out + (size_t)i * d);
+    if (rc == 0 && shared) {                           /* + FFN_shared(x_t), weight 1 */
+      rc = oracle_expert_ffn(x + (size_t)t * d, d, F, shared, NULL, y);
+      for (int c = 0; c < d && rc == 0; ++c) o[c] += y[c];
+    }
     if (rc == 0 && idx_out) memcpy(idx_out + (size_t)i * k, idx, sizeof(int32_t) * (size_t)k);
     if (rc == 0 && w_out) memcpy(w_out + (size_t)i * k, w, sizeof(float) * (size_t)k);
   }
-  free(idx); free(w); free(y); free(ysh); free(yrows);
+  free(idx); free(w); free(y);
   return rc;
 }

@@ -19,8 +19,10 @@
  *            two-layer MLP; grouped GEMM), sec. 4.2 (regroup tokens by expert).
  *
  * Types: bf16 and fp16 values are passed as their raw 16-bit patterns (uint16_t).
- * All arithmetic is fp64 except where the layer's data types fix a rounding
- * (bf16 activations h, y and out; fp32 routing weights).
+ * All arithmetic is fp64 and nothing is rounded on the way: the results are the
+ * exact layer math on the given bf16 inputs and weights (the routing weights
+ * are returned as fp32, the type they are stored in).  The CUDA path's bf16
+ * intermediates are approximations judged against these values.
  */
 #ifndef MOE_ORACLE_H
 #define MOE_ORACLE_H
@@ -49,7 +51,6 @@ typedef struct {
 
 /* Number helpers (exposed so tests can pin them against independent code). */
 double oracle_bf16_to_double(uint16_t b);
-uint16_t oracle_bf16_round(double v);          /* round to nearest even */
 double oracle_fp16_to_double(uint16_t h);
 double oracle_weight(const oracle_matrix* m, int row, int col);   /* dequantised value */
 
@@ -61,21 +62,22 @@ int oracle_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
                    int32_t* offsets /* E+1 */, int32_t* row_of_assign /* T*k */,
                    int32_t* token_of_row /* T*k */);
 
-/* SwiGLU expert FFN of one token row: h = bf16(silu(x Wg^T) * (x Wu^T)) [F],
- * y = bf16(h Wd^T) [d].  h_out may be NULL. */
+/* SwiGLU expert FFN of one token row: h = silu(x Wg^T) * (x Wu^T) [F],
+ * y = h Wd^T [d].  h_out may be NULL. */
 int oracle_expert_ffn(const uint16_t* x_row, int d, int F, const oracle_expert* ex,
-                      uint16_t* h_out, uint16_t* y_out);
+                      double* h_out, double* y_out);
 
-/* Weighted combine of one token: out = bf16(sum_j w[j] * y_j + y_shared). */
+/* Weighted combine of one token from bf16 expert outputs:
+ * out = sum_j w[j] * y_j + y_shared. */
 int oracle_combine_row(const uint16_t* const* y_rows, const float* w, int k, int d,
-                       const uint16_t* y_shared /* nullable */, uint16_t* out);
+                       const uint16_t* y_shared /* nullable */, double* out);
 
 /* Whole layer for the listed tokens (all T when token_list == NULL):
- * out [n][d] bf16, and per listed token its idx/w [n][k] (nullable). */
+ * out [n][d], and per listed token its idx/w [n][k] (nullable). */
 int oracle_layer_forward(const uint16_t* x, const float* logits, int T, int E, int k, int d,
                          int F, const oracle_expert* experts /* E */,
                          const oracle_expert* shared /* nullable, same d and F */,
-                         const int32_t* token_list, int n_tokens, uint16_t* out,
+                         const int32_t* token_list, int n_tokens, double* out,
                          int32_t* idx_out, float* w_out);
 
 #ifdef __cplusplus

@@ -48,7 +48,7 @@ class GpuLayer:
         return out, ws
 
     def oracle_forward(self, tokens=None):
-        """Oracle output rows (float32) for the listed tokens (all if None)."""
+        """Oracle output rows (exact, float64) for the listed tokens (all if None)."""
         cfg = self.cfg
         toks = list(range(cfg.T)) if tokens is None else list(tokens)
         idx, _ = oracle.route_topk(self.logits_np[toks], cfg.k)
@@ -59,7 +59,7 @@ class GpuLayer:
         sh = self.ref("shared") if cfg.shared else None
         out, _, _ = oracle.layer_forward(self.x.cpu(), self.logits_np, cfg.k, refs, sh, cfg.d,
                                          cfg.F, tokens=toks)
-        return oracle.bf16_bits_to_float(out)
+        return out
 
 
 def assert_close_rms(got: np.ndarray, want: np.ndarray, tol: float = TOL, what: str = ""):

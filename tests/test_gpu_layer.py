@@ -40,7 +40,9 @@ def test_layer_small_all_tokens(name):
 
 @pytest.mark.parametrize("name", ["tiny", "tiny_int4", "int4_ragged", "bf16_multichunk"])
 def test_grouped_ffn_and_combine_entry_points(name):
-    """route -> permute -> grouped_ffn -> combine through the separate ABI calls."""
+    """route -> permute -> grouped_ffn -> combine through the separate ABI calls:
+    y_perm (bf16) row by row against the oracle's expert FFN of that row's expert,
+    and the combine against the oracle's combine of the same bf16 y_perm rows."""
     L = GpuLayer(SMALL[name])
     cfg = L.cfg
     idx, w = moe.route_topk(L.logits, cfg.k)
@@ -49,16 +51,21 @@ def test_grouped_ffn_and_combine_entry_points(name):
     out = moe.combine(y_perm, perm["row_of_assign"], w)
     torch.cuda.synchronize()
     assert moe.last_device_error(ws) == 0
-    # y_perm row by row against the oracle's expert FFN of that row's expert
     tor = perm["token_of_row"].cpu().numpy()
     offs = perm["offsets"].cpu().numpy()
+    roa = perm["row_of_assign"].cpu().numpy()
     yp = y_perm.float().cpu().numpy()
+    yb = y_perm.cpu().view(torch.int16).numpy().view(np.uint16)
     rows = np.linspace(0, cfg.A - 1, min(cfg.A, 24)).astype(int)
     for r in rows:
         e = int(np.searchsorted(offs, r, side="right") - 1)
         _, y = oracle.expert_ffn(L.x[tor[r]].cpu(), L.ref(e), cfg.d, cfg.F)
-        assert_close_rms(yp[r], oracle.bf16_bits_to_float(y), what=f"{name} row {r}")
-    assert_close_rms(out.float().cpu().numpy(), L.oracle_forward(), what=name)
+        assert_close_rms(yp[r], y, what=f"{name} row {r}")
+    wc = w.cpu().numpy()
+    oc = out.float().cpu().numpy()
+    for t in range(min(cfg.T, 16)):
+        want = oracle.combine_row([yb[roa[t * cfg.k + j]] for j in range(cfg.k)], wc[t])
+        assert_close_rms(oc[t], want, what=f"{name} combine token {t}")
 
 
 def test_combine_with_shared_rows():
@@ -72,7 +79,7 @@ def test_combine_with_shared_rows():
     for t in range(T):
         bits = [yc[roac[t * k + j]].view(torch.int16).numpy().view(np.uint16) for j in range(k)]
         want = oracle.combine_row(bits, wc[t], shc[t].view(torch.int16).numpy().view(np.uint16))
-        assert_close_rms(out[t], oracle.bf16_bits_to_float(want), tol=1e-2, what=f"token {t}")
+        assert_close_rms(out[t], want, what=f"token {t}")
 
 
 @pytest.mark.parametrize("name", ["mixtral_decode", "phi35_prefill", "fg125b_decode",

@@ -24,26 +24,15 @@ def _bits(t: torch.Tensor) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------- numbers
-def test_bf16_round_matches_torch_on_floats():
+def test_bf16_decode_matches_torch():
     rng = np.random.default_rng(0)
-    vals = np.concatenate([
-        rng.standard_normal(20000).astype(np.float32) * 10.0 ** rng.integers(-40, 38, 20000),
-        np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 2 ** -130, 3.4e38, 1e-45], np.float32),
-    ]).astype(np.float32)
-    want = _bits(torch.from_numpy(vals).to(torch.bfloat16))   # library RNE conversion
+    bits = rng.integers(0, 65536, 5000).astype(np.uint16)
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
     L = oracle.lib()
-    got = np.array([L.oracle_bf16_round(float(v)) for v in vals], np.uint16)
-    assert np.array_equal(got, want)
-
-
-def test_bf16_round_is_single_rounding_from_double():
-    L = oracle.lib()
-    # exact tie between 1 and 1+2^-7 -> even (1.0); just above the tie -> up.
-    assert L.oracle_bf16_round(1 + 2 ** -8) == 0x3F80
-    assert L.oracle_bf16_round(1 + 2 ** -8 + 2 ** -40) == 0x3F81   # via fp32 this would tie to 1.0
-    assert L.oracle_bf16_round(-(1 + 3 * 2 ** -8)) == 0xBF82       # tie -> even mantissa 2
-    assert L.oracle_bf16_round(float("inf")) == 0x7F80
-    assert L.oracle_bf16_round(3.4e38 * 2) == 0x7F80
+    got = np.array([L.oracle_bf16_to_double(int(b)) for b in bits])
+    fin = np.isfinite(want)
+    assert np.array_equal(got[fin], want[fin])
+    assert np.array_equal(np.isnan(got), np.isnan(want))
 
 
 def test_fp16_decode_all_patterns():
@@ -209,13 +198,12 @@ def test_permute_all_to_one_expert():
 
 # ----------------------------------------------------------------------------- expert FFN
 def _dense_swiglu(x_bf16: torch.Tensor, Wg, Wu, Wd):
-    """Independent dense SwiGLU in float64 numpy; h and y rounded through torch's bf16."""
+    """Independent dense SwiGLU in float64 numpy (library matmuls)."""
     x = x_bf16.double().numpy()
     g = x @ Wg.T
     u = x @ Wu.T
-    h = torch.from_numpy(g / (1.0 + np.exp(-g)) * u).float().to(torch.bfloat16)
-    y = h.double().numpy() @ Wd.T
-    return h, torch.from_numpy(y).float().to(torch.bfloat16)
+    h = g / (1.0 + np.exp(-g)) * u
+    return h, h @ Wd.T
 
 
 def _dequant_numpy(enc):
@@ -226,14 +214,6 @@ def _dequant_numpy(enc):
     s = np.repeat(enc["scale"].double().numpy(), 128, axis=1)
     z = np.repeat(enc["zero"].double().numpy(), 128, axis=1)
     return (codes - z) * s
-
-
-def _ulps_bf16(a_bits, b_bits):
-    a = a_bits.astype(np.int32)
-    b = b_bits.astype(np.int32)
-    a = np.where(a & 0x8000, -(a & 0x7FFF), a)
-    b = np.where(b & 0x8000, -(b & 0x7FFF), b)
-    return np.abs(a - b)
 
 
 @pytest.mark.parametrize("fmt", ["bf16", "int4"])
@@ -250,12 +230,12 @@ def test_single_expert_reduces_to_dense_swiglu(fmt):
         Wg, Wu, Wd = (wts[m]["w"].double().numpy() for m in ("gate", "up", "down"))
     else:
         Wg, Wu, Wd = (_dequant_numpy(wts[m]) for m in ("gate", "up", "down"))
-    _, y = _dense_swiglu(x, Wg, Wu, Wd)
-    ul = _ulps_bf16(out, _bits(y))
-    assert ul.max() <= 1 and (ul > 0).mean() < 0.01
+    h, y = _dense_swiglu(x, Wg, Wu, Wd)
+    np.testing.assert_allclose(out, y, rtol=1e-9, atol=1e-12 * np.abs(y).max())
     # the single-row entry point gives the same h and y
     h1, y1 = oracle.expert_ffn(x[2], ref, cfg.d, cfg.F)
     assert np.array_equal(y1, out[2])
+    np.testing.assert_allclose(h1, h[2], rtol=1e-9, atol=1e-12 * np.abs(h).max())
 
 
 def test_combine_identical_experts_is_dense_ffn():
@@ -266,7 +246,7 @@ def test_combine_identical_experts_is_dense_ffn():
     ref = oracle.ExpertRef(wts, "bf16")
     out, _, _ = oracle.layer_forward(x, lg, 2, [ref] * 4, None, cfg.d, cfg.F)
     _, y = _dense_swiglu(x, *(wts[m]["w"].double().numpy() for m in ("gate", "up", "down")))
-    assert _ulps_bf16(out, _bits(y)).max() <= 1
+    np.testing.assert_allclose(out, y, rtol=1e-6, atol=1e-9)      # sum of fp32 weights = 1 +- 1e-7
 
 
 def test_down_projection_linearity():
@@ -280,7 +260,7 @@ def test_down_projection_linearity():
           for w in wts]
     out2, _, _ = oracle.layer_forward(x, lg, 2, [oracle.ExpertRef(w, "bf16") for w in w2], None,
                                       cfg.d, cfg.F)
-    assert np.array_equal(bf(out2), 2.0 * bf(out1))
+    assert np.array_equal(out2, 2.0 * out1)
 
 
 def test_shared_expert_alone_when_routed_down_is_zero():
@@ -306,6 +286,6 @@ def test_combine_row_hand_values():
     two = _bits(torch.tensor([2.0, 4.0, 0.25], dtype=torch.bfloat16))
     sh = _bits(torch.tensor([0.5, 0.5, 0.5], dtype=torch.bfloat16))
     out = oracle.combine_row([one, two], [0.25, 0.75])
-    assert bf(out).tolist() == [1.75, 2.5, 0.3125]
+    assert out.tolist() == [1.75, 2.5, 0.3125]
     out = oracle.combine_row([one, two], [0.25, 0.75], sh)
-    assert bf(out).tolist() == [2.25, 3.0, 0.8125]
+    assert out.tolist() == [2.25, 3.0, 0.8125]
