@@ -195,6 +195,31 @@ moe_status moe_layer_forward_timed(const uint16_t* x, const float* logits, int T
                                    void* ws, size_t ws_bytes, moe_stream_t stream,
                                    void* const* stage_events);
 
+/* Allocation-free variant of moe_layer_forward, for callers that cannot
+ * allocate device memory at call time and cannot hand the library a
+ * workspace: code running inside stream capture (an allocation there is not
+ * part of the graph and may synchronise), hosts that own every device
+ * allocation through their own pool and forbid libraries from calling
+ * cudaMalloc, and real-time loops where an allocation's latency is not
+ * allowed.  The pages have no counterpart to this entry point.
+ *
+ * Same arguments and results as moe_layer_forward, without ws / ws_bytes: the
+ * scratch is a file-scope device array of MOE_NOALLOC_SCRATCH_BYTES that every
+ * GPU loading the library holds until the process exits.  A call whose
+ * moe_layer_workspace_bytes(T, k, routed, shared) exceeds that size returns
+ * MOE_ERR_WORKSPACE and launches nothing (decode-sized batches fit; large
+ * prefill chunks do not).  No cudaMalloc, cudaFree or allocating library call
+ * is made.  The first call on a device looks up that device's address of the
+ * array (cudaGetSymbolAddress, with the device current); make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents (its error word is cleared at the start of each call):
+ * calls that overlap on the GPU -- on different streams, or from different
+ * host threads -- race on it and must be serialised by the caller. */
+#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+moe_status moe_layer_forward_noalloc(const uint16_t* x, const float* logits, int T, int k,
+                                     const moe_pool* routed, const moe_pool* shared,
+                                     uint16_t* out, moe_stream_t stream);
+
 /* Kernel launches one moe_layer_forward enqueues for these arguments (0 on error). */
 int moe_layer_launch_count(int T, int k, const moe_pool* routed, const moe_pool* shared);
 

@@ -34,7 +34,8 @@ DEVERR = {1: "timeout", 2: "expert index out of range", 4: "slot out of range", 
 EXPORTS = ("moe_status_str", "moe_slot_bytes", "moe_prepack_expert", "moe_route_topk",
            "moe_permute_workspace_bytes", "moe_permute", "moe_grouped_ffn_workspace_bytes",
            "moe_grouped_ffn", "moe_combine", "moe_layer_workspace_bytes", "moe_layer_forward",
-           "moe_layer_forward_timed", "moe_layer_launch_count", "moe_last_device_error")
+           "moe_layer_forward_timed", "moe_layer_launch_count", "moe_last_device_error",
+           "moe_layer_forward_noalloc")
 
 
 class MoeError(RuntimeError):

@@ -406,3 +406,45 @@ moe_status moe_last_device_error(const void* ws, int* code, moe_stream_t stream)
 }
 
 }  // extern "C"
+
+// ===================================================================== allocation-free variant
+// Scratch for moe_layer_forward_noalloc: one file-scope device array per GPU
+// that loads the library.  In host code `g_noalloc_scratch` names a host-side
+// stand-in, never a device address: the device address is looked up once per
+// device with cudaGetSymbolAddress and passed to the kernels as their workspace.
+namespace {
+__device__ __align__(256) uint8_t g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {nullptr};
+
+moe_status noalloc_scratch_for_current_device(void** ptr) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES)
+    return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+}  // namespace
+
+extern "C" moe_status moe_layer_forward_noalloc(const uint16_t* x, const float* logits, int T,
+                                                int k, const moe_pool* routed,
+                                                const moe_pool* shared, uint16_t* out,
+                                                moe_stream_t stream) {
+  const size_t need = moe_layer_workspace_bytes(T, k, routed, shared);
+  if (need == 0) return MOE_ERR_INVALID_ARG;
+  if (need > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+  void* ws = nullptr;
+  const moe_status st = noalloc_scratch_for_current_device(&ws);
+  if (st != MOE_OK) return st;
+  return layer_forward_impl(x, logits, T, k, routed, shared, out, ws, MOE_NOALLOC_SCRATCH_BYTES,
+                            (cudaStream_t)stream, nullptr);
+}
