@@ -49,16 +49,18 @@ inline bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 inline bool al256(const void* p) { return ((uintptr_t)p & 255u) == 0; }
 inline size_t up1k(size_t x) { return (x + 1023) & ~(size_t)1023; }
 
-// bf16 row-major [rows][K] -> TMA map with a {64 x box_rows} box, 128-byte swizzle.
-bool make_row_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
+// 16-bit row-major [rows][K] (bf16 or fp16) -> TMA map with a {64 x box_rows}
+// box and the 128-byte swizzle.
+bool make_row_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows, bool fp16) {
   if (!have_encoder()) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)K * 2};
   cuuint32_t box[2] = {(cuuint32_t)KSTEP, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return g_encode(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 moe_status check_pool(const moe_pool* p, bool single) {
@@ -99,7 +101,7 @@ int choose_ksplit(int A, int E, bool has_shared, int bn, int n_mt, int F) {
 
 struct LayerLayout {
   int A, Tsh, rows, E, d, F, bn, ksplit;
-  size_t err, idx, w, counts, offsets, roa, tor, xperm, h, part, total;
+  size_t err, idx, w, counts, offsets, roa, tor, xperm, h, part, xsum, hsum, total;
 };
 
 LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* shared) {
@@ -123,6 +125,9 @@ LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* s
   L.xperm = o;    o = up1k(o + (size_t)L.rows * L.d * 2);
   L.h = o;        o = up1k(o + (size_t)L.rows * L.F * 2);
   L.part = o;     o = up1k(o + (size_t)L.ksplit * L.rows * L.d * 4);
+  const bool f16 = gemm_uses_fp16(routed->fmt);   // int4: row sums for the group-scaled loop
+  L.xsum = o;     o = up1k(o + (f16 ? (size_t)(L.d / QGROUP) * L.rows * 4 : 0));
+  L.hsum = o;     o = up1k(o + (f16 ? (size_t)(L.F / QGROUP) * L.rows * 4 : 0));
   L.total = o;
   return L;
 }
@@ -150,13 +155,17 @@ GemmArgs base_args(const moe_pool* routed, const moe_pool* shared, int* err) {
 }
 
 // gate/up (SwiGLU) then down over the row groups described by `offsets`.
+// x_rows and h are fp16 for int4 pools (with xsum/hsum their per-group row
+// sums), bf16 otherwise.
 moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups, int rows,
                    const moe_pool* routed, const moe_pool* shared, int bn, int ksplit, uint16_t* h,
-                   float* part, int* err, cudaStream_t s, cudaEvent_t ev_mid, cudaEvent_t ev_down) {
+                   float* part, const float* xsum, float* hsum, int* err, cudaStream_t s,
+                   cudaEvent_t ev_mid, cudaEvent_t ev_down) {
   const int d = routed->d_model, F = routed->d_ff, fmt = routed->fmt;
+  const bool f16 = gemm_uses_fp16(fmt);
   const int grid = sm_count();
   CUtensorMap mx, mh;
-  if (!make_row_map(&mx, x_rows, rows, d, bn) || !make_row_map(&mh, h, rows, F, bn))
+  if (!make_row_map(&mx, x_rows, rows, d, bn, f16) || !make_row_map(&mh, h, rows, F, bn, f16))
     return MOE_ERR_CUDA;
   GemmArgs a = base_args(routed, shared, err);
   a.offsets = offsets;
@@ -172,6 +181,8 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
   g.out = h;
   g.out_ld = F;
   g.out_split_stride = 0;
+  g.bsum = xsum;
+  g.hsum_out = hsum;
   if (launch_grouped_gemm(fmt, true, mx, g, plan_gemm(fmt, true, bn, n_groups), grid, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev_mid && cudaEventRecord(ev_mid, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -184,6 +195,8 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
   dn.out = part;
   dn.out_ld = d;
   dn.out_split_stride = (unsigned long long)rows * d;
+  dn.bsum = hsum;
+  dn.hsum_out = nullptr;
   if (launch_grouped_gemm(fmt, false, mh, dn, plan_gemm(fmt, false, bn, n_groups), grid, s) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
@@ -229,6 +242,9 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
   uint16_t* xperm = (uint16_t*)(W + L.xperm);
   uint16_t* h = (uint16_t*)(W + L.h);
   float* part = (float*)(W + L.part);
+  const bool f16 = gemm_uses_fp16(routed->fmt);
+  float* xsum = f16 ? (float*)(W + L.xsum) : nullptr;
+  float* hsum = f16 ? (float*)(W + L.hsum) : nullptr;
   auto rec = [&](int i) -> bool {
     return !ev || !ev[i] || cudaEventRecord((cudaEvent_t)ev[i], s) == cudaSuccess;
   };
@@ -239,11 +255,11 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
   if (launch_permute_index(idx, T, k, E, L.Tsh, counts, offsets, roa, tor, err, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!rec(MOE_STAGE_GATHER)) return MOE_ERR_CUDA;
-  if (launch_gather_rows(x, tor, L.rows, T, L.d, xperm, sm_count(), s) != cudaSuccess)
+  if (launch_gather_rows(x, tor, L.rows, T, L.d, xperm, f16, xsum, sm_count(), s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!rec(MOE_STAGE_GATE_UP)) return MOE_ERR_CUDA;
   st = run_ffn(xperm, offsets, E + (shared ? 1 : 0), L.rows, routed, shared, L.bn, L.ksplit, h, part,
-               err, s, ev ? (cudaEvent_t)ev[MOE_STAGE_DOWN] : nullptr,
+               xsum, hsum, err, s, ev ? (cudaEvent_t)ev[MOE_STAGE_DOWN] : nullptr,
                ev ? (cudaEvent_t)ev[MOE_STAGE_COMBINE] : nullptr);
   if (st != MOE_OK) return st;
   if (launch_combine_partials(part, L.ksplit, (size_t)L.rows * L.d, roa, w, T, k, L.d,
@@ -319,16 +335,38 @@ moe_status moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int k,
   if (launch_permute_index(topk_idx, T, k, E, 0, counts, offsets, row_of_assign, token_of_row, err,
                            s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (launch_gather_rows(x, token_of_row, T * k, T, d, x_perm, sm_count(), s) != cudaSuccess)
+  if (launch_gather_rows(x, token_of_row, T * k, T, d, x_perm, false, nullptr, sm_count(), s) !=
+      cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
+// Workspace of the standalone grouped FFN: error word, h, down partials and, for
+// int4 pools, an fp16 copy of x_perm with its per-group row sums and the sums of h.
+struct FfnLayout {
+  int bn, ksplit;
+  size_t h, part, x16, xsum, hsum, total;
+};
+
+FfnLayout ffn_layout(int A, const moe_pool* pool) {
+  FfnLayout L{};
+  const int d = pool->d_model, F = pool->d_ff;
+  L.bn = choose_bn(A, pool->n_experts);
+  L.ksplit = choose_ksplit(A, pool->n_experts, false, L.bn, d / TILE_M, F);
+  const bool f16 = gemm_uses_fp16(pool->fmt);
+  size_t o = 1024;
+  L.h = o;     o = up1k(o + (size_t)A * F * 2);
+  L.part = o;  o = up1k(o + (size_t)L.ksplit * A * d * 4);
+  L.x16 = o;   o = up1k(o + (f16 ? (size_t)A * d * 2 : 0));
+  L.xsum = o;  o = up1k(o + (f16 ? (size_t)(d / QGROUP) * A * 4 : 0));
+  L.hsum = o;  o = up1k(o + (f16 ? (size_t)(F / QGROUP) * A * 4 : 0));
+  L.total = o;
+  return L;
+}
+
 size_t moe_grouped_ffn_workspace_bytes(int A, const moe_pool* pool) {
   if (A < 1 || check_pool(pool, false) != MOE_OK) return 0;
-  const int bn = choose_bn(A, pool->n_experts);
-  const int ks = choose_ksplit(A, pool->n_experts, false, bn, pool->d_model / TILE_M, pool->d_ff);
-  return 1024 + up1k((size_t)A * pool->d_ff * 2) + up1k((size_t)ks * A * pool->d_model * 4);
+  return ffn_layout(A, pool).total;
 }
 
 moe_status moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int A,
@@ -339,20 +377,32 @@ moe_status moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int A
   if (!x_perm || !offsets || !y_perm || !ws || A < 1) return MOE_ERR_INVALID_ARG;
   if (A > MAX_A) return MOE_ERR_UNSUPPORTED;
   if (!al16(x_perm) || !al16(offsets) || !al16(y_perm) || !al256(ws)) return MOE_ERR_INVALID_ARG;
-  if (ws_bytes < moe_grouped_ffn_workspace_bytes(A, pool)) return MOE_ERR_WORKSPACE;
-  const int bn = choose_bn(A, pool->n_experts);
-  const int ks = choose_ksplit(A, pool->n_experts, false, bn, pool->d_model / TILE_M, pool->d_ff);
+  const FfnLayout L = ffn_layout(A, pool);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   uint8_t* W = (uint8_t*)ws;
   int* err = (int*)W;
-  uint16_t* h = (uint16_t*)(W + 1024);
-  float* part = (float*)(W + 1024 + up1k((size_t)A * pool->d_ff * 2));
+  uint16_t* h = (uint16_t*)(W + L.h);
+  float* part = (float*)(W + L.part);
   cudaStream_t s = (cudaStream_t)stream;
+  const bool f16 = gemm_uses_fp16(pool->fmt);
+  const uint16_t* rows_in = x_perm;
+  float* xsum = nullptr;
+  float* hsum = nullptr;
   if (launch_clear_word(err, s) != cudaSuccess) return MOE_ERR_CUDA;
-  st = run_ffn(x_perm, offsets, pool->n_experts, A, pool, nullptr, bn, ks, h, part, err, s, nullptr,
-               nullptr);
+  if (f16) {   // the int4 GEMMs read fp16 rows and their group sums
+    uint16_t* x16 = (uint16_t*)(W + L.x16);
+    xsum = (float*)(W + L.xsum);
+    hsum = (float*)(W + L.hsum);
+    if (launch_gather_rows(x_perm, nullptr, A, A, pool->d_model, x16, true, xsum, sm_count(), s) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    rows_in = x16;
+  }
+  st = run_ffn(rows_in, offsets, pool->n_experts, A, pool, nullptr, L.bn, L.ksplit, h, part, xsum,
+               hsum, err, s, nullptr, nullptr);
   if (st != MOE_OK) return st;
-  return launch_reduce_splits(part, ks, (size_t)A * pool->d_model, A, pool->d_model, y_perm, s) ==
-                 cudaSuccess
+  return launch_reduce_splits(part, L.ksplit, (size_t)A * pool->d_model, A, pool->d_model, y_perm,
+                              s) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }

@@ -1,0 +1,124 @@
+// gemm_common.cuh -- pieces shared by the two grouped-GEMM kernels (gemm.cu:
+// shared-memory A operand; gemm_group.cu: int4 group-scaled loop with the A
+// operand in tensor memory): the device-built work list, item decoding, ring
+// positions, nibble unpacking.
+#pragma once
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace gemm {
+
+struct Item {
+  int g, mt, ks, r0, n_rows;
+  const uint8_t* slot;
+};
+
+// Work list in shared memory: prefix[g] = first item of row group g, nch[g] =
+// its row chunks, goff[g] = its first row.
+struct WorkList {
+  int* prefix;   // [n_groups + 1]
+  int* nch;      // [n_groups + 1]
+  int* goff;     // [n_groups + 1]
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ inline size_t worklist_ints(int n_groups) { return 3 * (size_t)(n_groups + 1); }
+
+// Built by one warp: items per group = row chunks * 128-row tiles * K splits.
+// Returns the total item count (valid in lane 0's caller after the CTA barrier).
+__device__ __forceinline__ int build_worklist(const GemmArgs& p, const WorkList& W, int lane) {
+  int running = 0;
+  bool bad = false;
+  for (int g0 = 0; g0 < p.n_groups; g0 += 32) {
+    const int g = g0 + lane;
+    int items = 0, nch = 0;
+    if (g < p.n_groups) {
+      const int lo = p.offsets[g], hi = p.offsets[g + 1];
+      int cnt = hi - lo;
+      if (lo < 0 || cnt < 0 || hi > p.rows_total) { bad = true; cnt = 0; }
+      nch = cnt > 0 ? (cnt + p.bn - 1) / p.bn : 0;
+      items = nch * p.n_mt * p.ksplit;
+      W.goff[g] = lo;
+      if (g == p.n_groups - 1) W.goff[g + 1] = hi;
+    }
+    int incl = items;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (g < p.n_groups) {
+      W.prefix[g] = running + incl - items;
+      W.nch[g] = nch;
+    }
+    running += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (bad) atomicOr(p.err, MOE_DEVERR_OFFSETS);
+  if (lane == 0) W.prefix[p.n_groups] = running;
+  return running;
+}
+
+__device__ __forceinline__ bool decode_item(int item, const GemmArgs& p, const WorkList& W, Item& it) {
+  int lo = 0, hi = p.n_groups - 1;
+  while (lo < hi) {   // last group whose first item is <= item (empty groups are skipped)
+    const int mid = (lo + hi + 1) >> 1;
+    if (W.prefix[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  const int g = lo;
+  const int local = item - W.prefix[g];
+  const int nch = W.nch[g];
+  const int nc = local % nch;
+  const int t2 = local / nch;
+  it.g = g;
+  it.ks = t2 % p.ksplit;
+  it.mt = t2 / p.ksplit;
+  const int cnt = W.goff[g + 1] - W.goff[g];
+  const int rpc = (((cnt + nch - 1) / nch) + 15) & ~15;   // rows per chunk, multiple of 16
+  it.r0 = W.goff[g] + nc * rpc;
+  it.n_rows = min(rpc, cnt - nc * rpc);
+  int slot;
+  if (g < p.n_routed) {
+    slot = p.e2s_r[g];
+    if (slot < 0 || slot >= p.n_slots_r) { atomicOr(p.err, MOE_DEVERR_SLOT_RANGE); return false; }
+    it.slot = p.pool_r + (size_t)slot * p.slot_bytes_r;
+  } else {
+    slot = p.e2s_s[0];
+    if (slot < 0 || slot >= p.n_slots_s) { atomicOr(p.err, MOE_DEVERR_SLOT_RANGE); return false; }
+    it.slot = p.pool_s + (size_t)slot * p.slot_bytes_s;
+  }
+  return true;
+}
+
+// K range of split ks, in whole quantisation groups of 128.
+__device__ __forceinline__ void kgroups(const GemmArgs& p, int ks, int& g0, int& g1) {
+  const int G = p.K / QGROUP;
+  g0 = (int)((long long)ks * G / p.ksplit);
+  g1 = (int)((long long)(ks + 1) * G / p.ksplit);
+}
+
+struct Ring {
+  int i;
+  uint32_t ph;
+  int n;
+  __device__ __forceinline__ void next() {
+    if (++i == n) { i = 0; ph ^= 1u; }
+  }
+};
+
+// The 8 nibbles of a word -> 4 fp16 pairs (1024 + q): one LOP3 per pair.  In
+// the prepacked layout element 2i sits in bits [4i, 4i+4) and 2i+1 in bits
+// [16+4i, 20+4i), so pair i comes out in K order.
+__device__ __forceinline__ void codes_of_word(uint32_t w, uint32_t* o) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = lop3_and_or(w >> (4 * i), 0x000F000Fu, 0x64006400u);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__device__ __forceinline__ __half to_half_sat(float v) {
+  return __float2half_rn(fminf(fmaxf(v, -65504.f), 65504.f));
+}
+
+}  // namespace gemm
+}  // namespace moe

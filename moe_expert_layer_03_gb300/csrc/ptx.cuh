@@ -52,6 +52,20 @@ MOE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Same, letting the hardware suspend the thread (up to ~the hint, in ns) until
+// the phase completes instead of returning at once: waiting warps stop taking
+// issue slots from the working ones.
+MOE_DEV bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
 
 // Waits for the phase with the given parity to complete.  Returns false (and
 // leaves the pipeline) if the CTA is aborting or the wait ran past its limit.
@@ -59,8 +73,8 @@ MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, 
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if ((i & 3u) == 0) {
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > MOE_WAIT_LIMIT_NS) {
         *abort_flag = 1;
@@ -143,24 +157,36 @@ MOE_DEV uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of kind::f16: bf16 x bf16 -> fp32, A and B K-major,
-// shape M x N (M = 128 here; N a multiple of 16, 16..256).
-MOE_DEV uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
-  return (1u << 4)            // D format: f32
-         | (1u << 7)          // A format: bf16
-         | (1u << 10)         // B format: bf16
-         | ((N >> 3) << 17)   // N / 8
-         | ((M >> 4) << 24);  // M / 16
+// Instruction descriptor of kind::f16 with fp32 accumulation, A and B K-major,
+// shape M x N (M = 128 here; N a multiple of 16, 16..256).  Both operands have
+// the same type: bf16 (ab_bf16 = 1) or fp16 (ab_bf16 = 0).
+MOE_DEV uint32_t idesc_f16kind_f32(uint32_t M, uint32_t N, uint32_t ab_bf16) {
+  return (1u << 4)                // D format: f32
+         | (ab_bf16 << 7)         // A format: 0 = f16, 1 = bf16
+         | (ab_bf16 << 10)        // B format: same as A
+         | ((N >> 3) << 17)       // N / 8
+         | ((M >> 4) << 24);      // M / 16
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-MOE_DEV void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+MOE_DEV void mma_f16kind(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                       uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Same with the A operand in tensor memory: a_tmem addresses a 128-lane x
+// (K/2)-column block, row m in lane m, two 16-bit K elements per column.
+MOE_DEV void mma_f16kind_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Arrives once on `bar` when every tcgen05 op this thread issued so far is done.
@@ -181,7 +207,34 @@ MOE_DEV void tmem_ld_16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
+// 32 lanes x 8 consecutive 32-bit columns.
+MOE_DEV void tmem_ld_8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr));
+}
 MOE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Registers -> tensor memory: thread i of the warp writes lane (quadrant*32 + i),
+// 32 (or 16) consecutive 32-bit columns starting at the address's column.
+MOE_DEV void tmem_st_32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+               : "memory");
+}
+MOE_DEV void tmem_st_16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+               : "memory");
+}
+MOE_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Barrier among a subset of the CTA's warps (id 1..15; nthreads a multiple of 32).
+MOE_DEV void named_barrier(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 // ------------------------------------------------------------------ misc
 MOE_DEV uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {   // (a & b) | c

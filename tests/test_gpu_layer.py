@@ -27,6 +27,10 @@ SMALL = {
     "k_equals_E": ms.LayerConfig("k_equals_E", T=9, d=128, F=128, E=4, k=4, fmt="bf16", seed=2),
     "single_token": ms.LayerConfig("single_token", T=1, d=256, F=256, E=8, k=2, fmt="int4"),
     "dense_E1": ms.LayerConfig("dense_E1", T=20, d=256, F=512, E=1, k=1, fmt="int4"),
+    # row chunks of 32 (int4 group-scaled main loop at its wider width)
+    "int4_chunk32": ms.LayerConfig("int4_chunk32", T=48, d=384, F=512, E=8, k=2, fmt="int4", seed=4),
+    # row chunks of 64 and 256 (int4 main loop that dequantises to fp16 in shared memory)
+    "int4_chunk64": ms.LayerConfig("int4_chunk64", T=96, d=256, F=384, E=8, k=2, fmt="int4", seed=6),
 }
 
 
