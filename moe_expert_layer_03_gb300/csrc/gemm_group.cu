@@ -20,13 +20,15 @@
 //         acc += s * (D_g - (1024 + z) * sum_{k in g} b_k),
 //     where sum b_k is the group sum of the token row's fp16 values (computed by
 //     the gather kernel for x, by the gate/up epilogue for h);
-//   * the MMA warp prepares the next stage's operands while the current
-//     stage's MMAs issue.
+//   * two MMA warps take alternate groups (each group has its own A stage
+//     and accumulator slice, so they never touch the same TMEM), and each
+//     prepares its next group's operands while the current MMAs issue: the
+//     issue rate of one warp, not the tensor core, bounds small-N MMAs.
 //
-//   warp 0   producer (bulk copy + TMA), warp 1 TMEM owner + MMA issuer,
-//   warps 2-9 unpack + fold + epilogue (two warps per TMEM lane quadrant:
-//   gate/up -> one warp per (matrix, quadrant); down -> the two warps of a
-//   quadrant split each row's K quads and the accumulator columns).
+//   warp 0   producer (bulk copy + TMA), warps 1-2 MMA issuers (warp 1 owns
+//   TMEM), warps 3-10 unpack + fold + epilogue (two warps per TMEM lane
+//   quadrant: gate/up -> one warp per (matrix, quadrant); down -> the two
+//   warps of a quadrant split each row's K quads and the accumulator columns).
 //
 // Every wait is bounded; on a timeout the CTA drains its copies and MMAs,
 // frees TMEM and returns with MOE_DEVERR_TIMEOUT set.
@@ -41,10 +43,12 @@ namespace {
 constexpr int G_NBUF = 4;     // accumulator slices
 constexpr int G_LAG = 2;      // groups between a slice's MMA and its fold
 constexpr int G_NA = 2;       // A stages in tensor memory
-constexpr int G_MISC = 10;    // [0] tmem [1] abort [2] items [3] raw consumed [5] b consumed
-                              // [6] raw issued [8] b issued [9] stays 0
+constexpr int G_MISC = 10;    // [0] tmem [1] abort [2] items [6] raw issued [8] b issued
+                              // [9] stays 0
+constexpr int G_NMMA = 2;     // MMA-issuing warps (alternate groups)
 constexpr int G_NDQ = 8;
-constexpr int G_THREADS = (2 + G_NDQ) * 32;
+constexpr int G_DQ0 = 1 + G_NMMA;                  // first dequant warp
+constexpr int G_THREADS = (1 + G_NMMA + G_NDQ) * 32;
 
 struct GShared {
   uint8_t* b_ring;
@@ -127,7 +131,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       mbar_init(smem_u32(&S.acc_empty[i]), G_NDQ * 32);
     }
     for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&S.xch_bar[i]), G_NDQ * 32);
-    mbar_init(smem_u32(S.fin), 1);
+    mbar_init(smem_u32(S.fin), G_NMMA);
     for (int i = 1; i < G_MISC; ++i)
       if (i != 2) S.misc[i] = 0;   // [0] written by tcgen05.alloc, [2] by warp 2
     fence_mbar_init();
@@ -137,7 +141,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     tmem_alloc(smem_u32(&S.misc[0]), p.tmem_cols);
     tmem_relinquish();
   }
-  if (warp == 2) {
+  if (warp == G_DQ0) {
     const int total = build_worklist(p, S.W, lane);
     if (lane == 0) S.misc[2] = total;
   }
@@ -182,13 +186,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       S.misc[6] = issued_raw;
       S.misc[8] = issued_b;
     }
-  } else if (warp == 1) {
-    // ================================================================ MMA issuer
-    // The whole warp runs the loop; lane 0 issues.  The next stage's operands
-    // are prepared while this stage's 16 MMAs issue (they depend only on ring
-    // positions and the group counter).
-    Ring ra{0, 0, G_NA}, rb{0, 0, p.n_b};
-    int consumed_b = 0;
+  } else if (warp < G_DQ0) {
+    // ================================================================ MMA issuers
+    // Warp 1 + mw issues the groups with (group counter % 2) == mw; their A
+    // stage is always mw.  Every ring position and phase follows from the
+    // group counter gc, which both warps advance identically.  The whole warp
+    // runs the loop; lane 0 issues.
+    const int mw = warp - 1;
     uint32_t gc = 0;
     bool ok = true;
     struct Ops {
@@ -197,65 +201,62 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       uint32_t d[NMAT];
     };
     const uint32_t b_ring0 = smem_u32(S.b_ring);
-    auto prep = [&](int ai, int bi, uint32_t g) -> Ops {
+    auto prep = [&](uint32_t g) -> Ops {
       Ops o;
-      const uint32_t bst = b_ring0 + (uint32_t)bi * B_STAGE;
+      const uint32_t bst = b_ring0 + (g % (uint32_t)p.n_b) * B_STAGE;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         o.b[q] = sdesc_kmajor_sw128(bst + (uint32_t)(q >> 2) * B_HALF + (uint32_t)(q & 3) * 32u);
 #pragma unroll
         for (int m = 0; m < NMAT; ++m)
-          o.a[m][q] = tmem_base + (uint32_t)ai * A_COLS + (uint32_t)(m * (QGROUP / 2) + q * 8);
+          o.a[m][q] = tmem_base + (uint32_t)mw * A_COLS + (uint32_t)(m * (QGROUP / 2) + q * 8);
       }
 #pragma unroll
       for (int m = 0; m < NMAT; ++m)
         o.d[m] = tmem_base + acc0 + (g % G_NBUF) * (uint32_t)(NMAT * GBN) + (uint32_t)(m * GBN);
       return o;
     };
-    Ops curo = prep(0, 0, 0);
+    Ops curo = prep((uint32_t)mw);
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
       Item it;
       if (!decode_item(item, p, S.W, it)) continue;
       int g0, g1;
       kgroups(p, it.ks, g0, g1);
       const uint32_t idesc = idesc_f16kind_f32(TILE_M, (uint32_t)((it.n_rows + 15) & ~15), 0u);
-      for (int kg = g0; kg < g1; ++kg) {
+      for (int kg = g0; kg < g1; ++kg, ++gc) {
+        if ((int)(gc & 1u) != mw) continue;
+        const uint32_t bi = gc % (uint32_t)p.n_b;
         if (!(ok = mbar_wait(smem_u32(&S.acc_empty[gc % G_NBUF]), ((gc / G_NBUF) & 1u) ^ 1u,
                              abort_flag, p.err)))
           break;
-        if (!(ok = mbar_wait(smem_u32(&S.a_full[ra.i]), ra.ph, abort_flag, p.err))) break;
-        if (!(ok = mbar_wait(smem_u32(&S.b_full[rb.i]), rb.ph, abort_flag, p.err))) break;
+        if (!(ok = mbar_wait(smem_u32(&S.a_full[mw]), (gc / G_NA) & 1u, abort_flag, p.err))) break;
+        if (!(ok = mbar_wait(smem_u32(&S.b_full[bi]), (gc / (uint32_t)p.n_b) & 1u, abort_flag, p.err)))
+          break;
         tc_fence_after();
-        const Ops nxt = prep(ra.i + 1 == G_NA ? 0 : ra.i + 1, rb.i + 1 == p.n_b ? 0 : rb.i + 1, gc + 1);
+        const Ops nxt = prep(gc + G_NMMA);
         if (lane == 0) {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
 #pragma unroll
             for (int m = 0; m < NMAT; ++m)
               mma_f16kind_ta(curo.d[m], curo.a[m][q], curo.b[q], idesc, q > 0 ? 1u : 0u);
-          mma_commit(smem_u32(&S.a_empty[ra.i]));
-          mma_commit(smem_u32(&S.b_empty[rb.i]));
+          mma_commit(smem_u32(&S.a_empty[mw]));
+          mma_commit(smem_u32(&S.b_empty[bi]));
           mma_commit(smem_u32(&S.acc_full[gc % G_NBUF]));
         }
         __syncwarp();
         curo = nxt;
-        ra.next();
-        rb.next();
-        ++consumed_b;
-        ++gc;
       }
     }
-    if (lane == 0) S.misc[5] = consumed_b;
   } else {
     // ================================================================ dequant + fold + epilogue
-    const int wr = warp - 2;
+    const int wr = warp - G_DQ0;
     const int quad = warp & 3;               // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;          // weight row of the tile = TMEM lane
     const int m_own = GATEUP ? (wr >> 2) : 0;
     const int j_own = GATEUP ? 0 : (wr >> 2);
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
     Ring ra{0, 0, G_NA}, rr{0, 0, p.n_raw};
-    int consumed_raw = 0;
     uint32_t it_count = 0, gc = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
@@ -340,7 +341,6 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         ra.next();
         mbar_arrive(smem_u32(&S.raw_empty[rr.i]));
         rr.next();
-        ++consumed_raw;
         // fold the group G_LAG behind this one, then queue this one
         if (np == G_LAG) {
           if (!(ok = fold(ps0, pc0))) break;
@@ -401,19 +401,25 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       }
       ++it_count;
     }
-    if (threadIdx.x == 64) S.misc[3] = consumed_raw;
   }
 
   // ------------------------------------------------------------ teardown
   __syncthreads();
   volatile int* no_abort = &S.misc[9];   // stays 0: drain waits are bounded by time only
   if (warp == 0 && lane == 0 && *abort_flag) {
-    for (int q = S.misc[3]; q < S.misc[6]; ++q)
-      mbar_wait(smem_u32(&S.raw_full[q % p.n_raw]), (uint32_t)((q / p.n_raw) & 1), no_abort, p.err);
-    for (int q = S.misc[5]; q < S.misc[8]; ++q)
-      mbar_wait(smem_u32(&S.b_full[q % p.n_b]), (uint32_t)((q / p.n_b) & 1), no_abort, p.err);
+    // for each ring slot, wait (bounded) for the last copy issued into it; an
+    // earlier copy into the same slot had landed before the slot was reused
+    const int iss_raw = S.misc[6], iss_b = S.misc[8];
+    for (int sl = 0; sl < p.n_raw && sl < iss_raw; ++sl) {
+      const int q = sl + ((iss_raw - 1 - sl) / p.n_raw) * p.n_raw;
+      mbar_wait(smem_u32(&S.raw_full[sl]), (uint32_t)((q / p.n_raw) & 1), no_abort, p.err);
+    }
+    for (int sl = 0; sl < p.n_b && sl < iss_b; ++sl) {
+      const int q = sl + ((iss_b - 1 - sl) / p.n_b) * p.n_b;
+      mbar_wait(smem_u32(&S.b_full[sl]), (uint32_t)((q / p.n_b) & 1), no_abort, p.err);
+    }
   }
-  if (warp == 1 && lane == 0) {   // every MMA this CTA issued has finished
+  if (warp >= 1 && warp < G_DQ0 && lane == 0) {   // every MMA this CTA issued has finished
     mma_commit(smem_u32(S.fin));
     mbar_wait(smem_u32(S.fin), 0, no_abort, p.err);
   }
