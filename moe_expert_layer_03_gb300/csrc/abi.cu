@@ -101,7 +101,7 @@ int choose_ksplit(int A, int E, bool has_shared, int bn, int n_mt, int F) {
 
 struct LayerLayout {
   int A, Tsh, rows, E, d, F, bn, ksplit;
-  size_t err, idx, w, counts, offsets, roa, tor, xperm, h, part, xsum, hsum, total;
+  size_t err, idx, w, counts, offsets, roa, tor, xperm, h, part, total;
 };
 
 LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* shared) {
@@ -125,9 +125,6 @@ LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* s
   L.xperm = o;    o = up1k(o + (size_t)L.rows * L.d * 2);
   L.h = o;        o = up1k(o + (size_t)L.rows * L.F * 2);
   L.part = o;     o = up1k(o + (size_t)L.ksplit * L.rows * L.d * 4);
-  const bool f16 = gemm_uses_fp16(routed->fmt);   // int4: row sums for the group-scaled loop
-  L.xsum = o;     o = up1k(o + (f16 ? (size_t)(L.d / QGROUP) * L.rows * 4 : 0));
-  L.hsum = o;     o = up1k(o + (f16 ? (size_t)(L.F / QGROUP) * L.rows * 4 : 0));
   L.total = o;
   return L;
 }
@@ -155,11 +152,10 @@ GemmArgs base_args(const moe_pool* routed, const moe_pool* shared, int* err) {
 }
 
 // gate/up (SwiGLU) then down over the row groups described by `offsets`.
-// x_rows and h are fp16 for int4 pools (with xsum/hsum their per-group row
-// sums), bf16 otherwise.
+// x_rows and h are fp16 for int4 pools, bf16 otherwise.
 moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups, int rows,
                    const moe_pool* routed, const moe_pool* shared, int bn, int ksplit, uint16_t* h,
-                   float* part, const float* xsum, float* hsum, int* err, cudaStream_t s,
+                   float* part, int* err, cudaStream_t s,
                    cudaEvent_t ev_mid, cudaEvent_t ev_down) {
   const int d = routed->d_model, F = routed->d_ff, fmt = routed->fmt;
   const bool f16 = gemm_uses_fp16(fmt);
@@ -181,8 +177,6 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
   g.out = h;
   g.out_ld = F;
   g.out_split_stride = 0;
-  g.bsum = xsum;
-  g.hsum_out = hsum;
   if (launch_grouped_gemm(fmt, true, mx, g, plan_gemm(fmt, true, bn, n_groups), grid, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev_mid && cudaEventRecord(ev_mid, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -195,8 +189,6 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
   dn.out = part;
   dn.out_ld = d;
   dn.out_split_stride = (unsigned long long)rows * d;
-  dn.bsum = hsum;
-  dn.hsum_out = nullptr;
   if (launch_grouped_gemm(fmt, false, mh, dn, plan_gemm(fmt, false, bn, n_groups), grid, s) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
@@ -243,8 +235,6 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
   uint16_t* h = (uint16_t*)(W + L.h);
   float* part = (float*)(W + L.part);
   const bool f16 = gemm_uses_fp16(routed->fmt);
-  float* xsum = f16 ? (float*)(W + L.xsum) : nullptr;
-  float* hsum = f16 ? (float*)(W + L.hsum) : nullptr;
   auto rec = [&](int i) -> bool {
     return !ev || !ev[i] || cudaEventRecord((cudaEvent_t)ev[i], s) == cudaSuccess;
   };
@@ -255,11 +245,11 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
   if (launch_permute_index(idx, T, k, E, L.Tsh, counts, offsets, roa, tor, err, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!rec(MOE_STAGE_GATHER)) return MOE_ERR_CUDA;
-  if (launch_gather_rows(x, tor, L.rows, T, L.d, xperm, f16, xsum, sm_count(), s) != cudaSuccess)
+  if (launch_gather_rows(x, tor, L.rows, T, L.d, xperm, f16, sm_count(), s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!rec(MOE_STAGE_GATE_UP)) return MOE_ERR_CUDA;
   st = run_ffn(xperm, offsets, E + (shared ? 1 : 0), L.rows, routed, shared, L.bn, L.ksplit, h, part,
-               xsum, hsum, err, s, ev ? (cudaEvent_t)ev[MOE_STAGE_DOWN] : nullptr,
+               err, s, ev ? (cudaEvent_t)ev[MOE_STAGE_DOWN] : nullptr,
                ev ? (cudaEvent_t)ev[MOE_STAGE_COMBINE] : nullptr);
   if (st != MOE_OK) return st;
   if (launch_combine_partials(part, L.ksplit, (size_t)L.rows * L.d, roa, w, T, k, L.d,
@@ -335,7 +325,7 @@ moe_status moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int k,
   if (launch_permute_index(topk_idx, T, k, E, 0, counts, offsets, row_of_assign, token_of_row, err,
                            s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (launch_gather_rows(x, token_of_row, T * k, T, d, x_perm, false, nullptr, sm_count(), s) !=
+  if (launch_gather_rows(x, token_of_row, T * k, T, d, x_perm, false, sm_count(), s) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
@@ -345,7 +335,7 @@ moe_status moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int k,
 // int4 pools, an fp16 copy of x_perm with its per-group row sums and the sums of h.
 struct FfnLayout {
   int bn, ksplit;
-  size_t h, part, x16, xsum, hsum, total;
+  size_t h, part, x16, total;
 };
 
 FfnLayout ffn_layout(int A, const moe_pool* pool) {
@@ -358,8 +348,6 @@ FfnLayout ffn_layout(int A, const moe_pool* pool) {
   L.h = o;     o = up1k(o + (size_t)A * F * 2);
   L.part = o;  o = up1k(o + (size_t)L.ksplit * A * d * 4);
   L.x16 = o;   o = up1k(o + (f16 ? (size_t)A * d * 2 : 0));
-  L.xsum = o;  o = up1k(o + (f16 ? (size_t)(d / QGROUP) * A * 4 : 0));
-  L.hsum = o;  o = up1k(o + (f16 ? (size_t)(F / QGROUP) * A * 4 : 0));
   L.total = o;
   return L;
 }
@@ -386,20 +374,16 @@ moe_status moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int A
   cudaStream_t s = (cudaStream_t)stream;
   const bool f16 = gemm_uses_fp16(pool->fmt);
   const uint16_t* rows_in = x_perm;
-  float* xsum = nullptr;
-  float* hsum = nullptr;
   if (launch_clear_word(err, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (f16) {   // the int4 GEMMs read fp16 rows and their group sums
+  if (f16) {   // the int4 GEMMs read fp16 rows
     uint16_t* x16 = (uint16_t*)(W + L.x16);
-    xsum = (float*)(W + L.xsum);
-    hsum = (float*)(W + L.hsum);
-    if (launch_gather_rows(x_perm, nullptr, A, A, pool->d_model, x16, true, xsum, sm_count(), s) !=
+    if (launch_gather_rows(x_perm, nullptr, A, A, pool->d_model, x16, true, sm_count(), s) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     rows_in = x16;
   }
-  st = run_ffn(rows_in, offsets, pool->n_experts, A, pool, nullptr, L.bn, L.ksplit, h, part, xsum,
-               hsum, err, s, nullptr, nullptr);
+  st = run_ffn(rows_in, offsets, pool->n_experts, A, pool, nullptr, L.bn, L.ksplit, h, part, err, s,
+               nullptr, nullptr);
   if (st != MOE_OK) return st;
   return launch_reduce_splits(part, L.ksplit, (size_t)A * pool->d_model, A, pool->d_model, y_perm,
                               s) == cudaSuccess

@@ -114,6 +114,32 @@ __device__ __forceinline__ void codes_of_word(uint32_t w, uint32_t* o) {
   for (int i = 0; i < 4; ++i) o[i] = lop3_and_or(w >> (4 * i), 0x000F000Fu, 0x64006400u);
 }
 
+// The 8 nibbles of a word -> 4 fp16 pairs holding q - z, exact for an integer
+// zero point z.  Pair i is (element 2i at bits [4i, 4i+4), element 2i+1 at bits
+// [16+4i, 20+4i)).  A nibble masked into the low mantissa bits of the fp16
+// pattern of 1024 (0x6400) reads as 1024 + q (bits 0-3) or 1024 + 16q (bits
+// 4-7); the upper two nibbles of each half are shifted down by 8 first.  One
+// fp16 add (or FMA with 1/16) then removes the offset and the zero:
+// nz_a = -(1024 + z), nz_b = -(64 + z).  Every intermediate is an integer
+// below 2048, so no step rounds.
+__device__ __forceinline__ uint32_t h2_add(uint32_t a, uint32_t b) {
+  const __half2 r = __hadd2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
+                            *reinterpret_cast<const __half2*>(&c));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ void codes_minus_zero(uint32_t w, uint32_t nz_a, uint32_t nz_b, uint32_t* o) {
+  constexpr uint32_t SIXTEENTH = 0x2C002C00u;   // fp16 1/16 in both halves
+  const uint32_t hi = w >> 8;
+  o[0] = h2_add(lop3_and_or(w, 0x000F000Fu, 0x64006400u), nz_a);
+  o[1] = h2_fma(lop3_and_or(w, 0x00F000F0u, 0x64006400u), SIXTEENTH, nz_b);
+  o[2] = h2_add(lop3_and_or(hi, 0x000F000Fu, 0x64006400u), nz_a);
+  o[3] = h2_fma(lop3_and_or(hi, 0x00F000F0u, 0x64006400u), SIXTEENTH, nz_b);
+}
+
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 __device__ __forceinline__ __half to_half_sat(float v) {

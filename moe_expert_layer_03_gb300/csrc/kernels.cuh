@@ -65,11 +65,6 @@ struct GemmArgs {
   int out_ld;                           // elements per output row
   unsigned long long out_split_stride;  // elements between K-split partial buffers
   int* err;                             // device error word
-  // int4 group-scaled main loop (see gemm.cu): per (quantisation group, row)
-  // sums of the B operand rows [K/128][rows_total], and, for gate/up, where to
-  // write the same sums of h for the down GEMM [F/128][rows_total].
-  const float* bsum;
-  float* hsum_out;
   int n_a, n_b, n_raw;                  // pipeline depths
   uint32_t tmem_cols;                   // TMEM columns (power of two >= 32)
 };
@@ -98,11 +93,9 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_
                                  int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
                                  int32_t* token_of_row, int* err, cudaStream_t s);
 // x_perm[r] = x[token_of_row[r]].  to_fp16: write fp16 (saturating) instead of
-// bf16 and, if xsum != nullptr, the per-(128-group, row) sums of the fp16 row
-// values into xsum [d/128][rows].
+// bf16.  token_of_row == nullptr: x_perm[r] = x[r].
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
-                               int d, uint16_t* x_perm, bool to_fp16, float* xsum, int n_sm,
-                               cudaStream_t s);
+                               int d, uint16_t* x_perm, bool to_fp16, int n_sm, cudaStream_t s);
 cudaError_t launch_combine_partials(const float* part, int n_split, size_t split_stride,
                                     const int32_t* row_of_assign, const float* topk_w, int T,
                                     int k, int d, int shared_row0, uint16_t* out, cudaStream_t s);

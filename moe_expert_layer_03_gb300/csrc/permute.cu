@@ -136,22 +136,18 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
 }
 
 // bf16 -> fp16 (saturating) pair
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u, float& sum) {
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
   const float a = fminf(fmaxf(__uint_as_float(u << 16), -65504.f), 65504.f);
   const float b = fminf(fmaxf(__uint_as_float(u & 0xFFFF0000u), -65504.f), 65504.f);
   const __half2 h = __floats2half2_rn(a, b);
-  const float2 back = __half22float2(h);
-  sum += back.x + back.y;
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Same gather, converting to fp16 (token_of_row == nullptr: row r of x, a plain
-// conversion); lanes 0-15 cover one 128-element group and lanes 16-31 the next,
-// so each half-warp also reduces its group's sum.
+// conversion).
 __global__ void __launch_bounds__(256)
     gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ token_of_row,
-                           int rows, int T, int d, uint16_t* __restrict__ x_perm,
-                           float* __restrict__ xsum) {
+                           int rows, int T, int d, uint16_t* __restrict__ x_perm) {
   const int lane = threadIdx.x & 31;
   const int nvec = d / 8;
   for (int r = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); r < rows;
@@ -160,22 +156,16 @@ __global__ void __launch_bounds__(256)
     const bool valid = (t >= 0 && t < T);
     uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * d);
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(valid ? t : 0) * d);
-    for (int base = 0; base < nvec; base += 32) {   // every lane runs every iteration
-      const int i = base + lane;
-      const bool act = i < nvec;                      // nvec % 16 == 0: whole half-warps
-      float sum = 0.f;
+    for (int i = lane; i < nvec; i += 32) {
       uint4 o = make_uint4(0, 0, 0, 0);
-      if (valid && act) {
+      if (valid) {
         const uint4 v = __ldg(src + i);
-        o.x = bf16x2_to_f16x2(v.x, sum);
-        o.y = bf16x2_to_f16x2(v.y, sum);
-        o.z = bf16x2_to_f16x2(v.z, sum);
-        o.w = bf16x2_to_f16x2(v.w, sum);
+        o.x = bf16x2_to_f16x2(v.x);
+        o.y = bf16x2_to_f16x2(v.y);
+        o.z = bf16x2_to_f16x2(v.z);
+        o.w = bf16x2_to_f16x2(v.w);
       }
-      if (act) dst[i] = o;
-#pragma unroll
-      for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      if (act && xsum != nullptr && (lane & 15) == 0) xsum[(size_t)(i >> 4) * rows + r] = sum;
+      dst[i] = o;
     }
   }
 }
@@ -189,13 +179,12 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
-                               int d, uint16_t* x_perm, bool to_fp16, float* xsum, int n_sm,
-                               cudaStream_t s) {
+                               int d, uint16_t* x_perm, bool to_fp16, int n_sm, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   int blocks = (rows + 7) / 8;   // 8 warps (rows) per block
   if (blocks > 4 * n_sm) blocks = 4 * n_sm;
   if (to_fp16)
-    gather_rows_f16_kernel<<<blocks, 256, 0, s>>>(x, token_of_row, rows, T, d, x_perm, xsum);
+    gather_rows_f16_kernel<<<blocks, 256, 0, s>>>(x, token_of_row, rows, T, d, x_perm);
   else
     gather_rows_kernel<<<blocks, 256, 0, s>>>(x, token_of_row, rows, T, d, x_perm);
   return cudaGetLastError();

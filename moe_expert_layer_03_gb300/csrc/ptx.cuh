@@ -52,6 +52,18 @@ MOE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test: true if the phase with the given parity has completed.
+MOE_DEV bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Same, letting the hardware suspend the thread (up to ~the hint, in ns) until
 // the phase completes instead of returning at once: waiting warps stop taking
 // issue slots from the working ones.
@@ -189,11 +201,47 @@ MOE_DEV void mma_f16kind_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, ui
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same MMAs issued from a converged warp: every lane executes the call and
+// elect.sync picks the one that issues.  Keeping the warp converged lets the
+// compiler treat the operands as warp-uniform, which makes back-to-back issue of
+// small-N MMAs several times cheaper than issuing from a lane-0 branch.
+MOE_DEV void mma_ta_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Two MMAs sharing the B operand (e.g. the gate and up rows of one K step).
+MOE_DEV void mma2_ta_elect(uint32_t d0, uint32_t d1, uint32_t a0, uint32_t a1, uint64_t bdesc,
+                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %4, %5, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [%3], %4, %5, p;\n\t}" ::"r"(d0),
+      "r"(d1), "r"(a0), "r"(a1), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives once on `bar` when every tcgen05 op this thread issued so far is done.
 MOE_DEV void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    bar)
                : "memory");
+}
+
+// mma_commit from a converged warp (one elected lane commits).
+MOE_DEV void mma_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
 }
 
 // 32 lanes x 16 consecutive 32-bit columns: thread i of the warp receives
@@ -216,6 +264,14 @@ MOE_DEV void tmem_ld_8(uint32_t taddr, uint32_t (&r)[8]) {
       : "r"(taddr));
 }
 MOE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// wait::ld, then tie the loaded registers to it so that no use of them can be
+// scheduled above the wait.
+template <int N>
+MOE_DEV void tmem_ld_wait_regs(uint32_t (&r)[N]) {
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
 
 // Registers -> tensor memory: thread i of the warp writes lane (quadrant*32 + i),
 // 32 (or 16) consecutive 32-bit columns starting at the address's column.
