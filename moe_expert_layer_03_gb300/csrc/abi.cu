@@ -18,6 +18,7 @@ constexpr int MAX_A = 1 << 20;
 constexpr int MAX_DIM = 32768;
 constexpr int TARGET_ITEMS = 640;   // down-GEMM work items to aim for when picking a K split
 constexpr int MAX_KSPLIT = 8;
+constexpr int SPLIT_GRID = 152;     // persistent CTAs the decode split is balanced for (GB300 SMs)
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -87,15 +88,30 @@ int choose_bn(int A, int E) {
   return bn;
 }
 
-int choose_ksplit(int A, int E, bool has_shared, int bn, int n_mt, int F) {
+// K split of the down GEMM.  Decode (group kernel): the split whose items
+// spread most evenly over the persistent CTAs (fewest quantisation groups on
+// the busiest CTA; its fp32 partials are small).  Otherwise: enough items to
+// fill the GPU, as few splits as that allows (partials of long batches are
+// large).
+int choose_ksplit(int A, int E, bool has_shared, int bn, int fmt, int d, int F) {
   const int active = (A < E ? A : E) + (has_shared ? 1 : 0);
   const int mean = (A + E - 1) / E;
   const int nch = mean > bn ? (mean + bn - 1) / bn : 1;
-  const long items = (long)active * n_mt * nch;
-  int s = (int)((TARGET_ITEMS + items - 1) / items);
   const int G = F / QGROUP;
-  if (s > MAX_KSPLIT) s = MAX_KSPLIT;
-  if (s > G) s = G;
+  const int smax = MAX_KSPLIT < G ? MAX_KSPLIT : G;
+  const long items = (long)active * down_work_tiles(fmt, bn, d / TILE_M) * nch;
+  if (gemm_is_group(fmt, bn)) {
+    int best_s = 1;
+    long best = -1;
+    for (int s = 1; s <= smax; ++s) {
+      const long waves = (items * s + SPLIT_GRID - 1) / SPLIT_GRID;
+      const long cost = waves * ((G + s - 1) / s);
+      if (best < 0 || cost < best) { best = cost; best_s = s; }
+    }
+    return best_s;
+  }
+  int s = (int)((TARGET_ITEMS + items - 1) / items);
+  if (s > smax) s = smax;
   return s < 1 ? 1 : s;
 }
 
@@ -113,7 +129,7 @@ LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* s
   L.d = routed->d_model;
   L.F = routed->d_ff;
   L.bn = choose_bn(L.A, L.E);
-  L.ksplit = choose_ksplit(L.A, L.E, shared != nullptr, L.bn, L.d / TILE_M, L.F);
+  L.ksplit = choose_ksplit(L.A, L.E, shared != nullptr, L.bn, routed->fmt, L.d, L.F);
   size_t o = 0;
   L.err = o;      o += 1024;
   L.idx = o;      o = up1k(o + (size_t)L.A * 4);
@@ -177,7 +193,7 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
   g.out = h;
   g.out_ld = F;
   g.out_split_stride = 0;
-  if (launch_grouped_gemm(fmt, true, mx, g, plan_gemm(fmt, true, bn, n_groups), grid, s) != cudaSuccess)
+  if (launch_grouped_gemm(fmt, true, mx, g, plan_gemm(fmt, true, bn, n_groups, F / TILE_M), grid, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev_mid && cudaEventRecord(ev_mid, s) != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -189,7 +205,7 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
   dn.out = part;
   dn.out_ld = d;
   dn.out_split_stride = (unsigned long long)rows * d;
-  if (launch_grouped_gemm(fmt, false, mh, dn, plan_gemm(fmt, false, bn, n_groups), grid, s) !=
+  if (launch_grouped_gemm(fmt, false, mh, dn, plan_gemm(fmt, false, bn, n_groups, d / TILE_M), grid, s) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev_down && cudaEventRecord(ev_down, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -342,7 +358,7 @@ FfnLayout ffn_layout(int A, const moe_pool* pool) {
   FfnLayout L{};
   const int d = pool->d_model, F = pool->d_ff;
   L.bn = choose_bn(A, pool->n_experts);
-  L.ksplit = choose_ksplit(A, pool->n_experts, false, L.bn, d / TILE_M, F);
+  L.ksplit = choose_ksplit(A, pool->n_experts, false, L.bn, pool->fmt, d, F);
   const bool f16 = gemm_uses_fp16(pool->fmt);
   size_t o = 1024;
   L.h = o;     o = up1k(o + (size_t)A * F * 2);

@@ -389,16 +389,17 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
 }
 
 // ------------------------------------------------------------------ host side
-GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups);
+GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups, int n_mt);
 cudaError_t launch_grouped_gemm_group(bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
                                       const GemmPlan& plan, int grid, cudaStream_t stream);
 
-GemmPlan plan_gemm(int fmt, bool gateup, int bn, int n_groups) {
+GemmPlan plan_gemm(int fmt, bool gateup, int bn, int n_groups, int n_mt) {
   const bool int4 = fmt == MOE_W_INT4_G128;
-  if (int4 && bn <= 32) return plan_gemm_group(gateup, bn, n_groups);
+  if (gemm_is_group(fmt, bn)) return plan_gemm_group(gateup, bn, n_groups, n_mt);
   GemmPlan pl{};
   const int nmat = gateup ? 2 : 1;
   pl.group = false;
+  pl.pair = false;
   pl.ndq = int4 ? 8 : 4;
   const size_t budget = 227 * 1024 - 1024;   // opt-in maximum minus the alignment pad
   pl.n_b = bn >= 128 ? 3 : (bn >= 64 ? 4 : 8);

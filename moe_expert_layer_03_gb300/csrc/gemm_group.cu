@@ -29,9 +29,12 @@
 //     also frees that group's A stage and pipeline stage.
 //
 //   warp 0   producer (bulk copy + TMA), warps 1-2 MMA issuers (warp 1 owns
-//   TMEM), warps 3-10 unpack + fold + epilogue (two warps per TMEM lane
-//   quadrant: gate/up -> one warp per (matrix, quadrant); down -> the two
-//   warps of a quadrant split each row's K quads and the accumulator columns).
+//   TMEM), warps 3-10 unpack + fold + epilogue, two warps per TMEM lane
+//   quadrant.  Modes: gate/up (the stage holds the gate and up rows of one
+//   output tile; SwiGLU epilogue), paired down (two adjacent 128-row output
+//   tiles sharing the token tile), single down (one tile; the two warps of a
+//   quadrant split each row's K quads and the accumulator columns).  In the
+//   two-matrix modes each dequant warp owns one (matrix, quadrant).
 //
 // Every wait is bounded; on a timeout the CTA drains its copies and MMAs,
 // frees TMEM and returns with MOE_DEVERR_TIMEOUT set.
@@ -51,6 +54,8 @@ constexpr int G_NDQ = 8;
 constexpr int G_DQ0 = 1 + G_NMMA;                  // first dequant warp
 constexpr int G_THREADS = (1 + G_NMMA + G_NDQ) * 32;
 
+enum GroupMode { G_GATEUP = 0, G_DOWN_PAIR = 1, G_DOWN = 2 };
+
 struct GShared {
   uint8_t* b_ring;     // [n_st][2 * bn * 128]  token rows, SW128 K-major (1024-aligned stages)
   uint8_t* raw_ring;   // [n_st][nmat * I4_MAT_BYTES]  nibbles + scale/zero words
@@ -60,9 +65,9 @@ struct GShared {
   WorkList W;
 };
 
-size_t group_carve_bytes(int nmat, int bn, int n_st, int n_groups) {
+size_t group_carve_bytes(int nmat, bool xch, int bn, int n_st, int n_groups) {
   size_t s = (size_t)n_st * ((size_t)bn * 256 + (size_t)nmat * I4_MAT_BYTES);
-  s += (nmat == 2 ? (size_t)TILE_M * bn * 4 : 0);
+  s += (xch ? (size_t)TILE_M * bn * 4 : 0);
   s = align_up(s, 16);
   s += 8 * (size_t)(2 * n_st + G_NA + G_NBUF + 2 + 1);
   s += 4 * (G_MISC + worklist_ints(n_groups));
@@ -71,11 +76,13 @@ size_t group_carve_bytes(int nmat, int bn, int n_st, int n_groups) {
 
 }  // namespace
 
-template <bool GATEUP, int GBN>
+template <int MODE, int GBN>
 __global__ void __launch_bounds__(G_THREADS, 1)
     grouped_gemm_group_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs p) {
-  constexpr int NMAT = GATEUP ? 2 : 1;
-  constexpr int CW = GATEUP ? GBN : GBN / 2;           // accumulator columns per dequant thread
+  constexpr bool GATEUP = MODE == G_GATEUP;
+  constexpr bool PAIR = MODE != G_DOWN;                // two 128-row matrices per stage
+  constexpr int NMAT = PAIR ? 2 : 1;
+  constexpr int CW = PAIR ? GBN : GBN / 2;             // accumulator columns per dequant thread
   constexpr uint32_t RAW_STAGE = NMAT * I4_MAT_BYTES;
   constexpr uint32_t A_COLS = NMAT * (QGROUP / 2);     // TMEM columns of one A stage
   constexpr uint32_t B_HALF = (uint32_t)GBN * 128u;    // one 64-wide K slice of the token rows
@@ -90,7 +97,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   S.raw_ring = S.b_ring + (size_t)n_st * B_STAGE;
   uint8_t* cur = S.raw_ring + (size_t)n_st * RAW_STAGE;
   S.xch = reinterpret_cast<float*>(cur);
-  cur += (NMAT == 2 ? (size_t)TILE_M * GBN * 4 : 0);
+  cur += (GATEUP ? (size_t)TILE_M * GBN * 4 : 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + align_up((size_t)(cur - base), 16));
   S.full = bars;
   S.empty = S.full + n_st;
@@ -139,7 +146,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   if (warp == 0) {
     // ================================================================ producer
     // Per group one stage: the NMAT nibble blocks and the two 64-wide K
-    // slices of the token rows, on one barrier.
+    // slices of the token rows, on one barrier.  In the paired down mode the
+    // item's tile index mt names the output tiles 2mt and 2mt + 1.
     if (lane == 0) {
       Ring rs{0, 0, n_st};
       int issued = 0;
@@ -156,8 +164,16 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           const uint32_t bar = smem_u32(&S.full[rs.i]);
           mbar_arrive_expect_tx(bar, RAW_STAGE + B_STAGE);
           const uint32_t raw = smem_u32(S.raw_ring + (size_t)rs.i * RAW_STAGE);
-          bulk_g2s_hint(raw, sec + ((size_t)it.mt * (p.K / QGROUP) + kg) * RAW_STAGE, RAW_STAGE, bar,
-                        pol);
+          if (MODE == G_DOWN_PAIR) {
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+              bulk_g2s_hint(raw + m * I4_MAT_BYTES,
+                            sec + ((size_t)(2 * it.mt + m) * (p.K / QGROUP) + kg) * I4_MAT_BYTES,
+                            I4_MAT_BYTES, bar, pol);
+          } else {
+            bulk_g2s_hint(raw, sec + ((size_t)it.mt * (p.K / QGROUP) + kg) * RAW_STAGE, RAW_STAGE, bar,
+                          pol);
+          }
           const uint32_t dst = smem_u32(S.b_ring + (size_t)rs.i * B_STAGE);
           tma_load_2d(dst, &tmap_b, (2 * kg) * KSTEP, it.r0, bar);
           tma_load_2d(dst + B_HALF, &tmap_b, (2 * kg + 1) * KSTEP, it.r0, bar);
@@ -216,8 +232,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const int wr = warp - G_DQ0;
     const int quad = warp & 3;               // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;          // weight row of the tile = TMEM lane
-    const int m_own = GATEUP ? (wr >> 2) : 0;
-    const int j_own = GATEUP ? 0 : (wr >> 2);
+    const int m_own = PAIR ? (wr >> 2) : 0;
+    const int j_own = PAIR ? 0 : (wr >> 2);
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
     constexpr int CH = (CW % 16 == 0) ? 16 : 8;   // columns per tcgen05.ld
     Ring rs{0, 0, n_st};
@@ -228,7 +244,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       if (!decode_item(item, p, S.W, it)) continue;
       int g0, g1;
       kgroups(p, it.ks, g0, g1);
-      const int cbeg = GATEUP ? 0 : j_own * (GBN / 2);
+      const int cbeg = PAIR ? 0 : j_own * (GBN / 2);
       const int nc = max(0, min(CW, it.n_rows - cbeg));
       float acc[CW];
 #pragma unroll
@@ -284,7 +300,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         const uint32_t ta = lane_base + (uint32_t)j * A_COLS + (uint32_t)(m_own * (QGROUP / 2));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {   // K halves of the group: 64 codes of my row each
-          if (GATEUP) {
+          if (PAIR) {
             uint32_t v[32];
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
@@ -360,7 +376,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           break;
       } else {
         float* y = reinterpret_cast<float*>(p.out) + (size_t)it.ks * p.out_split_stride;
-        const int f = it.mt * TILE_M + r;
+        const int f = (MODE == G_DOWN_PAIR ? 2 * it.mt + m_own : it.mt) * TILE_M + r;
 #pragma unroll
         for (int i = 0; i < CW; ++i)
           if (i < nc) y[(size_t)(it.r0 + cbeg + i) * p.out_ld + f] = acc[i];
@@ -392,18 +408,19 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ host side
-GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups) {
+GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups, int n_mt) {
   GemmPlan pl{};
-  const int nmat = gateup ? 2 : 1;
   pl.group = true;
+  pl.pair = !gateup && n_mt % 2 == 0;
+  const int nmat = (gateup || pl.pair) ? 2 : 1;
   pl.ndq = G_NDQ;
   pl.n_a = G_NA;
   const size_t budget = 227 * 1024 - 1024;
   int n_st = 3;
-  while (n_st < 16 && group_carve_bytes(nmat, bn, n_st + 1, n_groups) <= budget) ++n_st;
+  while (n_st < 16 && group_carve_bytes(nmat, gateup, bn, n_st + 1, n_groups) <= budget) ++n_st;
   pl.n_raw = n_st;   // stages (nibbles + token rows)
   pl.n_b = n_st;
-  pl.smem_bytes = group_carve_bytes(nmat, bn, n_st, n_groups) + 1024;
+  pl.smem_bytes = group_carve_bytes(nmat, gateup, bn, n_st, n_groups) + 1024;
   const uint32_t need = (uint32_t)(G_NA * nmat * (QGROUP / 2) + G_NBUF * nmat * bn);
   uint32_t cols = 32;
   while (cols < need) cols <<= 1;
@@ -411,10 +428,10 @@ GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups) {
   return pl;
 }
 
-template <bool GATEUP, int GBN>
+template <int MODE, int GBN>
 static cudaError_t launch_group_one(const CUtensorMap& tmap, const GemmArgs& a, const GemmPlan& pl,
                                     int grid, cudaStream_t s) {
-  auto kern = grouped_gemm_group_kernel<GATEUP, GBN>;
+  auto kern = grouped_gemm_group_kernel<MODE, GBN>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -425,17 +442,25 @@ static cudaError_t launch_group_one(const CUtensorMap& tmap, const GemmArgs& a, 
   return cudaGetLastError();
 }
 
+template <int MODE>
+static cudaError_t launch_group_mode(const CUtensorMap& tmap, const GemmArgs& a, const GemmPlan& pl,
+                                     int grid, cudaStream_t s) {
+  return a.bn == 16 ? launch_group_one<MODE, 16>(tmap, a, pl, grid, s)
+                    : launch_group_one<MODE, 32>(tmap, a, pl, grid, s);
+}
+
 cudaError_t launch_grouped_gemm_group(bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
                                       const GemmPlan& plan, int grid, cudaStream_t stream) {
   args.n_a = plan.n_a;
   args.n_b = plan.n_b;
   args.n_raw = plan.n_raw;
   args.tmem_cols = plan.tmem_cols;
-  if (args.bn == 16)
-    return gateup ? launch_group_one<true, 16>(tmap_b, args, plan, grid, stream)
-                  : launch_group_one<false, 16>(tmap_b, args, plan, grid, stream);
-  return gateup ? launch_group_one<true, 32>(tmap_b, args, plan, grid, stream)
-                : launch_group_one<false, 32>(tmap_b, args, plan, grid, stream);
+  if (gateup) return launch_group_mode<G_GATEUP>(tmap_b, args, plan, grid, stream);
+  if (plan.pair) {
+    args.n_mt /= 2;   // work items name pairs of output tiles
+    return launch_group_mode<G_DOWN_PAIR>(tmap_b, args, plan, grid, stream);
+  }
+  return launch_group_mode<G_DOWN>(tmap_b, args, plan, grid, stream);
 }
 
 }  // namespace moe

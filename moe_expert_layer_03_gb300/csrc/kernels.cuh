@@ -71,6 +71,7 @@ struct GemmArgs {
 
 struct GemmPlan {
   bool group;         // int4 group-scaled main loop (row chunks of <= 32)
+  bool pair;          // group loop, down GEMM: two 128-row output tiles per stage
   int ndq;            // dequant / epilogue warps
   int n_a, n_b, n_raw;
   size_t smem_bytes;
@@ -81,7 +82,15 @@ struct GemmPlan {
 // layers on bf16 operands.
 inline bool gemm_uses_fp16(int fmt) { return fmt == MOE_W_INT4_G128; }
 
-GemmPlan plan_gemm(int fmt, bool gateup, int bn, int n_groups);
+// Uses the group-scaled decode kernel (int4, row chunks of <= 32)?
+inline bool gemm_is_group(int fmt, int bn) { return fmt == MOE_W_INT4_G128 && bn <= 32; }
+// Work tiles per (group, row chunk, K split) of the down GEMM with n_mt output
+// tiles: the decode kernel pairs adjacent tiles when n_mt is even.
+inline int down_work_tiles(int fmt, int bn, int n_mt) {
+  return gemm_is_group(fmt, bn) && n_mt % 2 == 0 ? n_mt / 2 : n_mt;
+}
+
+GemmPlan plan_gemm(int fmt, bool gateup, int bn, int n_groups, int n_mt);
 cudaError_t launch_grouped_gemm(int fmt, bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
                                 const GemmPlan& plan, int grid, cudaStream_t stream);
 
