@@ -11,30 +11,31 @@
 //   * one pipeline stage = one quantisation group (128 K): one bulk copy of
 //     nibbles + scales and one TMA pair for the token rows, all on one
 //     barrier; 8 K16 steps of M = 128 weight rows x N = 16/32 token rows;
-//   * the A operand lives in tensor memory: each dequant thread owns one weight
-//     row (one TMEM lane) and writes the group's 128 codes with tcgen05.st,
-//     so shared memory carries only the nibbles and the small token tiles;
+//   * the A operand lives in tensor memory: each unpack thread owns one weight
+//     row (one TMEM lane) and writes the group's codes with tcgen05.st, so
+//     shared memory carries only the nibbles and the small token tiles;
 //   * the codes are q - z, exact in fp16 (a LOP3 into the fp16 pattern of
 //     1024, then one fp16 add or FMA); each group accumulates into its own
-//     TMEM slice and the dequant warps fold it, two groups later, into fp32
-//     registers with the group's scale:  acc += s * D_g;
-//   * two MMA warps take alternate groups (each group has its own A stage
-//     and accumulator slice, so they never touch the same TMEM) and issue
-//     from a converged warp (elect.sync): the issue rate of the MMA warps, not
-//     the tensor core, bounds small-N MMAs;
-//   * few waits per group: the MMA warp waits only for its A stage (which
-//     implies that the stage's token tile has landed and that the slice it
-//     overwrites was folded); the dequant warps wait for the stage (tested
-//     one group ahead) and for the accumulator of the group two back, which
-//     also frees that group's A stage and pipeline stage.
+//     TMEM slice, folded into fp32 registers with the group's scale:
+//     acc += s * D_g;
+//   * the warps that feed the MMAs (unpack) and the warps that consume them
+//     (fold + epilogue) are separate, each running a short per-group chain:
+//     unpack waits for the stage and a free A slot, fold waits for the
+//     group's accumulator; item epilogues never stall the unpacking;
+//   * two MMA warps take alternate groups and issue from a converged warp
+//     (elect.sync): their issue rate, not the tensor core, bounds small-N
+//     MMAs; 3 A slots where tensor memory allows (2 otherwise).
 //
-//   warp 0   producer (bulk copy + TMA), warps 1-2 MMA issuers (warp 1 owns
-//   TMEM), warps 3-10 unpack + fold + epilogue, two warps per TMEM lane
-//   quadrant.  Modes: gate/up (the stage holds the gate and up rows of one
-//   output tile; SwiGLU epilogue), paired down (two adjacent 128-row output
-//   tiles sharing the token tile), single down (one tile; the two warps of a
-//   quadrant split each row's K quads and the accumulator columns).  In the
-//   two-matrix modes each dequant warp owns one (matrix, quadrant).
+//   warp 0       producer (bulk copy + TMA)
+//   warps 1-2    MMA issuers (warp 1 owns TMEM)
+//   warps 3-10   unpack, two per TMEM lane quadrant: in the two-matrix modes
+//                each writes one matrix's codes for its quadrant's rows, in
+//                single down each writes one K quad of each half
+//   warps 11-14  fold + epilogue, one per quadrant: every matrix and token
+//                column of its 32 rows
+// Modes: gate/up (a stage holds the gate and up rows of one output tile;
+// SwiGLU epilogue), paired down (two adjacent 128-row output tiles sharing the
+// token tile), single down (one tile).
 //
 // Every wait is bounded; on a timeout the CTA drains its copies and MMAs,
 // frees TMEM and returns with MOE_DEVERR_TIMEOUT set.
@@ -47,31 +48,38 @@ using namespace gemm;
 namespace {
 
 constexpr int G_NBUF = 4;     // accumulator slices: group g uses slice g % 4
-constexpr int G_NA = 2;       // A stages in tensor memory, one per MMA warp
+constexpr int G_MAX_NA = 3;   // A slots in tensor memory (3 where the columns allow)
 constexpr int G_MISC = 8;     // [0] tmem [1] abort [2] items [3] stages issued [4] stays 0
 constexpr int G_NMMA = 2;     // MMA-issuing warps (alternate groups)
-constexpr int G_NDQ = 8;
-constexpr int G_DQ0 = 1 + G_NMMA;                  // first dequant warp
-constexpr int G_THREADS = (1 + G_NMMA + G_NDQ) * 32;
+constexpr int G_NUP = 8;      // unpack warps
+constexpr int G_NFOLD = 4;    // fold + epilogue warps
+constexpr int G_UP0 = 1 + G_NMMA;                  // first unpack warp
+constexpr int G_FOLD0 = G_UP0 + G_NUP;             // first fold warp
+constexpr int G_THREADS = (G_FOLD0 + G_NFOLD) * 32;
 
 enum GroupMode { G_GATEUP = 0, G_DOWN_PAIR = 1, G_DOWN = 2 };
 
 struct GShared {
   uint8_t* b_ring;     // [n_st][2 * bn * 128]  token rows, SW128 K-major (1024-aligned stages)
   uint8_t* raw_ring;   // [n_st][nmat * I4_MAT_BYTES]  nibbles + scale/zero words
-  float* xch;          // gate/up: up accumulators handed to the gate threads [bn][128]
-  uint64_t *full, *empty, *a_full, *acc_full, *xch_bar, *fin;
+  uint64_t *full, *empty;          // stages: producer -> consumers, consumers -> producer
+  uint64_t *a_full, *a_empty;      // A slots: unpack -> MMA, MMA (commit) -> unpack
+  uint64_t *acc_full, *acc_empty;  // accumulator slices: MMA (commit) -> fold, fold -> MMA
+  uint64_t* fin;
   int* misc;
   WorkList W;
 };
 
-size_t group_carve_bytes(int nmat, bool xch, int bn, int n_st, int n_groups) {
+size_t group_carve_bytes(int nmat, int bn, int n_st, int n_groups) {
   size_t s = (size_t)n_st * ((size_t)bn * 256 + (size_t)nmat * I4_MAT_BYTES);
-  s += (xch ? (size_t)TILE_M * bn * 4 : 0);
   s = align_up(s, 16);
-  s += 8 * (size_t)(2 * n_st + G_NA + G_NBUF + 2 + 1);
+  s += 8 * (size_t)(2 * n_st + 2 * G_MAX_NA + 2 * G_NBUF + 1);
   s += 4 * (G_MISC + worklist_ints(n_groups));
   return s;
+}
+
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err));
 }
 
 }  // namespace
@@ -82,12 +90,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   constexpr bool GATEUP = MODE == G_GATEUP;
   constexpr bool PAIR = MODE != G_DOWN;                // two 128-row matrices per stage
   constexpr int NMAT = PAIR ? 2 : 1;
-  constexpr int CW = PAIR ? GBN : GBN / 2;             // accumulator columns per dequant thread
   constexpr uint32_t RAW_STAGE = NMAT * I4_MAT_BYTES;
-  constexpr uint32_t A_COLS = NMAT * (QGROUP / 2);     // TMEM columns of one A stage
+  constexpr uint32_t A_COLS = NMAT * (QGROUP / 2);     // TMEM columns of one A slot
   constexpr uint32_t B_HALF = (uint32_t)GBN * 128u;    // one 64-wide K slice of the token rows
   constexpr uint32_t B_STAGE = 2u * B_HALF;
   const int n_st = p.n_raw;
+  const uint32_t n_a = (uint32_t)p.n_a;
 
   extern __shared__ uint8_t smem_dyn[];
   const uint32_t pad = (1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u;
@@ -96,15 +104,14 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   S.b_ring = base;
   S.raw_ring = S.b_ring + (size_t)n_st * B_STAGE;
   uint8_t* cur = S.raw_ring + (size_t)n_st * RAW_STAGE;
-  S.xch = reinterpret_cast<float*>(cur);
-  cur += (GATEUP ? (size_t)TILE_M * GBN * 4 : 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + align_up((size_t)(cur - base), 16));
   S.full = bars;
   S.empty = S.full + n_st;
   S.a_full = S.empty + n_st;
-  S.acc_full = S.a_full + G_NA;
-  S.xch_bar = S.acc_full + G_NBUF;
-  S.fin = S.xch_bar + 2;
+  S.a_empty = S.a_full + G_MAX_NA;
+  S.acc_full = S.a_empty + G_MAX_NA;
+  S.acc_empty = S.acc_full + G_NBUF;
+  S.fin = S.acc_empty + G_NBUF;
   S.misc = reinterpret_cast<int*>(S.fin + 1);
   S.W.prefix = S.misc + G_MISC;
   S.W.nch = S.W.prefix + (p.n_groups + 1);
@@ -117,14 +124,19 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < n_st; ++i) {
       mbar_init(smem_u32(&S.full[i]), 1);
-      mbar_init(smem_u32(&S.empty[i]), G_NDQ * 32);
+      mbar_init(smem_u32(&S.empty[i]), (G_NUP + G_NFOLD) * 32);
     }
-    for (int i = 0; i < G_NA; ++i) mbar_init(smem_u32(&S.a_full[i]), G_NDQ * 32);
-    for (int i = 0; i < G_NBUF; ++i) mbar_init(smem_u32(&S.acc_full[i]), 1);
-    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&S.xch_bar[i]), G_NDQ * 32);
+    for (int i = 0; i < G_MAX_NA; ++i) {
+      mbar_init(smem_u32(&S.a_full[i]), G_NUP * 32);
+      mbar_init(smem_u32(&S.a_empty[i]), 1);
+    }
+    for (int i = 0; i < G_NBUF; ++i) {
+      mbar_init(smem_u32(&S.acc_full[i]), 1);
+      mbar_init(smem_u32(&S.acc_empty[i]), G_NFOLD * 32);
+    }
     mbar_init(smem_u32(S.fin), G_NMMA);
     for (int i = 1; i < G_MISC; ++i)
-      if (i != 2) S.misc[i] = 0;   // [0] written by tcgen05.alloc, [2] by the first dequant warp
+      if (i != 2) S.misc[i] = 0;   // [0] written by tcgen05.alloc, [2] by the first unpack warp
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) prefetch_tensormap(&tmap_b);
@@ -132,7 +144,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     tmem_alloc(smem_u32(&S.misc[0]), p.tmem_cols);
     tmem_relinquish();
   }
-  if (warp == G_DQ0) {
+  if (warp == G_UP0) {
     const int total = build_worklist(p, S.W, lane);
     if (lane == 0) S.misc[2] = total;
   }
@@ -141,7 +153,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = (uint32_t)S.misc[0];
   const int total = S.misc[2];
-  const uint32_t acc0 = (uint32_t)G_NA * A_COLS;   // accumulator slices follow the A stages
+  const uint32_t acc0 = n_a * A_COLS;   // accumulator slices follow the A slots
 
   if (warp == 0) {
     // ================================================================ producer
@@ -183,18 +195,16 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       }
       S.misc[3] = issued;
     }
-  } else if (warp < G_DQ0) {
+  } else if (warp < G_UP0) {
     // ================================================================ MMA issuers
-    // Warp 1 + mw issues the groups with (group counter % 2) == mw into A
-    // stage mw.  Its only wait is that stage's a_full: the dequant threads
-    // arrive there after the group's stage barrier completed (so the token
-    // tile has landed) and after folding the group four back (so the
-    // accumulator slice is free).  The whole warp runs the loop.
+    // Warp 1 + mw issues the groups with (group counter % 2) == mw.  Group gc
+    // uses A slot gc % n_a and accumulator slice gc % 4.  a_full(gc) also
+    // implies that the group's stage (token tile) has landed: the unpack
+    // threads arrive only after seeing it.  The whole warp runs the loop.
     const int mw = warp - 1;
     uint32_t gc = 0;
     bool ok = true;
     const uint32_t b_ring0 = smem_u32(S.b_ring);
-    const uint32_t a_base = tmem_base + (uint32_t)mw * A_COLS;
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
       Item it;
       if (!decode_item(item, p, S.W, it)) continue;
@@ -203,12 +213,14 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       const uint32_t idesc = idesc_f16kind_f32(TILE_M, (uint32_t)((it.n_rows + 15) & ~15), 0u);
       for (int kg = g0; kg < g1; ++kg, ++gc) {
         if ((int)(gc & 1u) != mw) continue;
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.a_full[mw]), (gc >> 1) & 1u,
-                                                     abort_flag, p.err))))
+        const uint32_t ai = gc % n_a, bi = gc % G_NBUF;
+        if (!(ok = wait_all(smem_u32(&S.a_full[ai]), (gc / n_a) & 1u, abort_flag, p.err))) break;
+        if (!(ok = wait_all(smem_u32(&S.acc_empty[bi]), ((gc / G_NBUF) & 1u) ^ 1u, abort_flag, p.err)))
           break;
         tc_fence_after();
         const uint32_t bst = b_ring0 + (gc % (uint32_t)n_st) * B_STAGE;
-        const uint32_t d0 = tmem_base + acc0 + (gc % G_NBUF) * (uint32_t)(NMAT * GBN);
+        const uint32_t a_base = tmem_base + ai * A_COLS;
+        const uint32_t d0 = tmem_base + acc0 + bi * (uint32_t)(NMAT * GBN);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const uint64_t bd = sdesc_kmajor_sw128(bst + (uint32_t)(q >> 2) * B_HALF + (uint32_t)(q & 3) * 32u);
@@ -218,86 +230,43 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           else
             mma_ta_elect(d0, a_base + q * 8, bd, idesc, q > 0 ? 1u : 0u);
         }
-        mma_commit_elect(smem_u32(&S.acc_full[gc % G_NBUF]));
+        mma_commit_elect(smem_u32(&S.a_empty[ai]));
+        mma_commit_elect(smem_u32(&S.acc_full[bi]));
       }
     }
-  } else {
-    // ================================================================ dequant + fold + epilogue
-    // Group gc (counted over the CTA's whole run): wait for its stage; wait
-    // for the accumulator of group gc-2 (its MMAs are done, so A stage gc%2
-    // and gc-2's pipeline stage are free) and start loading it; write gc's
-    // codes into the A stage and hand it to the MMA warp; then fold gc-2 when
-    // it belongs to this item (an item's last two groups are folded after its
-    // loop).
-    const int wr = warp - G_DQ0;
+  } else if (warp < G_FOLD0) {
+    // ================================================================ unpack
+    // Group gc: wait for its stage and for A slot gc % n_a to be free (the
+    // MMAs of group gc - n_a are done), both tested one group ahead; write
+    // the codes; hand the slot to the MMA warp; release my reads of the stage.
+    const int wr = warp - G_UP0;
     const int quad = warp & 3;               // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;          // weight row of the tile = TMEM lane
-    const int m_own = PAIR ? (wr >> 2) : 0;
-    const int j_own = PAIR ? 0 : (wr >> 2);
+    const int hw = wr >> 2;                  // which of the quadrant's two unpack warps
+    const int m_own = PAIR ? hw : 0;         // matrix ...
+    const int j_own = PAIR ? 0 : hw;         // ... and K quad of each half (single down)
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
-    constexpr int CH = (CW % 16 == 0) ? 16 : 8;   // columns per tcgen05.ld
     Ring rs{0, 0, n_st};
-    uint32_t it_count = 0, gc = 0;
-    bool ok = true, full_ready = false;
+    uint32_t gc = 0;
+    bool ok = true, full_ready = false, a_ready = false;
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
       Item it;
       if (!decode_item(item, p, S.W, it)) continue;
       int g0, g1;
       kgroups(p, it.ks, g0, g1);
-      const int cbeg = PAIR ? 0 : j_own * (GBN / 2);
-      const int nc = max(0, min(CW, it.n_rows - cbeg));
-      float acc[CW];
-#pragma unroll
-      for (int i = 0; i < CW; ++i) acc[i] = 0.f;
-      float fs0 = 0.f, fs1 = 0.f;   // scales of the groups awaiting their fold (slot = group & 1)
-      int fst0 = 0, fst1 = 0;       // and their pipeline stages
-
-      auto acc_wait = [&](uint32_t g) -> bool {
-        return __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.acc_full[g % G_NBUF]), (g / G_NBUF) & 1u,
-                                                 abort_flag, p.err));
-      };
-      auto acc_load = [&](uint32_t g, uint32_t (&d)[CW]) {
-        const uint32_t ta = lane_base + acc0 + (g % G_NBUF) * (uint32_t)(NMAT * GBN) +
-                            (uint32_t)(m_own * GBN + cbeg);
-#pragma unroll
-        for (int ch = 0; ch < CW / CH; ++ch) {
-          if (ch * CH < nc) {
-            if (CH == 16) tmem_ld_16(ta + ch * 16, *reinterpret_cast<uint32_t(*)[16]>(&d[ch * 16]));
-            else tmem_ld_8(ta + ch * 8, *reinterpret_cast<uint32_t(*)[8]>(&d[ch * 8]));
-          }
-        }
-      };
-      auto fold = [&](float s, const uint32_t (&d)[CW]) {
-#pragma unroll
-        for (int ch = 0; ch < CW / CH; ++ch)
-          if (ch * CH < nc) {
-#pragma unroll
-            for (int i = ch * CH; i < ch * CH + CH; ++i) acc[i] = fmaf(s, __uint_as_float(d[i]), acc[i]);
-          }
-      };
-
       for (int kg = g0; kg < g1 && ok; ++kg, ++gc) {
-        if (!full_ready &&
-            !(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err))))
+        const uint32_t ai = gc % n_a;
+        if (!full_ready && !(ok = wait_all(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err))) break;
+        if (!a_ready && !(ok = wait_all(smem_u32(&S.a_empty[ai]), ((gc / n_a) & 1u) ^ 1u, abort_flag, p.err)))
           break;
+        tc_fence_after();
         const uint8_t* mat = S.raw_ring + (size_t)rs.i * RAW_STAGE + m_own * I4_MAT_BYTES;
         const uint32_t sz = *reinterpret_cast<const uint32_t*>(mat + I4_PACKED_BYTES + r * 4);
-        const bool fold_prev = kg - 2 >= g0;
-        const int j = (int)(gc & 1u);   // fold slot of group gc (and of gc - 2)
-        uint32_t d[CW];
-        if (gc >= 2) {
-          if (!(ok = acc_wait(gc - 2))) break;
-          tc_fence_after();
-          if (fold_prev) {
-            acc_load(gc - 2, d);
-            mbar_arrive(smem_u32(&S.empty[j ? fst1 : fst0]));
-          }
-        }
         const float zf = __half2float(__ushort_as_half((unsigned short)(sz >> 16)));
         const __half2 za = __float2half2_rn(-(1024.f + zf)), zb = __float2half2_rn(-(64.f + zf));
         const uint32_t nz_a = *reinterpret_cast<const uint32_t*>(&za);
         const uint32_t nz_b = *reinterpret_cast<const uint32_t*>(&zb);
-        const uint32_t ta = lane_base + (uint32_t)j * A_COLS + (uint32_t)(m_own * (QGROUP / 2));
+        const uint32_t ta = lane_base + ai * A_COLS + (uint32_t)(m_own * (QGROUP / 2));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {   // K halves of the group: 64 codes of my row each
           if (PAIR) {
@@ -321,67 +290,97 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             tmem_st_16(ta + (uint32_t)(h * 32 + j_own * 16), v);
           }
         }
-        // test the next group's stage while the stores drain
-        const int nxt_i = rs.i + 1 == n_st ? 0 : rs.i + 1;
-        const uint32_t nxt_ph = rs.i + 1 == n_st ? rs.ph ^ 1u : rs.ph;
-        full_ready = __all_sync(0xffffffffu, mbar_test_wait(smem_u32(&S.full[nxt_i]), nxt_ph));
+        mbar_arrive(smem_u32(&S.empty[rs.i]));   // my reads of the stage are done
+        {   // while the stores drain, test what the next group waits for
+          const int nxt_i = rs.i + 1 == n_st ? 0 : rs.i + 1;
+          const uint32_t nxt_ph = rs.i + 1 == n_st ? rs.ph ^ 1u : rs.ph;
+          const uint32_t gn = gc + 1u;
+          const uint32_t t = __reduce_and_sync(
+              0xffffffffu, mbar_test_wait2(smem_u32(&S.full[nxt_i]), nxt_ph,
+                                           smem_u32(&S.a_empty[gn % n_a]), ((gn / n_a) & 1u) ^ 1u));
+          full_ready = (t & 1u) != 0;
+          a_ready = (t & 2u) != 0;
+        }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(smem_u32(&S.a_full[j]));
-        if (fold_prev) {
-          tmem_ld_wait_regs(d);
-          fold(j ? fs1 : fs0, d);
-        }
-        const float s = __half2float(__ushort_as_half((unsigned short)(sz & 0xFFFFu)));
-        if (j) { fs1 = s; fst1 = rs.i; } else { fs0 = s; fst0 = rs.i; }
+        mbar_arrive(smem_u32(&S.a_full[ai]));
         rs.next();
       }
-      // fold the item's last (up to) two groups
-      for (uint32_t g = gc - (uint32_t)min(2, g1 - g0); ok && g < gc; ++g) {
-        if (!(ok = acc_wait(g))) break;
+    }
+  } else {
+    // ================================================================ fold + epilogue
+    // One warp per TMEM lane quadrant; each thread owns weight row r of every
+    // matrix and all the item's token columns.  Group gc: wait for its
+    // accumulator slice, fold it with the group's scales (read from the
+    // stage, which this warp releases afterwards), free the slice.
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+    constexpr int CH = 16;   // columns per tcgen05.ld
+    Ring rs{0, 0, n_st};
+    uint32_t gc = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      Item it;
+      if (!decode_item(item, p, S.W, it)) continue;
+      int g0, g1;
+      kgroups(p, it.ks, g0, g1);
+      const int nc = it.n_rows;   // token columns of this item (<= GBN)
+      float acc[NMAT][GBN];
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+        for (int i = 0; i < GBN; ++i) acc[m][i] = 0.f;
+      for (int kg = g0; kg < g1 && ok; ++kg, ++gc) {
+        const uint32_t bi = gc % G_NBUF;
+        if (!(ok = wait_all(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err))) break;
+        const uint8_t* raw = S.raw_ring + (size_t)rs.i * RAW_STAGE;
+        float sc[NMAT];
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m)
+          sc[m] = __half2float(__ushort_as_half(
+              *reinterpret_cast<const unsigned short*>(raw + m * I4_MAT_BYTES + I4_PACKED_BYTES + r * 4)));
+        if (!(ok = wait_all(smem_u32(&S.acc_full[bi]), (gc / G_NBUF) & 1u, abort_flag, p.err))) break;
         tc_fence_after();
-        uint32_t d[CW];
-        acc_load(g, d);
-        mbar_arrive(smem_u32(&S.empty[(g & 1u) ? fst1 : fst0]));
-        tmem_ld_wait_regs(d);
-        fold((g & 1u) ? fs1 : fs0, d);
+        const uint32_t ta = lane_base + acc0 + bi * (uint32_t)(NMAT * GBN);
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+#pragma unroll
+          for (int ch = 0; ch < GBN / CH; ++ch) {
+            if (ch * CH < nc) {
+              uint32_t d[CH];
+              tmem_ld_16(ta + (uint32_t)(m * GBN + ch * CH), d);
+              tmem_ld_wait_regs(d);
+#pragma unroll
+              for (int i = 0; i < CH; ++i)
+                acc[m][ch * CH + i] = fmaf(sc[m], __uint_as_float(d[i]), acc[m][ch * CH + i]);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&S.acc_empty[bi]));
+        mbar_arrive(smem_u32(&S.empty[rs.i]));
+        rs.next();
       }
       if (!ok) break;
-      tc_fence_before();
 
       // ---- item epilogue from the register accumulators
       if (GATEUP) {
-        // hand-offs among the dequant warps use bounded mbarrier waits (not
-        // bar.sync), so a warp that aborted cannot leave the others blocked
-        const uint32_t xpar = it_count & 1u;
-        if (m_own == 1) {
+        __half* hout = reinterpret_cast<__half*>(p.out);
+        const int f = it.mt * TILE_M + r;
 #pragma unroll
-          for (int i = 0; i < CW; ++i)
-            if (i < nc) S.xch[i * TILE_M + r] = acc[i];
-        }
-        mbar_arrive(smem_u32(&S.xch_bar[0]));
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.xch_bar[0]), xpar, abort_flag, p.err))))
-          break;
-        if (m_own == 0) {
-          __half* hout = reinterpret_cast<__half*>(p.out);
-          const int f = it.mt * TILE_M + r;
-#pragma unroll
-          for (int i = 0; i < CW; ++i)
-            if (i < nc)
-              hout[(size_t)(it.r0 + i) * p.out_ld + f] = to_half_sat(silu_f(acc[i]) * S.xch[i * TILE_M + r]);
-        }
-        // the gate warps are done with xch before any warp writes it again
-        mbar_arrive(smem_u32(&S.xch_bar[1]));
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.xch_bar[1]), xpar, abort_flag, p.err))))
-          break;
+        for (int i = 0; i < GBN; ++i)
+          if (i < nc) hout[(size_t)(it.r0 + i) * p.out_ld + f] = to_half_sat(silu_f(acc[0][i]) * acc[1][i]);
       } else {
         float* y = reinterpret_cast<float*>(p.out) + (size_t)it.ks * p.out_split_stride;
-        const int f = (MODE == G_DOWN_PAIR ? 2 * it.mt + m_own : it.mt) * TILE_M + r;
 #pragma unroll
-        for (int i = 0; i < CW; ++i)
-          if (i < nc) y[(size_t)(it.r0 + cbeg + i) * p.out_ld + f] = acc[i];
+        for (int m = 0; m < NMAT; ++m) {
+          const int f = (MODE == G_DOWN_PAIR ? 2 * it.mt + m : it.mt) * TILE_M + r;
+#pragma unroll
+          for (int i = 0; i < GBN; ++i)
+            if (i < nc) y[(size_t)(it.r0 + i) * p.out_ld + f] = acc[m][i];
+        }
       }
-      ++it_count;
     }
   }
 
@@ -397,7 +396,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       mbar_wait(smem_u32(&S.full[sl]), (uint32_t)((q / n_st) & 1), no_abort, p.err);
     }
   }
-  if (warp >= 1 && warp < G_DQ0) {   // every MMA this CTA issued has finished
+  if (warp >= 1 && warp < G_UP0) {   // every MMA this CTA issued has finished
     mma_commit_elect(smem_u32(S.fin));
     mbar_wait(smem_u32(S.fin), 0, no_abort, p.err);
   }
@@ -413,15 +412,18 @@ GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups, int n_mt) {
   pl.group = true;
   pl.pair = !gateup && n_mt % 2 == 0;
   const int nmat = (gateup || pl.pair) ? 2 : 1;
-  pl.ndq = G_NDQ;
-  pl.n_a = G_NA;
+  pl.ndq = G_NUP + G_NFOLD;
   const size_t budget = 227 * 1024 - 1024;
   int n_st = 3;
-  while (n_st < 16 && group_carve_bytes(nmat, gateup, bn, n_st + 1, n_groups) <= budget) ++n_st;
+  while (n_st < 16 && group_carve_bytes(nmat, bn, n_st + 1, n_groups) <= budget) ++n_st;
   pl.n_raw = n_st;   // stages (nibbles + token rows)
   pl.n_b = n_st;
-  pl.smem_bytes = group_carve_bytes(nmat, gateup, bn, n_st, n_groups) + 1024;
-  const uint32_t need = (uint32_t)(G_NA * nmat * (QGROUP / 2) + G_NBUF * nmat * bn);
+  pl.smem_bytes = group_carve_bytes(nmat, bn, n_st, n_groups) + 1024;
+  // A slots: as many as fit (up to 3) beside the 4 accumulator slices in 512 columns
+  const uint32_t acc_cols = (uint32_t)(G_NBUF * nmat * bn);
+  pl.n_a = G_MAX_NA;
+  while (pl.n_a > 2 && (uint32_t)(pl.n_a * nmat * (QGROUP / 2)) + acc_cols > 512u) --pl.n_a;
+  const uint32_t need = (uint32_t)(pl.n_a * nmat * (QGROUP / 2)) + acc_cols;
   uint32_t cols = 32;
   while (cols < need) cols <<= 1;
   pl.tmem_cols = cols;

@@ -64,6 +64,21 @@ MOE_DEV bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Two non-blocking tests in one go (their latencies overlap): bit 0 = phase
+// par0 of bar0 completed, bit 1 = phase par1 of bar1 completed.
+MOE_DEV uint32_t mbar_test_wait2(uint32_t bar0, uint32_t par0, uint32_t bar1, uint32_t par1) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@q or.b32 %0, %0, 2;\n\t}"
+      : "=r"(r)
+      : "r"(bar0), "r"(par0), "r"(bar1), "r"(par1)
+      : "memory");
+  return r;
+}
 // Same, letting the hardware suspend the thread (up to ~the hint, in ns) until
 // the phase completes instead of returning at once: waiting warps stop taking
 // issue slots from the working ones.
@@ -262,6 +277,12 @@ MOE_DEV void tmem_ld_8(uint32_t taddr, uint32_t (&r)[8]) {
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7])
       : "r"(taddr));
+}
+// 32 lanes x 4 consecutive 32-bit columns.
+MOE_DEV void tmem_ld_4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
 }
 MOE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // wait::ld, then tie the loaded registers to it so that no use of them can be
