@@ -94,8 +94,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   constexpr uint32_t A_COLS = NMAT * (QGROUP / 2);     // TMEM columns of one A slot
   constexpr uint32_t B_HALF = (uint32_t)GBN * 128u;    // one 64-wide K slice of the token rows
   constexpr uint32_t B_STAGE = 2u * B_HALF;
+  // A slots: 3 where they fit beside the 4 accumulator slices in 512 columns
+  constexpr int NA = (3 * A_COLS + G_NBUF * NMAT * GBN <= 512) ? 3 : 2;
   const int n_st = p.n_raw;
-  const uint32_t n_a = (uint32_t)p.n_a;
 
   extern __shared__ uint8_t smem_dyn[];
   const uint32_t pad = (1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u;
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = (uint32_t)S.misc[0];
   const int total = S.misc[2];
-  const uint32_t acc0 = n_a * A_COLS;   // accumulator slices follow the A slots
+  const uint32_t acc0 = NA * A_COLS;   // accumulator slices follow the A slots
 
   if (warp == 0) {
     // ================================================================ producer
@@ -198,46 +199,49 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   } else if (warp < G_UP0) {
     // ================================================================ MMA issuers
     // Warp 1 + mw issues the groups with (group counter % 2) == mw.  Group gc
-    // uses A slot gc % n_a and accumulator slice gc % 4.  a_full(gc) also
+    // uses A slot gc % NA and accumulator slice gc % 4.  a_full(gc) also
     // implies that the group's stage (token tile) has landed: the unpack
-    // threads arrive only after seeing it.  The whole warp runs the loop.
+    // threads arrive only after seeing it.  The whole warp runs the loop;
+    // ring positions advance by one per group, owned or not.
     const int mw = warp - 1;
     uint32_t gc = 0;
     bool ok = true;
-    const uint32_t b_ring0 = smem_u32(S.b_ring);
+    Ring rs{0, 0, n_st}, ra{0, 0, NA};
+    const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(S.b_ring));   // stage 0, K step 0
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
       Item it;
       if (!decode_item(item, p, S.W, it)) continue;
       int g0, g1;
       kgroups(p, it.ks, g0, g1);
       const uint32_t idesc = idesc_f16kind_f32(TILE_M, (uint32_t)((it.n_rows + 15) & ~15), 0u);
-      for (int kg = g0; kg < g1; ++kg, ++gc) {
+      for (int kg = g0; kg < g1; ++kg, ++gc, rs.next(), ra.next()) {
         if ((int)(gc & 1u) != mw) continue;
-        const uint32_t ai = gc % n_a, bi = gc % G_NBUF;
-        if (!(ok = wait_all(smem_u32(&S.a_full[ai]), (gc / n_a) & 1u, abort_flag, p.err))) break;
+        const uint32_t bi = gc % G_NBUF;
+        if (!(ok = wait_all(smem_u32(&S.a_full[ra.i]), ra.ph, abort_flag, p.err))) break;
         if (!(ok = wait_all(smem_u32(&S.acc_empty[bi]), ((gc / G_NBUF) & 1u) ^ 1u, abort_flag, p.err)))
           break;
         tc_fence_after();
-        const uint32_t bst = b_ring0 + (gc % (uint32_t)n_st) * B_STAGE;
-        const uint32_t a_base = tmem_base + ai * A_COLS;
+        // the descriptor's start-address field counts 16-byte units
+        const uint64_t bd = bdesc0 + (uint64_t)(((uint32_t)rs.i * B_STAGE) >> 4);
+        const uint32_t a_base = tmem_base + (uint32_t)ra.i * A_COLS;
         const uint32_t d0 = tmem_base + acc0 + bi * (uint32_t)(NMAT * GBN);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const uint64_t bd = sdesc_kmajor_sw128(bst + (uint32_t)(q >> 2) * B_HALF + (uint32_t)(q & 3) * 32u);
+          const uint64_t bq = bd + (uint64_t)(((q >> 2) * B_HALF + (q & 3) * 32) >> 4);
           if (NMAT == 2)
-            mma2_ta_elect(d0, d0 + GBN, a_base + q * 8, a_base + (QGROUP / 2) + q * 8, bd, idesc,
+            mma2_ta_elect(d0, d0 + GBN, a_base + q * 8, a_base + (QGROUP / 2) + q * 8, bq, idesc,
                           q > 0 ? 1u : 0u);
           else
-            mma_ta_elect(d0, a_base + q * 8, bd, idesc, q > 0 ? 1u : 0u);
+            mma_ta_elect(d0, a_base + q * 8, bq, idesc, q > 0 ? 1u : 0u);
         }
-        mma_commit_elect(smem_u32(&S.a_empty[ai]));
+        mma_commit_elect(smem_u32(&S.a_empty[ra.i]));
         mma_commit_elect(smem_u32(&S.acc_full[bi]));
       }
     }
   } else if (warp < G_FOLD0) {
     // ================================================================ unpack
-    // Group gc: wait for its stage and for A slot gc % n_a to be free (the
-    // MMAs of group gc - n_a are done), both tested one group ahead; write
+    // Group gc: wait for its stage and for A slot gc % NA to be free (the
+    // MMAs of group gc - NA are done), both tested one group ahead; write
     // the codes; hand the slot to the MMA warp; release my reads of the stage.
     const int wr = warp - G_UP0;
     const int quad = warp & 3;               // TMEM lane quadrant of this warp
@@ -246,19 +250,16 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const int m_own = PAIR ? hw : 0;         // matrix ...
     const int j_own = PAIR ? 0 : hw;         // ... and K quad of each half (single down)
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
-    Ring rs{0, 0, n_st};
-    uint32_t gc = 0;
+    Ring rs{0, 0, n_st}, ra{0, 0, NA};
     bool ok = true, full_ready = false, a_ready = false;
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
       Item it;
       if (!decode_item(item, p, S.W, it)) continue;
       int g0, g1;
       kgroups(p, it.ks, g0, g1);
-      for (int kg = g0; kg < g1 && ok; ++kg, ++gc) {
-        const uint32_t ai = gc % n_a;
+      for (int kg = g0; kg < g1 && ok; ++kg) {
         if (!full_ready && !(ok = wait_all(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err))) break;
-        if (!a_ready && !(ok = wait_all(smem_u32(&S.a_empty[ai]), ((gc / n_a) & 1u) ^ 1u, abort_flag, p.err)))
-          break;
+        if (!a_ready && !(ok = wait_all(smem_u32(&S.a_empty[ra.i]), ra.ph ^ 1u, abort_flag, p.err))) break;
         tc_fence_after();
         const uint8_t* mat = S.raw_ring + (size_t)rs.i * RAW_STAGE + m_own * I4_MAT_BYTES;
         const uint32_t sz = *reinterpret_cast<const uint32_t*>(mat + I4_PACKED_BYTES + r * 4);
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         const __half2 za = __float2half2_rn(-(1024.f + zf)), zb = __float2half2_rn(-(64.f + zf));
         const uint32_t nz_a = *reinterpret_cast<const uint32_t*>(&za);
         const uint32_t nz_b = *reinterpret_cast<const uint32_t*>(&zb);
-        const uint32_t ta = lane_base + ai * A_COLS + (uint32_t)(m_own * (QGROUP / 2));
+        const uint32_t ta = lane_base + (uint32_t)ra.i * A_COLS + (uint32_t)(m_own * (QGROUP / 2));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {   // K halves of the group: 64 codes of my row each
           if (PAIR) {
@@ -292,19 +293,20 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         }
         mbar_arrive(smem_u32(&S.empty[rs.i]));   // my reads of the stage are done
         {   // while the stores drain, test what the next group waits for
-          const int nxt_i = rs.i + 1 == n_st ? 0 : rs.i + 1;
-          const uint32_t nxt_ph = rs.i + 1 == n_st ? rs.ph ^ 1u : rs.ph;
-          const uint32_t gn = gc + 1u;
+          Ring ns = rs, na = ra;
+          ns.next();
+          na.next();
           const uint32_t t = __reduce_and_sync(
-              0xffffffffu, mbar_test_wait2(smem_u32(&S.full[nxt_i]), nxt_ph,
-                                           smem_u32(&S.a_empty[gn % n_a]), ((gn / n_a) & 1u) ^ 1u));
+              0xffffffffu, mbar_test_wait2(smem_u32(&S.full[ns.i]), ns.ph, smem_u32(&S.a_empty[na.i]),
+                                           na.ph ^ 1u));
           full_ready = (t & 1u) != 0;
           a_ready = (t & 2u) != 0;
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(smem_u32(&S.a_full[ai]));
+        mbar_arrive(smem_u32(&S.a_full[ra.i]));
         rs.next();
+        ra.next();
       }
     }
   } else {
@@ -419,10 +421,10 @@ GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups, int n_mt) {
   pl.n_raw = n_st;   // stages (nibbles + token rows)
   pl.n_b = n_st;
   pl.smem_bytes = group_carve_bytes(nmat, bn, n_st, n_groups) + 1024;
-  // A slots: as many as fit (up to 3) beside the 4 accumulator slices in 512 columns
+  // A slots: 3 where they fit beside the 4 accumulator slices in 512 columns
+  // (the kernel derives the same number from its template arguments)
   const uint32_t acc_cols = (uint32_t)(G_NBUF * nmat * bn);
-  pl.n_a = G_MAX_NA;
-  while (pl.n_a > 2 && (uint32_t)(pl.n_a * nmat * (QGROUP / 2)) + acc_cols > 512u) --pl.n_a;
+  pl.n_a = (uint32_t)(3 * nmat * (QGROUP / 2)) + acc_cols <= 512u ? 3 : 2;
   const uint32_t need = (uint32_t)(pl.n_a * nmat * (QGROUP / 2)) + acc_cols;
   uint32_t cols = 32;
   while (cols < need) cols <<= 1;
