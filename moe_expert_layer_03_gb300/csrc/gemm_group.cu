@@ -59,7 +59,18 @@ constexpr int G_THREADS = (G_FOLD0 + G_NFOLD) * 32;
 
 enum GroupMode { G_GATEUP = 0, G_DOWN_PAIR = 1, G_DOWN = 2 };
 
+// A work item decoded once per CTA (the decode needs integer divisions by
+// run-time values, which every warp would otherwise repeat).
+struct ItemDesc {
+  const uint8_t* slot;   // nullptr: the item is skipped (bad expert slot)
+  int g0, g1;            // quantisation groups [g0, g1) of its K split
+  int r0, n_rows;        // token rows
+  int mt, ks;            // output tile (pair) and K split
+};
+constexpr int G_ITEM_TAB = 64;   // items per CTA kept in the table; later ones are decoded on the fly
+
 struct GShared {
+  ItemDesc* items;     // [G_ITEM_TAB]
   uint8_t* b_ring;     // [n_st][2 * bn * 128]  token rows, SW128 K-major (1024-aligned stages)
   uint8_t* raw_ring;   // [n_st][nmat * I4_MAT_BYTES]  nibbles + scale/zero words
   uint64_t *full, *empty;          // stages: producer -> consumers, consumers -> producer
@@ -72,10 +83,29 @@ struct GShared {
 
 size_t group_carve_bytes(int nmat, int bn, int n_st, int n_groups) {
   size_t s = (size_t)n_st * ((size_t)bn * 256 + (size_t)nmat * I4_MAT_BYTES);
+  s += sizeof(ItemDesc) * G_ITEM_TAB;
   s = align_up(s, 16);
   s += 8 * (size_t)(2 * n_st + 2 * G_MAX_NA + 2 * G_NBUF + 1);
   s += 4 * (G_MISC + worklist_ints(n_groups));
   return s;
+}
+
+__device__ __forceinline__ ItemDesc make_item_desc(int item, const GemmArgs& p, const WorkList& W) {
+  ItemDesc d;
+  Item it;
+  d.slot = decode_item(item, p, W, it) ? it.slot : nullptr;
+  kgroups(p, it.ks, d.g0, d.g1);
+  d.r0 = it.r0;
+  d.n_rows = it.n_rows;
+  d.mt = it.mt;
+  d.ks = it.ks;
+  return d;
+}
+
+// The CTA's i-th item (item index blockIdx.x + i * gridDim.x).
+__device__ __forceinline__ ItemDesc get_item(int i, const GemmArgs& p, const GShared& S) {
+  if (i < G_ITEM_TAB) return S.items[i];
+  return make_item_desc(blockIdx.x + i * gridDim.x, p, S.W);
 }
 
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
@@ -105,6 +135,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   S.b_ring = base;
   S.raw_ring = S.b_ring + (size_t)n_st * B_STAGE;
   uint8_t* cur = S.raw_ring + (size_t)n_st * RAW_STAGE;
+  S.items = reinterpret_cast<ItemDesc*>(cur);
+  cur += sizeof(ItemDesc) * G_ITEM_TAB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + align_up((size_t)(cur - base), 16));
   S.full = bars;
   S.empty = S.full + n_st;
@@ -147,13 +179,17 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   }
   if (warp == G_UP0) {
     const int total = build_worklist(p, S.W, lane);
-    if (lane == 0) S.misc[2] = total;
+    __syncwarp();
+    const int n_mine = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    for (int i = lane; i < n_mine && i < G_ITEM_TAB; i += 32)
+      S.items[i] = make_item_desc(blockIdx.x + i * gridDim.x, p, S.W);
+    if (lane == 0) S.misc[2] = n_mine;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = (uint32_t)S.misc[0];
-  const int total = S.misc[2];
+  const int n_mine = S.misc[2];   // items of this CTA
   const uint32_t acc0 = NA * A_COLS;   // accumulator slices follow the A slots
 
   if (warp == 0) {
@@ -166,11 +202,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       int issued = 0;
       const uint64_t pol = policy_evict_first();
       bool ok = true;
-      for (int item = blockIdx.x; item < total && ok && !*abort_flag; item += gridDim.x) {
-        Item it;
-        if (!decode_item(item, p, S.W, it)) continue;
-        int g0, g1;
-        kgroups(p, it.ks, g0, g1);
+      for (int ii = 0; ii < n_mine && ok && !*abort_flag; ++ii) {
+        const ItemDesc it = get_item(ii, p, S);
+        if (!it.slot) continue;
+        const int g0 = it.g0, g1 = it.g1;
         const uint8_t* sec = it.slot + p.sec_off;
         for (int kg = g0; kg < g1; ++kg) {
           if (!(ok = mbar_wait(smem_u32(&S.empty[rs.i]), rs.ph ^ 1u, abort_flag, p.err))) break;
@@ -208,11 +243,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     bool ok = true;
     Ring rs{0, 0, n_st}, ra{0, 0, NA};
     const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(S.b_ring));   // stage 0, K step 0
-    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-      Item it;
-      if (!decode_item(item, p, S.W, it)) continue;
-      int g0, g1;
-      kgroups(p, it.ks, g0, g1);
+    for (int ii = 0; ii < n_mine && ok; ++ii) {
+      const ItemDesc it = get_item(ii, p, S);
+      if (!it.slot) continue;
+      const int g0 = it.g0, g1 = it.g1;
       const uint32_t idesc = idesc_f16kind_f32(TILE_M, (uint32_t)((it.n_rows + 15) & ~15), 0u);
       for (int kg = g0; kg < g1; ++kg, ++gc, rs.next(), ra.next()) {
         if ((int)(gc & 1u) != mw) continue;
@@ -252,11 +286,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
     Ring rs{0, 0, n_st}, ra{0, 0, NA};
     bool ok = true, full_ready = false, a_ready = false;
-    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-      Item it;
-      if (!decode_item(item, p, S.W, it)) continue;
-      int g0, g1;
-      kgroups(p, it.ks, g0, g1);
+    for (int ii = 0; ii < n_mine && ok; ++ii) {
+      const ItemDesc it = get_item(ii, p, S);
+      if (!it.slot) continue;
+      const int g0 = it.g0, g1 = it.g1;
       for (int kg = g0; kg < g1 && ok; ++kg) {
         if (!full_ready && !(ok = wait_all(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err))) break;
         if (!a_ready && !(ok = wait_all(smem_u32(&S.a_empty[ra.i]), ra.ph ^ 1u, abort_flag, p.err))) break;
@@ -322,11 +355,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     Ring rs{0, 0, n_st};
     uint32_t gc = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-      Item it;
-      if (!decode_item(item, p, S.W, it)) continue;
-      int g0, g1;
-      kgroups(p, it.ks, g0, g1);
+    for (int ii = 0; ii < n_mine && ok; ++ii) {
+      const ItemDesc it = get_item(ii, p, S);
+      if (!it.slot) continue;
+      const int g0 = it.g0, g1 = it.g1;
       const int nc = it.n_rows;   // token columns of this item (<= GBN)
       float acc[NMAT][GBN];
 #pragma unroll

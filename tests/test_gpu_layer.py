@@ -99,6 +99,19 @@ def test_layer_full_size_sampled(name):
     assert_close_rms(got[toks], L.oracle_forward(toks), what=name)
 
 
+def test_many_items_per_cta():
+    """256 experts with d_ff = 8192 give the decode gate/up GEMM about 90 work
+    items per persistent CTA, more than the per-CTA item table holds, so the
+    items past it are decoded on the fly; sampled tokens against the oracle."""
+    cfg = ms.LayerConfig("many_items", T=64, d=256, F=8192, E=256, k=8, fmt="int4", seed=12)
+    L = GpuLayer(cfg)
+    out, ws = L.forward()
+    assert moe.last_device_error(ws) == 0
+    got = out.float().cpu().numpy()
+    toks = [0, 31, 63]
+    assert_close_rms(got[toks], L.oracle_forward(toks), what=cfg.name)
+
+
 @pytest.mark.parametrize("fmt", ["bf16", "int4"])
 def test_one_expert_takes_every_token(fmt):
     """50 tokens on expert 0 of 16 (B tile of 16 rows -> 4 row chunks), 15 experts idle."""
