@@ -234,16 +234,25 @@ def load_peaks() -> tuple[float, float, str]:
     return 6800.0, 1900.0, "fallback"
 
 
+GEMM_SOURCES = ("gemm.cu", "gemm_group.cu", "gemm_common.cuh", "ptx.cuh", "kernels.cuh")
+
+
+def gemm_sources_sha256() -> str:
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        h.update(open(os.path.join(ROOT, "moe_expert_layer_03_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
 def kernel_traffic(key: str):
     """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
-    valid only while the kernel source is unchanged (else None)."""
+    valid only while the GEMM sources are unchanged (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     j = json.load(open(p))
-    src = open(os.path.join(ROOT, "moe_expert_layer_03_gb300", "csrc", "gemm.cu"), "rb").read()
     ent = j.get(key)
-    if not ent or ent.get("gemm_cu_sha256") != hashlib.sha256(src).hexdigest():
+    if not ent or ent.get("gemm_sources_sha256") != gemm_sources_sha256():
         return None
     return ent.get("dram_bytes_per_launch")
 
