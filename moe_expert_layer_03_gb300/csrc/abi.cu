@@ -168,10 +168,11 @@ GemmArgs base_args(const moe_pool* routed, const moe_pool* shared, int* err) {
 }
 
 // gate/up (SwiGLU) then down over the row groups described by `offsets`.
-// x_rows and h are fp16 for int4 pools, bf16 otherwise.
+// x_rows and h are fp16 for int4 pools, bf16 otherwise.  pdl: both launches
+// follow a kernel of the same call (dependent launch).
 moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups, int rows,
                    const moe_pool* routed, const moe_pool* shared, int bn, int ksplit, uint16_t* h,
-                   float* part, int* err, cudaStream_t s,
+                   float* part, int* err, cudaStream_t s, bool pdl,
                    cudaEvent_t ev_mid, cudaEvent_t ev_down) {
   const int d = routed->d_model, F = routed->d_ff, fmt = routed->fmt;
   const bool f16 = gemm_uses_fp16(fmt);
@@ -193,7 +194,8 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
   g.out = h;
   g.out_ld = F;
   g.out_split_stride = 0;
-  if (launch_grouped_gemm(fmt, true, mx, g, plan_gemm(fmt, true, bn, n_groups, F / TILE_M), grid, s) != cudaSuccess)
+  if (launch_grouped_gemm(fmt, true, mx, g, plan_gemm(fmt, true, bn, n_groups, F / TILE_M), grid, s,
+                          pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev_mid && cudaEventRecord(ev_mid, s) != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -205,8 +207,8 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
   dn.out = part;
   dn.out_ld = d;
   dn.out_split_stride = (unsigned long long)rows * d;
-  if (launch_grouped_gemm(fmt, false, mh, dn, plan_gemm(fmt, false, bn, n_groups, d / TILE_M), grid, s) !=
-      cudaSuccess)
+  if (launch_grouped_gemm(fmt, false, mh, dn, plan_gemm(fmt, false, bn, n_groups, d / TILE_M), grid, s,
+                          pdl && !ev_mid) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ev_down && cudaEventRecord(ev_down, s) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
@@ -254,22 +256,25 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
   auto rec = [&](int i) -> bool {
     return !ev || !ev[i] || cudaEventRecord((cudaEvent_t)ev[i], s) == cudaSuccess;
   };
+  // the kernels after the first start early (dependent launch), except when
+  // stage events sit between them
+  const bool pdl = ev == nullptr;
 
   if (!rec(MOE_STAGE_ROUTE)) return MOE_ERR_CUDA;
   if (launch_route_topk(logits, T, E, k, idx, w, nullptr, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (!rec(MOE_STAGE_PERMUTE)) return MOE_ERR_CUDA;
-  if (launch_permute_index(idx, T, k, E, L.Tsh, counts, offsets, roa, tor, err, s) != cudaSuccess)
+  if (launch_permute_index(idx, T, k, E, L.Tsh, counts, offsets, roa, tor, err, s, pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!rec(MOE_STAGE_GATHER)) return MOE_ERR_CUDA;
-  if (launch_gather_rows(x, tor, L.rows, T, L.d, xperm, f16, sm_count(), s) != cudaSuccess)
+  if (launch_gather_rows(x, tor, L.rows, T, L.d, xperm, f16, sm_count(), s, pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!rec(MOE_STAGE_GATE_UP)) return MOE_ERR_CUDA;
   st = run_ffn(xperm, offsets, E + (shared ? 1 : 0), L.rows, routed, shared, L.bn, L.ksplit, h, part,
-               err, s, ev ? (cudaEvent_t)ev[MOE_STAGE_DOWN] : nullptr,
+               err, s, pdl, ev ? (cudaEvent_t)ev[MOE_STAGE_DOWN] : nullptr,
                ev ? (cudaEvent_t)ev[MOE_STAGE_COMBINE] : nullptr);
   if (st != MOE_OK) return st;
   if (launch_combine_partials(part, L.ksplit, (size_t)L.rows * L.d, roa, w, T, k, L.d,
-                              shared ? L.A : -1, out, s) != cudaSuccess)
+                              shared ? L.A : -1, out, s, pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!rec(MOE_N_STAGES)) return MOE_ERR_CUDA;
   return MOE_OK;
@@ -341,7 +346,7 @@ moe_status moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int k,
   if (launch_permute_index(topk_idx, T, k, E, 0, counts, offsets, row_of_assign, token_of_row, err,
                            s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (launch_gather_rows(x, token_of_row, T * k, T, d, x_perm, false, sm_count(), s) !=
+  if (launch_gather_rows(x, token_of_row, T * k, T, d, x_perm, false, sm_count(), s, true) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
@@ -393,16 +398,16 @@ moe_status moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int A
   if (launch_clear_word(err, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (f16) {   // the int4 GEMMs read fp16 rows
     uint16_t* x16 = (uint16_t*)(W + L.x16);
-    if (launch_gather_rows(x_perm, nullptr, A, A, pool->d_model, x16, true, sm_count(), s) !=
+    if (launch_gather_rows(x_perm, nullptr, A, A, pool->d_model, x16, true, sm_count(), s, true) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     rows_in = x16;
   }
   st = run_ffn(rows_in, offsets, pool->n_experts, A, pool, nullptr, L.bn, L.ksplit, h, part, err, s,
-               nullptr, nullptr);
+               true, nullptr, nullptr);
   if (st != MOE_OK) return st;
   return launch_reduce_splits(part, L.ksplit, (size_t)A * pool->d_model, A, pool->d_model, y_perm,
-                              s) == cudaSuccess
+                              s, true) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }

@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(256)
                             const int32_t* __restrict__ row_of_assign,
                             const float* __restrict__ topk_w, int k, int d, int shared_row0,
                             uint16_t* __restrict__ out) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int t = blockIdx.x;
   const int c = (blockIdx.y * 256 + threadIdx.x) * 4;
   if (c >= d) return;
@@ -106,6 +108,8 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restrict__ part,
                                                             int n_split, size_t split_stride,
                                                             int d, uint16_t* __restrict__ y) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int r = blockIdx.x;
   const int c = (blockIdx.y * 256 + threadIdx.x) * 4;
   if (c >= d) return;
@@ -116,12 +120,11 @@ static dim3 grid_rows(int rows, int d) { return dim3((unsigned)rows, (unsigned)(
 
 cudaError_t launch_combine_partials(const float* part, int n_split, size_t split_stride,
                                     const int32_t* row_of_assign, const float* topk_w, int T,
-                                    int k, int d, int shared_row0, uint16_t* out, cudaStream_t s) {
+                                    int k, int d, int shared_row0, uint16_t* out, cudaStream_t s,
+                                    bool pdl) {
   if (T <= 0) return cudaSuccess;
-  combine_partials_kernel<<<grid_rows(T, d), 256, 0, s>>>(part, n_split, split_stride,
-                                                          row_of_assign, topk_w, k, d,
-                                                          shared_row0, out);
-  return cudaGetLastError();
+  return launch_kernel(combine_partials_kernel, grid_rows(T, d), dim3(256), 0, s, pdl, part, n_split,
+                       split_stride, row_of_assign, topk_w, k, d, shared_row0, out);
 }
 
 cudaError_t launch_combine_bf16(const uint16_t* y_perm, const int32_t* row_of_assign,
@@ -134,10 +137,10 @@ cudaError_t launch_combine_bf16(const uint16_t* y_perm, const int32_t* row_of_as
 }
 
 cudaError_t launch_reduce_splits(const float* part, int n_split, size_t split_stride, int rows,
-                                 int d, uint16_t* y, cudaStream_t s) {
+                                 int d, uint16_t* y, cudaStream_t s, bool pdl) {
   if (rows <= 0) return cudaSuccess;
-  reduce_splits_kernel<<<grid_rows(rows, d), 256, 0, s>>>(part, n_split, split_stride, d, y);
-  return cudaGetLastError();
+  return launch_kernel(reduce_splits_kernel, grid_rows(rows, d), dim3(256), 0, s, pdl, part, n_split,
+                       split_stride, d, y);
 }
 
 }  // namespace moe

@@ -144,6 +144,10 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
     tmem_alloc(smem_u32(&S.misc[0]), p.tmem_cols);
     tmem_relinquish();
   }
+  // everything above overlaps the previous kernel's tail (dependent launch);
+  // below, the offsets, token rows and outputs of earlier kernels are read
+  griddep_wait();
+  griddep_launch_dependents();
   if (warp == 2) {
     const int total = build_worklist(p, S.W, lane);
     if (lane == 0) S.misc[2] = total;
@@ -391,7 +395,7 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
 // ------------------------------------------------------------------ host side
 GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups, int n_mt);
 cudaError_t launch_grouped_gemm_group(bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
-                                      const GemmPlan& plan, int grid, cudaStream_t stream);
+                                      const GemmPlan& plan, int grid, cudaStream_t stream, bool pdl);
 
 GemmPlan plan_gemm(int fmt, bool gateup, int bn, int n_groups, int n_mt) {
   const bool int4 = fmt == MOE_W_INT4_G128;
@@ -424,7 +428,7 @@ GemmPlan plan_gemm(int fmt, bool gateup, int bn, int n_groups, int n_mt) {
 
 template <int FMT, bool GATEUP, int NDQ>
 static cudaError_t launch_one(const CUtensorMap& tmap, const GemmArgs& a, const GemmPlan& pl,
-                              int grid, cudaStream_t s) {
+                              int grid, cudaStream_t s, bool pdl) {
   auto kern = grouped_gemm_kernel<FMT, GATEUP, NDQ>;
   static bool attr_set = false;   // per instantiation; the maximum is requested once
   if (!attr_set) {
@@ -432,23 +436,22 @@ static cudaError_t launch_one(const CUtensorMap& tmap, const GemmArgs& a, const 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<grid, (2 + NDQ) * 32, pl.smem_bytes, s>>>(tmap, a);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), dim3((2 + NDQ) * 32), pl.smem_bytes, s, pdl, tmap, a);
 }
 
 cudaError_t launch_grouped_gemm(int fmt, bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
-                                const GemmPlan& plan, int grid, cudaStream_t stream) {
-  if (plan.group) return launch_grouped_gemm_group(gateup, tmap_b, args, plan, grid, stream);
+                                const GemmPlan& plan, int grid, cudaStream_t stream, bool pdl) {
+  if (plan.group) return launch_grouped_gemm_group(gateup, tmap_b, args, plan, grid, stream, pdl);
   args.n_a = plan.n_a;
   args.n_b = plan.n_b;
   args.n_raw = plan.n_raw;
   args.tmem_cols = plan.tmem_cols;
   constexpr int I4 = MOE_W_INT4_G128, B16 = MOE_W_BF16;
   if (fmt == I4)
-    return gateup ? launch_one<I4, true, 8>(tmap_b, args, plan, grid, stream)
-                  : launch_one<I4, false, 8>(tmap_b, args, plan, grid, stream);
-  return gateup ? launch_one<B16, true, 4>(tmap_b, args, plan, grid, stream)
-                : launch_one<B16, false, 4>(tmap_b, args, plan, grid, stream);
+    return gateup ? launch_one<I4, true, 8>(tmap_b, args, plan, grid, stream, pdl)
+                  : launch_one<I4, false, 8>(tmap_b, args, plan, grid, stream, pdl);
+  return gateup ? launch_one<B16, true, 4>(tmap_b, args, plan, grid, stream, pdl)
+                : launch_one<B16, false, 4>(tmap_b, args, plan, grid, stream, pdl);
 }
 
 }  // namespace moe

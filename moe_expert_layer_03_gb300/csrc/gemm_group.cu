@@ -177,6 +177,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     tmem_alloc(smem_u32(&S.misc[0]), p.tmem_cols);
     tmem_relinquish();
   }
+  // everything above overlaps the previous kernel's tail (dependent launch);
+  // below, the offsets, token rows and outputs of earlier kernels are read
+  griddep_wait();
+  griddep_launch_dependents();
   if (warp == G_UP0) {
     const int total = build_worklist(p, S.W, lane);
     __syncwarp();
@@ -466,7 +470,7 @@ GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups, int n_mt) {
 
 template <int MODE, int GBN>
 static cudaError_t launch_group_one(const CUtensorMap& tmap, const GemmArgs& a, const GemmPlan& pl,
-                                    int grid, cudaStream_t s) {
+                                    int grid, cudaStream_t s, bool pdl) {
   auto kern = grouped_gemm_group_kernel<MODE, GBN>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -474,29 +478,28 @@ static cudaError_t launch_group_one(const CUtensorMap& tmap, const GemmArgs& a, 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<grid, G_THREADS, pl.smem_bytes, s>>>(tmap, a);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), dim3(G_THREADS), pl.smem_bytes, s, pdl, tmap, a);
 }
 
 template <int MODE>
 static cudaError_t launch_group_mode(const CUtensorMap& tmap, const GemmArgs& a, const GemmPlan& pl,
-                                     int grid, cudaStream_t s) {
-  return a.bn == 16 ? launch_group_one<MODE, 16>(tmap, a, pl, grid, s)
-                    : launch_group_one<MODE, 32>(tmap, a, pl, grid, s);
+                                     int grid, cudaStream_t s, bool pdl) {
+  return a.bn == 16 ? launch_group_one<MODE, 16>(tmap, a, pl, grid, s, pdl)
+                    : launch_group_one<MODE, 32>(tmap, a, pl, grid, s, pdl);
 }
 
 cudaError_t launch_grouped_gemm_group(bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
-                                      const GemmPlan& plan, int grid, cudaStream_t stream) {
+                                      const GemmPlan& plan, int grid, cudaStream_t stream, bool pdl) {
   args.n_a = plan.n_a;
   args.n_b = plan.n_b;
   args.n_raw = plan.n_raw;
   args.tmem_cols = plan.tmem_cols;
-  if (gateup) return launch_group_mode<G_GATEUP>(tmap_b, args, plan, grid, stream);
+  if (gateup) return launch_group_mode<G_GATEUP>(tmap_b, args, plan, grid, stream, pdl);
   if (plan.pair) {
     args.n_mt /= 2;   // work items name pairs of output tiles
-    return launch_group_mode<G_DOWN_PAIR>(tmap_b, args, plan, grid, stream);
+    return launch_group_mode<G_DOWN_PAIR>(tmap_b, args, plan, grid, stream, pdl);
   }
-  return launch_group_mode<G_DOWN>(tmap_b, args, plan, grid, stream);
+  return launch_group_mode<G_DOWN>(tmap_b, args, plan, grid, stream, pdl);
 }
 
 }  // namespace moe

@@ -92,27 +92,51 @@ inline int down_work_tiles(int fmt, int bn, int n_mt) {
 
 GemmPlan plan_gemm(int fmt, bool gateup, int bn, int n_groups, int n_mt);
 cudaError_t launch_grouped_gemm(int fmt, bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
-                                const GemmPlan& plan, int grid, cudaStream_t stream);
+                                const GemmPlan& plan, int grid, cudaStream_t stream, bool pdl = false);
+
+// One kernel launch; pdl: programmatic stream serialisation (see below).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // ------------------------------------------------------------------ other kernels
 // err_clear (nullable): error word zeroed by the first thread (first launch of a forward).
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                               int* err_clear, cudaStream_t s);
+// The launches below take pdl = true when the previous kernel in the stream
+// belongs to the same call (programmatic dependent launch: this kernel's
+// prologue overlaps that kernel's tail; it reads nothing before
+// griddep_wait()).  The first kernel of every entry point launches normally,
+// so it never overlaps the caller's earlier work.
 cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_shared,
                                  int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
-                                 int32_t* token_of_row, int* err, cudaStream_t s);
+                                 int32_t* token_of_row, int* err, cudaStream_t s, bool pdl = false);
 // x_perm[r] = x[token_of_row[r]].  to_fp16: write fp16 (saturating) instead of
 // bf16.  token_of_row == nullptr: x_perm[r] = x[r].
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
-                               int d, uint16_t* x_perm, bool to_fp16, int n_sm, cudaStream_t s);
+                               int d, uint16_t* x_perm, bool to_fp16, int n_sm, cudaStream_t s,
+                               bool pdl = false);
 cudaError_t launch_combine_partials(const float* part, int n_split, size_t split_stride,
                                     const int32_t* row_of_assign, const float* topk_w, int T,
-                                    int k, int d, int shared_row0, uint16_t* out, cudaStream_t s);
+                                    int k, int d, int shared_row0, uint16_t* out, cudaStream_t s,
+                                    bool pdl = false);
 cudaError_t launch_combine_bf16(const uint16_t* y_perm, const int32_t* row_of_assign,
                                 const float* topk_w, const uint16_t* shared_y, int T, int k, int d,
                                 uint16_t* out, cudaStream_t s);
 cudaError_t launch_reduce_splits(const float* part, int n_split, size_t split_stride, int rows,
-                                 int d, uint16_t* y, cudaStream_t s);
+                                 int d, uint16_t* y, cudaStream_t s, bool pdl = false);
 cudaError_t launch_clear_word(int* p, cudaStream_t s);
 cudaError_t launch_prepack(int fmt, int d, int F, const moe_expert_src& src, uint8_t* dst,
                            cudaStream_t s);

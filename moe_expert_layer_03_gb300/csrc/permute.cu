@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(PERM_THREADS, 1)
                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                          int32_t* __restrict__ row_of_assign, int32_t* __restrict__ token_of_row,
                          int* __restrict__ err) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ int s_cnt[PERM_MAX_E];
   __shared__ int s_base[PERM_MAX_E];
   __shared__ int s_wc[PERM_WARPS][PERM_MAX_E];
@@ -120,6 +122,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ token_of_row,
                                                           int rows, int T, int d,
                                                           uint16_t* __restrict__ x_perm) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int nvec = d / 8;   // 16-byte vectors per row
   for (int r = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); r < rows;
@@ -148,6 +152,8 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
 __global__ void __launch_bounds__(256)
     gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ token_of_row,
                            int rows, int T, int d, uint16_t* __restrict__ x_perm) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int nvec = d / 8;
   for (int r = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); r < rows;
@@ -172,22 +178,22 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_shared,
                                  int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
-                                 int32_t* token_of_row, int* err, cudaStream_t s) {
-  permute_index_kernel<<<1, PERM_THREADS, 0, s>>>(idx, T, k, E, t_shared, counts, offsets,
-                                                  row_of_assign, token_of_row, err);
-  return cudaGetLastError();
+                                 int32_t* token_of_row, int* err, cudaStream_t s, bool pdl) {
+  return launch_kernel(permute_index_kernel, dim3(1), dim3(PERM_THREADS), 0, s, pdl, idx, T, k, E,
+                       t_shared, counts, offsets, row_of_assign, token_of_row, err);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
-                               int d, uint16_t* x_perm, bool to_fp16, int n_sm, cudaStream_t s) {
+                               int d, uint16_t* x_perm, bool to_fp16, int n_sm, cudaStream_t s,
+                               bool pdl) {
   if (rows <= 0) return cudaSuccess;
   int blocks = (rows + 7) / 8;   // 8 warps (rows) per block
   if (blocks > 4 * n_sm) blocks = 4 * n_sm;
   if (to_fp16)
-    gather_rows_f16_kernel<<<blocks, 256, 0, s>>>(x, token_of_row, rows, T, d, x_perm);
-  else
-    gather_rows_kernel<<<blocks, 256, 0, s>>>(x, token_of_row, rows, T, d, x_perm);
-  return cudaGetLastError();
+    return launch_kernel(gather_rows_f16_kernel, dim3(blocks), dim3(256), 0, s, pdl, x, token_of_row,
+                         rows, T, d, x_perm);
+  return launch_kernel(gather_rows_kernel, dim3(blocks), dim3(256), 0, s, pdl, x, token_of_row, rows,
+                       T, d, x_perm);
 }
 
 __global__ void clear_word_kernel(int* p) { *p = 0; }

@@ -28,6 +28,17 @@ MOE_DEV uint64_t global_timer_ns() {
   return t;
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start before
+// the previous kernel in the stream has finished.  griddep_wait() blocks the
+// calling thread until every prerequisite grid has completed and its writes
+// are visible (a no-op for a normal launch); griddep_launch_dependents() lets
+// the next such kernel be scheduled once every CTA of this one has called it
+// or exited (the dependent still waits for this grid's completion before it
+// reads anything).
+MOE_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 MOE_DEV void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
