@@ -81,13 +81,6 @@ moe_status check_pool(const moe_pool* p, bool single) {
 }
 
 // Largest chunk of one expert's rows that one work item covers (the B tile height).
-int choose_bn(int A, int E) {
-  const int mean = (A + E - 1) / E;
-  int bn = 16;
-  while (bn < 2 * mean && bn < 256) bn <<= 1;
-  return bn;
-}
-
 // K split of the down GEMM.  Decode (group kernel): the split whose items
 // spread most evenly over the persistent CTAs (fewest quantisation groups on
 // the busiest CTA; its fp32 partials are small).  Otherwise: enough items to
@@ -99,7 +92,7 @@ int choose_ksplit(int A, int E, bool has_shared, int bn, int fmt, int d, int F) 
   const int nch = mean > bn ? (mean + bn - 1) / bn : 1;
   const int G = F / QGROUP;
   const int smax = MAX_KSPLIT < G ? MAX_KSPLIT : G;
-  const long items = (long)active * down_work_tiles(fmt, bn, d / TILE_M) * nch;
+  const long items = (long)active * down_work_tiles(fmt, d / TILE_M) * nch;
   if (gemm_is_group(fmt, bn)) {
     int best_s = 1;
     long best = -1;
@@ -128,7 +121,7 @@ LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* s
   L.E = routed->n_experts;
   L.d = routed->d_model;
   L.F = routed->d_ff;
-  L.bn = choose_bn(L.A, L.E);
+  L.bn = choose_bn(L.A, L.E, routed->fmt);
   L.ksplit = choose_ksplit(L.A, L.E, shared != nullptr, L.bn, routed->fmt, L.d, L.F);
   size_t o = 0;
   L.err = o;      o += 1024;
@@ -362,7 +355,7 @@ struct FfnLayout {
 FfnLayout ffn_layout(int A, const moe_pool* pool) {
   FfnLayout L{};
   const int d = pool->d_model, F = pool->d_ff;
-  L.bn = choose_bn(A, pool->n_experts);
+  L.bn = choose_bn(A, pool->n_experts, pool->fmt);
   L.ksplit = choose_ksplit(A, pool->n_experts, false, L.bn, pool->fmt, d, F);
   const bool f16 = gemm_uses_fp16(pool->fmt);
   size_t o = 1024;

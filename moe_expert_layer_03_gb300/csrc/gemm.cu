@@ -17,12 +17,19 @@
 //   warp 0      producer: 1-D bulk copies of the prepacked weight blocks
 //               (int4 nibbles + scales, or pre-swizzled bf16 tiles) and 2-D TMA
 //               loads of the 64-wide K slices of the token rows (128-byte swizzle)
-//   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 with fp32
-//               accumulators in TMEM (gate at column 0, up at column bn); bf16
-//               operands for bf16 weights, fp16 for int4 weights
-//   warps 2..   int4: write fp16((q - z) * s) ((q - z) exact, one rounding of the
-//               product) into the swizzled A tile; then, per item, the
-//               epilogue: tcgen05.ld, SwiGLU -> h, or fp32 K-split partials.
+//   warp 1      TMEM owner and MMA issuer (tcgen05.mma kind::f16 from a
+//               converged warp, fp32 accumulators in TMEM: gate/tile 0 at
+//               column 0, up/tile 1 at column bn); bf16 operands for bf16
+//               weights (A tiles in shared memory), fp16 for int4 weights
+//   warps 2..   int4: write fp16((q - z) * s) ((q - z) exact, one rounding of
+//               the product) for each 64-wide K slice into an A slot in TMEM
+//               (beside the accumulators), so the A operand costs no shared-
+//               memory bandwidth; then, per item, the epilogue: tcgen05.ld,
+//               SwiGLU -> h, or fp32 K-split partials.
+// int4 down GEMMs with an even number of output tiles take two adjacent tiles
+// per item (like gate and up), so each token tile serves two weight tiles.
+// Prefill-sized int4 items are at most 192 rows wide: 2 x 192 accumulator
+// columns + 2 A slots of 64 columns fill the 512 TMEM columns.
 //
 // Every wait is bounded (ptx.cuh); on a timeout the CTA drains its in-flight
 // copies and MMAs, frees TMEM and returns with MOE_DEVERR_TIMEOUT set.
@@ -36,9 +43,10 @@ namespace {
 
 constexpr int MISC_INTS = 10;   // [0] tmem [1] abort [2] items; consumed raw/a/b [3..5];
                                 // issued raw/a/b [6..8]; [9] stays 0
+constexpr int A_SLOT_COLS = 32;   // TMEM columns of one matrix's 64-wide fp16 K slice
 
 struct Shared {   // views into the dynamic shared-memory carve-out
-  uint8_t* a_ring;
+  uint8_t* a_ring;   // bf16 only (int4 A slots live in TMEM)
   uint8_t* b_ring;
   uint8_t* raw_ring;
   uint64_t *a_full, *a_empty, *b_full, *b_empty, *raw_full, *raw_empty;
@@ -48,7 +56,7 @@ struct Shared {   // views into the dynamic shared-memory carve-out
 };
 
 size_t carve_bytes(int nmat, bool int4, int bn, int n_a, int n_b, int n_raw, int n_groups) {
-  size_t s = (size_t)n_a * nmat * BF16_TILE_BYTES + (size_t)n_b * bn * 128;
+  size_t s = (int4 ? 0 : (size_t)n_a * nmat * BF16_TILE_BYTES) + (size_t)n_b * bn * 128;
   if (int4) s += (size_t)n_raw * nmat * I4_MAT_BYTES;
   s = align_up(s, 16);
   s += 8 * (size_t)(2 * (n_a + n_b + (int4 ? n_raw : 0)) + 3);
@@ -56,36 +64,42 @@ size_t carve_bytes(int nmat, bool int4, int bn, int n_a, int n_b, int n_raw, int
   return s;
 }
 
-// One 16-byte quad (32 K elements of one weight row) -> 4 chunks of the swizzled
-// A row: fp16((q - z) * s).
-__device__ __forceinline__ void dequant_quad(uint4 wq, __half2 c2, __half2 s2, uint8_t* arow, int j,
-                                             int r) {
-  const uint32_t words[4] = {wq.x, wq.y, wq.z, wq.w};
+// 8 words of one row (64 K elements) -> 32 fp16 pairs (q - z) * s, K order.
+__device__ __forceinline__ void dequant_words(const uint4& w0, const uint4& w1, uint32_t nz_a, uint32_t nz_b,
+                                              __half2 s2, uint32_t (&v)[32]) {
+  const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    uint32_t o[4];
-    codes_of_word(words[w], o);
+  for (int w = 0; w < 8; ++w) codes_minus_zero(words[w], nz_a, nz_b, &v[w * 4]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __half2 b = *reinterpret_cast<const __half2*>(&o[i]);
-      b = __hmul2(__hsub2(b, c2), s2);   // (q - z) exact, then one rounding of * s
-      o[i] = *reinterpret_cast<uint32_t*>(&b);
-    }
-    const int chunk = (j * 4 + w) ^ (r & 7);
-    *reinterpret_cast<uint4*>(arow + chunk * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+  for (int i = 0; i < 32; ++i) {
+    const __half2 b = __hmul2(*reinterpret_cast<const __half2*>(&v[i]), s2);   // one rounding
+    v[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+}
+__device__ __forceinline__ void dequant_words16(const uint4& w0, uint32_t nz_a, uint32_t nz_b, __half2 s2,
+                                                uint32_t (&v)[16]) {
+  const uint32_t words[4] = {w0.x, w0.y, w0.z, w0.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) codes_minus_zero(words[w], nz_a, nz_b, &v[w * 4]);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const __half2 b = __hmul2(*reinterpret_cast<const __half2*>(&v[i]), s2);
+    v[i] = *reinterpret_cast<const uint32_t*>(&b);
   }
 }
 
 }  // namespace
 
-template <int FMT, bool GATEUP, int NDQ>
+template <int FMT, bool GATEUP, int NDQ, bool PAIR>
 __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs p) {
-  constexpr int NMAT = GATEUP ? 2 : 1;
   constexpr bool INT4 = (FMT == MOE_W_INT4_G128);
+  static_assert(!PAIR || (INT4 && !GATEUP), "paired output tiles: int4 down GEMM only");
+  constexpr int NMAT = (GATEUP || PAIR) ? 2 : 1;
   static_assert(!INT4 || NDQ == 8, "int4 dequantisation assumes 8 warps (2 per TMEM quadrant)");
   constexpr uint32_t AB_BF16 = INT4 ? 0u : 1u;   // operand type of the MMA
-  constexpr uint32_t A_STAGE = NMAT * BF16_TILE_BYTES;
+  constexpr uint32_t A_STAGE = NMAT * BF16_TILE_BYTES;   // bf16: shared-memory A stage
+  constexpr uint32_t A_SLOT = NMAT * A_SLOT_COLS;        // int4: TMEM columns of one A slot
   constexpr uint32_t RAW_STAGE = NMAT * I4_MAT_BYTES;
   constexpr int NDQ_THREADS = NDQ * 32;
   const uint32_t B_STAGE = (uint32_t)p.bn * 128u;
@@ -96,7 +110,7 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
 
   Shared S;
   S.a_ring = base;
-  S.b_ring = S.a_ring + (size_t)p.n_a * A_STAGE;
+  S.b_ring = S.a_ring + (INT4 ? 0 : (size_t)p.n_a * A_STAGE);
   S.raw_ring = S.b_ring + (size_t)p.n_b * B_STAGE;
   uint8_t* cur = S.raw_ring + (INT4 ? (size_t)p.n_raw * RAW_STAGE : 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + align_up((size_t)(cur - base), 16));
@@ -157,6 +171,7 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
   tc_fence_after();
   const uint32_t tmem_base = (uint32_t)S.misc[0];
   const int total = S.misc[2];
+  const uint32_t a_col0 = (uint32_t)(NMAT * p.bn);   // int4: A slots follow the accumulators
 
   // ------------------------------------------------------------ roles
   if (warp == 0) {
@@ -176,8 +191,17 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
             if (!(ok = mbar_wait(smem_u32(&S.raw_empty[rr.i]), rr.ph ^ 1u, abort_flag, p.err))) break;
             const uint32_t bar = smem_u32(&S.raw_full[rr.i]);
             mbar_arrive_expect_tx(bar, RAW_STAGE);
-            bulk_g2s_hint(smem_u32(S.raw_ring + (size_t)rr.i * RAW_STAGE),
-                          sec + ((size_t)it.mt * (p.K / QGROUP) + kg) * RAW_STAGE, RAW_STAGE, bar, pol);
+            const uint32_t raw = smem_u32(S.raw_ring + (size_t)rr.i * RAW_STAGE);
+            if (PAIR) {
+#pragma unroll
+              for (int m = 0; m < 2; ++m)
+                bulk_g2s_hint(raw + m * I4_MAT_BYTES,
+                              sec + ((size_t)(2 * it.mt + m) * (p.K / QGROUP) + kg) * I4_MAT_BYTES,
+                              I4_MAT_BYTES, bar, pol);
+            } else {
+              bulk_g2s_hint(raw, sec + ((size_t)it.mt * (p.K / QGROUP) + kg) * RAW_STAGE, RAW_STAGE, bar,
+                            pol);
+            }
             rr.next();
             ++issued_raw;
           }
@@ -207,57 +231,53 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
       S.misc[8] = issued_b;
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer.  The whole warp runs the loop and lane 0
-    // issues; the next K step's operands are prepared while this step's MMAs
-    // issue (they depend only on ring positions).
+    // ---------------- MMA issuer: the whole warp runs the loop, one elected
+    // lane issues.  Descriptors are built once and offset per stage / K step.
     Ring ra{0, 0, p.n_a}, rb{0, 0, p.n_b};
     int consumed_a = 0, consumed_b = 0;
     uint32_t it_count = 0;
     bool ok = true;
-    struct Ops {
-      uint64_t a[NMAT][4];
-      uint64_t b[4];
-    };
-    const uint32_t a_ring0 = smem_u32(S.a_ring), b_ring0 = smem_u32(S.b_ring);
-    auto prep = [&](int ai, int bi) -> Ops {
-      Ops o;
-#pragma unroll
-      for (int kk = 0; kk < KSTEP / 16; ++kk) {
-        o.b[kk] = sdesc_kmajor_sw128(b_ring0 + (uint32_t)bi * B_STAGE + kk * 32);
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m)
-          o.a[m][kk] = sdesc_kmajor_sw128(a_ring0 + (uint32_t)ai * A_STAGE + m * BF16_TILE_BYTES + kk * 32);
-      }
-      return o;
-    };
-    Ops curo = prep(ra.i, rb.i);
+    const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(S.b_ring));
+    const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(S.a_ring));   // bf16 only
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
       Item it;
       if (!decode_item(item, p, S.W, it)) continue;
       int g0, g1;
       kgroups(p, it.ks, g0, g1);
-      if (!(ok = mbar_wait(smem_u32(S.tmem_empty), (it_count & 1u) ^ 1u, abort_flag, p.err))) break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tmem_empty), (it_count & 1u) ^ 1u,
+                                                   abort_flag, p.err))))
+        break;
       tc_fence_after();
       const uint32_t idesc = idesc_f16kind_f32(TILE_M, (uint32_t)((it.n_rows + 15) & ~15), AB_BF16);
       for (int kg = g0; kg < g1 && ok; ++kg) {
         for (int h = 0; h < 2; ++h) {
-          if (!(ok = mbar_wait(smem_u32(&S.a_full[ra.i]), ra.ph, abort_flag, p.err))) break;
-          if (!(ok = mbar_wait(smem_u32(&S.b_full[rb.i]), rb.ph, abort_flag, p.err))) break;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.a_full[ra.i]), ra.ph, abort_flag, p.err))))
+            break;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.b_full[rb.i]), rb.ph, abort_flag, p.err))))
+            break;
           tc_fence_after();
-          const Ops nxt = prep(ra.i + 1 == p.n_a ? 0 : ra.i + 1, rb.i + 1 == p.n_b ? 0 : rb.i + 1);
           const bool fresh = (kg == g0 && h == 0);
-          if (lane == 0) {
+          const uint64_t bd = bdesc0 + (uint64_t)(((uint32_t)rb.i * B_STAGE) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < KSTEP / 16; ++kk)
+          for (int kk = 0; kk < KSTEP / 16; ++kk) {
+            const uint64_t bq = bd + (uint64_t)((kk * 32) >> 4);
+            const uint32_t acc = (fresh && kk == 0) ? 0u : 1u;
+            if constexpr (INT4) {
+              const uint32_t a0 = tmem_base + a_col0 + (uint32_t)ra.i * A_SLOT + (uint32_t)(kk * 8);
+              if (NMAT == 2)
+                mma2_ta_elect(tmem_base, tmem_base + (uint32_t)p.bn, a0, a0 + A_SLOT_COLS, bq, idesc, acc);
+              else
+                mma_ta_elect(tmem_base, a0, bq, idesc, acc);
+            } else {
+              const uint64_t aq = adesc0 + (uint64_t)(((uint32_t)ra.i * A_STAGE + kk * 32) >> 4);
 #pragma unroll
               for (int m = 0; m < NMAT; ++m)
-                mma_f16kind(tmem_base + (uint32_t)(m * p.bn), curo.a[m][kk], curo.b[kk], idesc,
-                            (fresh && kk == 0) ? 0u : 1u);
-            mma_commit(smem_u32(&S.a_empty[ra.i]));
-            mma_commit(smem_u32(&S.b_empty[rb.i]));
+                mma_ss_elect(tmem_base + (uint32_t)(m * p.bn), aq + (uint64_t)((m * BF16_TILE_BYTES) >> 4), bq,
+                             idesc, acc);
+            }
           }
-          __syncwarp();
-          curo = nxt;
+          mma_commit_elect(smem_u32(&S.a_empty[ra.i]));
+          mma_commit_elect(smem_u32(&S.b_empty[rb.i]));
           ra.next();
           rb.next();
           ++consumed_a;
@@ -265,8 +285,7 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) mma_commit(smem_u32(S.tmem_full));
-      __syncwarp();
+      mma_commit_elect(smem_u32(S.tmem_full));
       ++it_count;
     }
     if (lane == 0) {
@@ -277,9 +296,10 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
     const int wr = warp - 2;                  // 0 .. NDQ-1
     const int quad = warp & 3;                // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;           // weight row of the tile = TMEM lane
-    // int4 ownership: gate/up -> matrix m_own of row r (both quads); down -> quad j_own of row r
-    const int m_own = GATEUP ? (wr >> 2) : 0;
-    const int j_own = GATEUP ? 0 : (wr >> 2);
+    const uint32_t tl = tmem_base + ((uint32_t)(quad * 32) << 16);
+    // int4 ownership: two matrices -> matrix m_own of row r; one matrix -> K quad j_own of row r
+    const int m_own = NMAT == 2 ? (wr >> 2) : 0;
+    const int j_own = NMAT == 2 ? 0 : (wr >> 2);
     constexpr int NHALF = NDQ / 4;            // epilogue: column interleave per quadrant
     Ring ra{0, 0, p.n_a}, rr{0, 0, p.n_raw};
     int consumed_raw = 0;
@@ -297,21 +317,31 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
           const uint8_t* mat = S.raw_ring + (size_t)rr.i * RAW_STAGE + m_own * I4_MAT_BYTES;
           const uint32_t sz = *reinterpret_cast<const uint32_t*>(mat + I4_PACKED_BYTES + r * 4);
           const __half sh = __ushort_as_half((unsigned short)(sz & 0xFFFFu));
-          const __half zh = __ushort_as_half((unsigned short)(sz >> 16));
+          const float zf = __half2float(__ushort_as_half((unsigned short)(sz >> 16)));
           const __half2 s2 = __halves2half2(sh, sh);
-          const __half2 c2 = __hadd2(__halves2half2(zh, zh), __float2half2_rn(1024.f));
-          for (int h = 0; h < 2; ++h) {
+          const __half2 za = __float2half2_rn(-(1024.f + zf)), zb = __float2half2_rn(-(64.f + zf));
+          const uint32_t nz_a = *reinterpret_cast<const uint32_t*>(&za);
+          const uint32_t nz_b = *reinterpret_cast<const uint32_t*>(&zb);
+          for (int h = 0; h < 2; ++h) {   // K slices of the group: 64 codes of my row each
             ok = __all_sync(0xffffffffu,
                             mbar_wait(smem_u32(&S.a_empty[ra.i]), ra.ph ^ 1u, abort_flag, p.err));
             if (!ok) break;
-            uint8_t* arow = S.a_ring + (size_t)ra.i * A_STAGE + m_own * BF16_TILE_BYTES + r * 128;
-#pragma unroll
-            for (int jj = 0; jj < (GATEUP ? 2 : 1); ++jj) {
-              const int j = GATEUP ? jj : j_own;
-              const uint4 wq = *reinterpret_cast<const uint4*>(mat + ((h * 2 + j) * TILE_M + r) * 16);
-              dequant_quad(wq, c2, s2, arow, j, r);
+            tc_fence_after();
+            const uint32_t ta = tl + a_col0 + (uint32_t)ra.i * A_SLOT;
+            if (NMAT == 2) {
+              uint32_t v[32];
+              const uint4 w0 = *reinterpret_cast<const uint4*>(mat + ((h * 2 + 0) * TILE_M + r) * 16);
+              const uint4 w1 = *reinterpret_cast<const uint4*>(mat + ((h * 2 + 1) * TILE_M + r) * 16);
+              dequant_words(w0, w1, nz_a, nz_b, s2, v);
+              tmem_st_32(ta + (uint32_t)(m_own * A_SLOT_COLS), v);
+            } else {
+              uint32_t v[16];
+              const uint4 w0 = *reinterpret_cast<const uint4*>(mat + ((h * 2 + j_own) * TILE_M + r) * 16);
+              dequant_words16(w0, nz_a, nz_b, s2, v);
+              tmem_st_16(ta + (uint32_t)(j_own * 16), v);
             }
-            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
             mbar_arrive(smem_u32(&S.a_full[ra.i]));
             ra.next();
           }
@@ -323,17 +353,16 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
         if (!ok) break;
       }
       // ---- epilogue: one accumulator per item
-      const uint32_t tl = tmem_base + ((uint32_t)(quad * 32) << 16);
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tmem_full), it_count & 1u, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
       const int half = wr >> 2;
-      const int f = it.mt * TILE_M + r;   // output feature of this thread
       const int n_chunks = (it.n_rows + 15) >> 4;
       for (int c = half; c < n_chunks; c += NHALF) {
         uint32_t acc0[16];
         tmem_ld_16(tl + (uint32_t)(c * 16), acc0);
         if (GATEUP) {
+          const int f = it.mt * TILE_M + r;   // output feature of this thread
           uint32_t acc1[16];
           tmem_ld_16(tl + (uint32_t)(p.bn + c * 16), acc1);
           tmem_ld_wait();
@@ -350,12 +379,19 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
             }
           }
         } else {
-          tmem_ld_wait();
           float* y = reinterpret_cast<float*>(p.out) + (size_t)it.ks * p.out_split_stride;
+          uint32_t acc1[16];
+          if (PAIR) tmem_ld_16(tl + (uint32_t)(p.bn + c * 16), acc1);
+          tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int n = c * 16 + i;
-            if (n < it.n_rows) y[(size_t)(it.r0 + n) * p.out_ld + f] = __uint_as_float(acc0[i]);
+          for (int m = 0; m < NMAT; ++m) {
+            const int f = (PAIR ? 2 * it.mt + m : it.mt) * TILE_M + r;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int n = c * 16 + i;
+              if (n < it.n_rows)
+                y[(size_t)(it.r0 + n) * p.out_ld + f] = __uint_as_float(m == 0 ? acc0[i] : acc1[i]);
+            }
           }
         }
       }
@@ -382,8 +418,8 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
         mbar_wait(smem_u32(&fulls[rg][q % ns[rg]]), (uint32_t)((q / ns[rg]) & 1), no_abort, p.err);
     }
   }
-  if (warp == 1 && lane == 0) {   // every MMA this CTA issued has finished
-    mma_commit(smem_u32(S.fin));
+  if (warp == 1) {   // every MMA this CTA issued has finished
+    mma_commit_elect(smem_u32(S.fin));
     mbar_wait(smem_u32(S.fin), 0, no_abort, p.err);
   }
   tc_fence_before();
@@ -401,35 +437,40 @@ GemmPlan plan_gemm(int fmt, bool gateup, int bn, int n_groups, int n_mt) {
   const bool int4 = fmt == MOE_W_INT4_G128;
   if (gemm_is_group(fmt, bn)) return plan_gemm_group(gateup, bn, n_groups, n_mt);
   GemmPlan pl{};
-  const int nmat = gateup ? 2 : 1;
   pl.group = false;
-  pl.pair = false;
+  pl.pair = !gateup && down_paired(fmt, n_mt);
+  const int nmat = (gateup || pl.pair) ? 2 : 1;
   pl.ndq = int4 ? 8 : 4;
   const size_t budget = 227 * 1024 - 1024;   // opt-in maximum minus the alignment pad
   pl.n_b = bn >= 128 ? 3 : (bn >= 64 ? 4 : 8);
+  uint32_t cols = 32;
   if (int4) {
-    pl.n_a = gateup ? (bn >= 128 ? 2 : 3) : (bn >= 128 ? 3 : 4);
+    // A slots in TMEM after the accumulators (nmat * bn columns), 2..4 of them
+    const int acc_cols = nmat * bn;
+    pl.n_a = (512 - acc_cols) / (nmat * A_SLOT_COLS);
+    if (pl.n_a > 4) pl.n_a = 4;
+    if (bn >= 128 && pl.n_b < 4) pl.n_b = 4;
     pl.n_raw = 2;
     while (pl.n_raw < 12 &&
            carve_bytes(nmat, true, bn, pl.n_a, pl.n_b, pl.n_raw + 1, n_groups) <= budget)
       ++pl.n_raw;
+    while (cols < (uint32_t)(acc_cols + pl.n_a * nmat * A_SLOT_COLS)) cols <<= 1;
   } else {
     pl.n_raw = 0;
     pl.n_a = 2;
     while (pl.n_a < 8 && carve_bytes(nmat, false, bn, pl.n_a + 1, pl.n_b, 0, n_groups) <= budget)
       ++pl.n_a;
+    while (cols < (uint32_t)(nmat * bn)) cols <<= 1;
   }
   pl.smem_bytes = carve_bytes(nmat, int4, bn, pl.n_a, pl.n_b, pl.n_raw, n_groups) + 1024;
-  uint32_t cols = 32;
-  while (cols < (uint32_t)(nmat * bn)) cols <<= 1;
   pl.tmem_cols = cols;
   return pl;
 }
 
-template <int FMT, bool GATEUP, int NDQ>
+template <int FMT, bool GATEUP, int NDQ, bool PAIR>
 static cudaError_t launch_one(const CUtensorMap& tmap, const GemmArgs& a, const GemmPlan& pl,
                               int grid, cudaStream_t s, bool pdl) {
-  auto kern = grouped_gemm_kernel<FMT, GATEUP, NDQ>;
+  auto kern = grouped_gemm_kernel<FMT, GATEUP, NDQ, PAIR>;
   static bool attr_set = false;   // per instantiation; the maximum is requested once
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -447,11 +488,16 @@ cudaError_t launch_grouped_gemm(int fmt, bool gateup, const CUtensorMap& tmap_b,
   args.n_raw = plan.n_raw;
   args.tmem_cols = plan.tmem_cols;
   constexpr int I4 = MOE_W_INT4_G128, B16 = MOE_W_BF16;
-  if (fmt == I4)
-    return gateup ? launch_one<I4, true, 8>(tmap_b, args, plan, grid, stream, pdl)
-                  : launch_one<I4, false, 8>(tmap_b, args, plan, grid, stream, pdl);
-  return gateup ? launch_one<B16, true, 4>(tmap_b, args, plan, grid, stream, pdl)
-                : launch_one<B16, false, 4>(tmap_b, args, plan, grid, stream, pdl);
+  if (fmt == I4) {
+    if (gateup) return launch_one<I4, true, 8, false>(tmap_b, args, plan, grid, stream, pdl);
+    if (plan.pair) {
+      args.n_mt /= 2;   // work items name pairs of output tiles
+      return launch_one<I4, false, 8, true>(tmap_b, args, plan, grid, stream, pdl);
+    }
+    return launch_one<I4, false, 8, false>(tmap_b, args, plan, grid, stream, pdl);
+  }
+  return gateup ? launch_one<B16, true, 4, false>(tmap_b, args, plan, grid, stream, pdl)
+                : launch_one<B16, false, 4, false>(tmap_b, args, plan, grid, stream, pdl);
 }
 
 }  // namespace moe

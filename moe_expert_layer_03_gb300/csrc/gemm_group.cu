@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups, int n_mt) {
   GemmPlan pl{};
   pl.group = true;
-  pl.pair = !gateup && n_mt % 2 == 0;
+  pl.pair = !gateup && down_paired(MOE_W_INT4_G128, n_mt);
   const int nmat = (gateup || pl.pair) ? 2 : 1;
   pl.ndq = G_NUP + G_NFOLD;
   const size_t budget = 227 * 1024 - 1024;

@@ -85,9 +85,18 @@ inline bool gemm_uses_fp16(int fmt) { return fmt == MOE_W_INT4_G128; }
 // Uses the group-scaled decode kernel (int4, row chunks of <= 32)?
 inline bool gemm_is_group(int fmt, int bn) { return fmt == MOE_W_INT4_G128 && bn <= 32; }
 // Work tiles per (group, row chunk, K split) of the down GEMM with n_mt output
-// tiles: the decode kernel pairs adjacent tiles when n_mt is even.
-inline int down_work_tiles(int fmt, int bn, int n_mt) {
-  return gemm_is_group(fmt, bn) && n_mt % 2 == 0 ? n_mt / 2 : n_mt;
+// tiles: the int4 kernels pair adjacent tiles when n_mt is even.
+inline bool down_paired(int fmt, int n_mt) { return fmt == MOE_W_INT4_G128 && n_mt % 2 == 0; }
+inline int down_work_tiles(int fmt, int n_mt) { return down_paired(fmt, n_mt) ? n_mt / 2 : n_mt; }
+// Row-chunk width (the GEMMs' N): a power of two >= twice the mean rows per
+// expert, 16..256; int4 layers stop at 192 so that the gate and up
+// accumulators (2 x 192 TMEM columns) leave room for the dequantised A tiles.
+inline int choose_bn(int A, int E, int fmt) {
+  const int mean = (A + E - 1) / E;
+  int bn = 16;
+  while (bn < 2 * mean && bn < 256) bn <<= 1;
+  if (fmt == MOE_W_INT4_G128 && bn > 128) bn = 192;
+  return bn;
 }
 
 GemmPlan plan_gemm(int fmt, bool gateup, int bn, int n_groups, int n_mt);

@@ -253,6 +253,17 @@ MOE_DEV void mma2_ta_elect(uint32_t d0, uint32_t d1, uint32_t a0, uint32_t a1, u
       "r"(d1), "r"(a0), "r"(a1), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Same with A from shared memory (descriptor), issued from a converged warp.
+MOE_DEV void mma_ss_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives once on `bar` when every tcgen05 op this thread issued so far is done.
 MOE_DEV void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

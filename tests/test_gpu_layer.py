@@ -29,8 +29,12 @@ SMALL = {
     "dense_E1": ms.LayerConfig("dense_E1", T=20, d=256, F=512, E=1, k=1, fmt="int4"),
     # row chunks of 32 (int4 group-scaled main loop at its wider width)
     "int4_chunk32": ms.LayerConfig("int4_chunk32", T=48, d=384, F=512, E=8, k=2, fmt="int4", seed=4),
-    # row chunks of 64 and 256 (int4 main loop that dequantises to fp16 in shared memory)
+    # row chunks of 64 (int4 prefill kernel: fp16 A tiles in TMEM, paired down tiles)
     "int4_chunk64": ms.LayerConfig("int4_chunk64", T=96, d=256, F=384, E=8, k=2, fmt="int4", seed=6),
+    # row chunks of 128 with an odd number of output tiles (one down tile per item)
+    "int4_wide_odd": ms.LayerConfig("int4_wide_odd", T=96, d=384, F=512, E=4, k=2, fmt="int4", seed=7),
+    # row chunks of 192, the widest int4 chunk
+    "int4_wide192": ms.LayerConfig("int4_wide192", T=200, d=256, F=384, E=2, k=1, fmt="int4", seed=8),
 }
 
 
