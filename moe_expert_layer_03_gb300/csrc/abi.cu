@@ -64,6 +64,19 @@ bool make_row_map(CUtensorMap* m, const void* base, int rows, int K, int box_row
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Byte rows [rows][K] (e4m3) -> TMA map with a {128 x box_rows} box (one
+// 128-byte row per token row and quantisation group) and the 128-byte swizzle.
+bool make_byte_row_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
+  if (!have_encoder()) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {(cuuint32_t)QGROUP, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 moe_status check_pool(const moe_pool* p, bool single) {
   if (!p || !p->pool || !p->expert_to_slot) return MOE_ERR_INVALID_ARG;
   if (p->fmt != MOE_W_BF16 && p->fmt != MOE_W_INT4_G128) return MOE_ERR_INVALID_ARG;
@@ -108,9 +121,38 @@ int choose_ksplit(int A, int E, bool has_shared, int bn, int fmt, int d, int F) 
   return s < 1 ? 1 : s;
 }
 
+// The int4 decode GEMMs' e4m3 operands (see gemm_group.cu): the gathered rows
+// and h as hi/lo byte rows [2*rows][K], per (group, row) sums [K/128][rows]
+// and unscale factors ([rows] for x, [F/128][rows] for h).
+struct Fp8Rows {
+  uint8_t* xq;
+  float *xs, *xe;
+  uint8_t* hq;
+  float *hs, *he;
+};
+struct Fp8Offsets {
+  size_t xq, xs, xe, hq, hs, he;
+};
+// Appends the e4m3 regions at offset o (1 KB aligned) and returns the new end.
+size_t fp8_regions(Fp8Offsets& f, size_t o, int rows, int d, int F) {
+  f.xq = o;  o = up1k(o + 2 * (size_t)rows * d);
+  f.xs = o;  o = up1k(o + (size_t)(d / QGROUP) * rows * 4 + SUMS_PAD_BYTES);
+  f.xe = o;  o = up1k(o + (size_t)rows * 4);
+  f.hq = o;  o = up1k(o + 2 * (size_t)rows * F);
+  f.hs = o;  o = up1k(o + (size_t)(F / QGROUP) * rows * 4 + SUMS_PAD_BYTES);
+  f.he = o;  o = up1k(o + (size_t)(F / QGROUP) * rows * 4 + SUMS_PAD_BYTES);
+  return o;
+}
+Fp8Rows fp8_rows(uint8_t* W, const Fp8Offsets& f) {
+  return Fp8Rows{W + f.xq, (float*)(W + f.xs), (float*)(W + f.xe),
+                 W + f.hq, (float*)(W + f.hs), (float*)(W + f.he)};
+}
+
 struct LayerLayout {
   int A, Tsh, rows, E, d, F, bn, ksplit;
+  bool fp8;   // int4 decode path: e4m3 operands instead of x_perm / h
   size_t err, idx, w, counts, offsets, roa, tor, xperm, h, part, total;
+  Fp8Offsets f8;
 };
 
 LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* shared) {
@@ -131,9 +173,11 @@ LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* s
   L.offsets = o;  o = up1k(o + (size_t)(L.E + 2) * 4);
   L.roa = o;      o = up1k(o + (size_t)L.A * 4);
   L.tor = o;      o = up1k(o + (size_t)L.rows * 4);
-  L.xperm = o;    o = up1k(o + (size_t)L.rows * L.d * 2);
-  L.h = o;        o = up1k(o + (size_t)L.rows * L.F * 2);
+  L.fp8 = gemm_is_group(routed->fmt, L.bn);
+  L.xperm = o;    o = up1k(o + (L.fp8 ? 0 : (size_t)L.rows * L.d * 2));
+  L.h = o;        o = up1k(o + (L.fp8 ? 0 : (size_t)L.rows * L.F * 2));
   L.part = o;     o = up1k(o + (size_t)L.ksplit * L.rows * L.d * 4);
+  if (L.fp8) o = fp8_regions(L.f8, o, L.rows, L.d, L.F);
   L.total = o;
   return L;
 }
@@ -161,18 +205,23 @@ GemmArgs base_args(const moe_pool* routed, const moe_pool* shared, int* err) {
 }
 
 // gate/up (SwiGLU) then down over the row groups described by `offsets`.
-// x_rows and h are fp16 for int4 pools, bf16 otherwise.  pdl: both launches
-// follow a kernel of the same call (dependent launch).
+// x_rows and h are fp16 for int4 pools, bf16 otherwise; with f8 (the int4
+// decode path) the GEMMs read and write the e4m3 forms instead.  pdl: both
+// launches follow a kernel of the same call (dependent launch).
 moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups, int rows,
                    const moe_pool* routed, const moe_pool* shared, int bn, int ksplit, uint16_t* h,
-                   float* part, int* err, cudaStream_t s, bool pdl,
+                   float* part, const Fp8Rows* f8, int* err, cudaStream_t s, bool pdl,
                    cudaEvent_t ev_mid, cudaEvent_t ev_down) {
   const int d = routed->d_model, F = routed->d_ff, fmt = routed->fmt;
   const bool f16 = gemm_uses_fp16(fmt);
   const int grid = sm_count();
   CUtensorMap mx, mh;
-  if (!make_row_map(&mx, x_rows, rows, d, bn, f16) || !make_row_map(&mh, h, rows, F, bn, f16))
+  if (f8) {
+    if (!make_byte_row_map(&mx, f8->xq, 2 * rows, d, bn) || !make_byte_row_map(&mh, f8->hq, 2 * rows, F, bn))
+      return MOE_ERR_CUDA;
+  } else if (!make_row_map(&mx, x_rows, rows, d, bn, f16) || !make_row_map(&mh, h, rows, F, bn, f16)) {
     return MOE_ERR_CUDA;
+  }
   GemmArgs a = base_args(routed, shared, err);
   a.offsets = offsets;
   a.n_groups = n_groups;
@@ -187,6 +236,14 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
   g.out = h;
   g.out_ld = F;
   g.out_split_stride = 0;
+  if (f8) {
+    g.out = nullptr;
+    g.b_sum = f8->xs;
+    g.b_scale = f8->xe;
+    g.q_out = f8->hq;
+    g.sum_out = f8->hs;
+    g.scale_out = f8->he;
+  }
   if (launch_grouped_gemm(fmt, true, mx, g, plan_gemm(fmt, true, bn, n_groups, F / TILE_M), grid, s,
                           pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -200,6 +257,10 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
   dn.out = part;
   dn.out_ld = d;
   dn.out_split_stride = (unsigned long long)rows * d;
+  if (f8) {
+    dn.b_sum = f8->hs;
+    dn.b_scale = f8->he;
+  }
   if (launch_grouped_gemm(fmt, false, mh, dn, plan_gemm(fmt, false, bn, n_groups, d / TILE_M), grid, s,
                           pdl && !ev_mid) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -246,6 +307,7 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
   uint16_t* h = (uint16_t*)(W + L.h);
   float* part = (float*)(W + L.part);
   const bool f16 = gemm_uses_fp16(routed->fmt);
+  const Fp8Rows f8 = L.fp8 ? fp8_rows(W, L.f8) : Fp8Rows{};
   auto rec = [&](int i) -> bool {
     return !ev || !ev[i] || cudaEventRecord((cudaEvent_t)ev[i], s) == cudaSuccess;
   };
@@ -259,11 +321,16 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
   if (launch_permute_index(idx, T, k, E, L.Tsh, counts, offsets, roa, tor, err, s, pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!rec(MOE_STAGE_GATHER)) return MOE_ERR_CUDA;
-  if (launch_gather_rows(x, tor, L.rows, T, L.d, xperm, f16, sm_count(), s, pdl) != cudaSuccess)
+  if (L.fp8) {
+    if (launch_gather_rows_fp8(x, tor, L.rows, T, L.d, f8.xq, f8.xs, f8.xe, sm_count(), s, pdl) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else if (launch_gather_rows(x, tor, L.rows, T, L.d, xperm, f16, sm_count(), s, pdl) != cudaSuccess) {
     return MOE_ERR_CUDA;
+  }
   if (!rec(MOE_STAGE_GATE_UP)) return MOE_ERR_CUDA;
   st = run_ffn(xperm, offsets, E + (shared ? 1 : 0), L.rows, routed, shared, L.bn, L.ksplit, h, part,
-               err, s, pdl, ev ? (cudaEvent_t)ev[MOE_STAGE_DOWN] : nullptr,
+               L.fp8 ? &f8 : nullptr, err, s, pdl, ev ? (cudaEvent_t)ev[MOE_STAGE_DOWN] : nullptr,
                ev ? (cudaEvent_t)ev[MOE_STAGE_COMBINE] : nullptr);
   if (st != MOE_OK) return st;
   if (launch_combine_partials(part, L.ksplit, (size_t)L.rows * L.d, roa, w, T, k, L.d,
@@ -346,10 +413,12 @@ moe_status moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int k,
 }
 
 // Workspace of the standalone grouped FFN: error word, h, down partials and, for
-// int4 pools, an fp16 copy of x_perm with its per-group row sums and the sums of h.
+// int4 pools, an fp16 copy of x_perm, or (decode path) the e4m3 operands.
 struct FfnLayout {
   int bn, ksplit;
+  bool fp8;
   size_t h, part, x16, total;
+  Fp8Offsets f8;
 };
 
 FfnLayout ffn_layout(int A, const moe_pool* pool) {
@@ -358,10 +427,12 @@ FfnLayout ffn_layout(int A, const moe_pool* pool) {
   L.bn = choose_bn(A, pool->n_experts, pool->fmt);
   L.ksplit = choose_ksplit(A, pool->n_experts, false, L.bn, pool->fmt, d, F);
   const bool f16 = gemm_uses_fp16(pool->fmt);
+  L.fp8 = gemm_is_group(pool->fmt, L.bn);
   size_t o = 1024;
-  L.h = o;     o = up1k(o + (size_t)A * F * 2);
+  L.h = o;     o = up1k(o + (L.fp8 ? 0 : (size_t)A * F * 2));
   L.part = o;  o = up1k(o + (size_t)L.ksplit * A * d * 4);
-  L.x16 = o;   o = up1k(o + (f16 ? (size_t)A * d * 2 : 0));
+  L.x16 = o;   o = up1k(o + (f16 && !L.fp8 ? (size_t)A * d * 2 : 0));
+  if (L.fp8) o = fp8_regions(L.f8, o, A, d, F);
   L.total = o;
   return L;
 }
@@ -388,16 +459,21 @@ moe_status moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int A
   cudaStream_t s = (cudaStream_t)stream;
   const bool f16 = gemm_uses_fp16(pool->fmt);
   const uint16_t* rows_in = x_perm;
+  const Fp8Rows f8 = L.fp8 ? fp8_rows(W, L.f8) : Fp8Rows{};
   if (launch_clear_word(err, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (f16) {   // the int4 GEMMs read fp16 rows
+  if (L.fp8) {   // the int4 decode GEMMs read e4m3 rows
+    if (launch_gather_rows_fp8(x_perm, nullptr, A, A, pool->d_model, f8.xq, f8.xs, f8.xe, sm_count(), s,
+                               true) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else if (f16) {   // the other int4 GEMMs read fp16 rows
     uint16_t* x16 = (uint16_t*)(W + L.x16);
     if (launch_gather_rows(x_perm, nullptr, A, A, pool->d_model, x16, true, sm_count(), s, true) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     rows_in = x16;
   }
-  st = run_ffn(rows_in, offsets, pool->n_experts, A, pool, nullptr, L.bn, L.ksplit, h, part, err, s,
-               true, nullptr, nullptr);
+  st = run_ffn(rows_in, offsets, pool->n_experts, A, pool, nullptr, L.bn, L.ksplit, h, part,
+               L.fp8 ? &f8 : nullptr, err, s, true, nullptr, nullptr);
   if (st != MOE_OK) return st;
   return launch_reduce_splits(part, L.ksplit, (size_t)A * pool->d_model, A, pool->d_model, y_perm,
                               s, true) == cudaSuccess

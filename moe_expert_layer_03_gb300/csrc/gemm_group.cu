@@ -3,39 +3,47 @@
 //
 // "125B MoE on an RTX 3090 at 100+ tok/s": sec. 3.2 (grouped GEMM over the
 // active experts, each a two-layer MLP), sec. 3.1 (per-expert int4 weights with
-// their own scale and zero-point, turned into fp16 for the tensor cores without
-// a separate pass over memory).
+// their own scale and zero-point, turned into tensor-core operands without a
+// separate pass over memory).
 //
-// At decode the layer streams int4 weights from HBM; the tensor-core work per
-// weight is tiny, so the kernel is built to keep per-byte overheads low:
-//   * one pipeline stage = one quantisation group (128 K): one bulk copy of
-//     nibbles + scales and one TMA pair for the token rows, all on one
-//     barrier; 8 K16 steps of M = 128 weight rows x N = 16/32 token rows;
-//   * the A operand lives in tensor memory: each unpack thread owns one weight
-//     row (one TMEM lane) and writes the group's codes with tcgen05.st, so
-//     shared memory carries only the nibbles and the small token tiles;
-//   * the codes are q - z, exact in fp16 (a LOP3 into the fp16 pattern of
-//     1024, then one fp16 add or FMA); each group accumulates into its own
-//     TMEM slice, folded into fp32 registers with the group's scale:
-//     acc += s * D_g;
+// At decode the layer streams int4 weights from HBM and the tensor-core work
+// per weight is tiny, so the kernel is built around the per-byte cost of
+// turning nibbles into MMA operands:
+//   * the A operand is e4m3: a nibble q zero-extended to a byte is exactly the
+//     e4m3 number q * 2^-9, so one AND (and one shift per 8 codes) makes the
+//     operand; it lives in tensor memory (tcgen05.st), one TMEM lane per
+//     weight row;
+//   * the B operand is the token rows in e4m3 too, each row scaled by a power
+//     of two and split into hi + lo parts that hold a bf16 value exactly (the
+//     gather kernel and this kernel's gate/up epilogue write them); the hi
+//     and lo tiles go through two MMAs into the same accumulator;
+//   * the MMA is tcgen05.mma kind::f8f6f4 (K = 32), A from TMEM;
+//   * each quantisation group (K = 128) accumulates into its own TMEM slice,
+//     folded into fp32 registers with the group's scale s and zero z:
+//         acc += s * (2^9 * D - z * S),
+//     S the group's sum of the (scaled) token row; the token row's scale is
+//     undone at the end (gate/up) or per group (down, where h is scaled per
+//     128-feature block);
+//   * within every 8-element K block the MMA sees the order {0,4,1,5,2,6,3,7}
+//     (the order the nibbles come out of a word); the token rows are stored
+//     in that order;
+//   * one pipeline stage = one quantisation group: the int4 blocks of two
+//     128-row matrices (gate and up of one output tile, or two adjacent down
+//     tiles when d/128 is even), the token tile and the token rows' group
+//     sums (and, for down, their per-group unscale factors), on one barrier;
 //   * the warps that feed the MMAs (unpack) and the warps that consume them
-//     (fold + epilogue) are separate, each running a short per-group chain:
-//     unpack waits for the stage and a free A slot, fold waits for the
-//     group's accumulator; item epilogues never stall the unpacking;
-//   * two MMA warps take alternate groups and issue from a converged warp
-//     (elect.sync): their issue rate, not the tensor core, bounds small-N
-//     MMAs; 3 A slots where tensor memory allows (2 otherwise).
+//     (fold + epilogue) are separate; two MMA warps take alternate groups and
+//     issue from a converged warp (elect.sync).
 //
 //   warp 0       producer (bulk copy + TMA)
 //   warps 1-2    MMA issuers (warp 1 owns TMEM)
 //   warps 3-10   unpack, two per TMEM lane quadrant: in the two-matrix modes
 //                each writes one matrix's codes for its quadrant's rows, in
-//                single down each writes one K quad of each half
-//   warps 11-14  fold + epilogue, one per quadrant: every matrix and token
-//                column of its 32 rows
-// Modes: gate/up (a stage holds the gate and up rows of one output tile;
-// SwiGLU epilogue), paired down (two adjacent 128-row output tiles sharing the
-// token tile), single down (one tile).
+//                single down each writes one K half
+//   warps 11-18  fold + epilogue, two per quadrant: every matrix and half the
+//                token columns of its 32 rows
+// Modes: gate/up (SwiGLU epilogue, h written in the e4m3 form the down GEMM
+// reads), paired down (two output tiles), single down (one tile).
 //
 // Every wait is bounded; on a timeout the CTA drains its copies and MMAs,
 // frees TMEM and returns with MOE_DEVERR_TIMEOUT set.
@@ -47,17 +55,21 @@ using namespace gemm;
 
 namespace {
 
-constexpr int G_NBUF = 4;     // accumulator slices: group g uses slice g % 4
-constexpr int G_MAX_NA = 3;   // A slots in tensor memory (3 where the columns allow)
-constexpr int G_MISC = 8;     // [0] tmem [1] abort [2] items [3] stages issued [4] stays 0
-constexpr int G_NMMA = 2;     // MMA-issuing warps (alternate groups)
-constexpr int G_NUP = 8;      // unpack warps
-constexpr int G_NFOLD = 4;    // fold + epilogue warps
+constexpr int G_MAX_NBUF = 4;   // accumulator slices (fewer where TMEM is short)
+constexpr int G_MAX_NA = 3;     // A slots in tensor memory
+constexpr int G_MISC = 8;       // [0] tmem [1] abort [2] items [3] stages issued [4] stays 0
+constexpr int G_NMMA = 2;       // MMA-issuing warps (alternate groups)
+constexpr int G_NUP = 8;        // unpack warps
+constexpr int G_NFOLD = 8;      // fold + epilogue warps
 constexpr int G_UP0 = 1 + G_NMMA;                  // first unpack warp
 constexpr int G_FOLD0 = G_UP0 + G_NUP;             // first fold warp
 constexpr int G_THREADS = (G_FOLD0 + G_NFOLD) * 32;
 
 enum GroupMode { G_GATEUP = 0, G_DOWN_PAIR = 1, G_DOWN = 2 };
+
+// Where element e (0..7) of an 8-element K block is stored: the MMA sees the
+// block in the order {0,4,1,5,2,6,3,7}.
+__host__ __device__ constexpr int k_slot(int e) { return e < 4 ? 2 * e : 2 * (e - 4) + 1; }
 
 // A work item decoded once per CTA (the decode needs integer divisions by
 // run-time values, which every warp would otherwise repeat).
@@ -69,23 +81,41 @@ struct ItemDesc {
 };
 constexpr int G_ITEM_TAB = 64;   // items per CTA kept in the table; later ones are decoded on the fly
 
+// Per stage the producer also copies the token rows' group sums (and, for
+// down, unscale factors) of the item's rows: a 16-byte-aligned superset of
+// bn + 4 floats each, so the arrays need SUMS_PAD_BYTES of readable slack.
+__host__ __device__ constexpr uint32_t sums_bytes(int bn) { return (uint32_t)(bn + 4) * 4u; }
+
+// Where the row range [r0, r0 + bn) of row `kg` of a [groups][rows_total]
+// float array starts: a 16-byte-aligned address at or below it, and the float
+// offset of r0 from that address.
+__device__ __forceinline__ const float* sums_src(const float* arr, int rows_total, int kg, int r0, int& off) {
+  const float* a = arr + (size_t)kg * rows_total + r0;
+  const uintptr_t u = reinterpret_cast<uintptr_t>(a);
+  off = (int)((u & 15u) >> 2);
+  return reinterpret_cast<const float*>(u & ~(uintptr_t)15);
+}
+
 struct GShared {
   ItemDesc* items;     // [G_ITEM_TAB]
-  uint8_t* b_ring;     // [n_st][2 * bn * 128]  token rows, SW128 K-major (1024-aligned stages)
-  uint8_t* raw_ring;   // [n_st][nmat * I4_MAT_BYTES]  nibbles + scale/zero words
+  uint8_t* b_ring;     // [n_st][2 * bn * 128]  token rows (hi, then lo), SW128 K-major
+  uint8_t* raw_ring;   // [n_st][nmat * I4_MAT_BYTES + 2 * sums_bytes]  nibbles + scale/zero
+                       // words, then the token rows' group sums and unscale factors
+  float* red;          // gate/up epilogue: [2][4][32] per-quadrant partial max / sum
   uint64_t *full, *empty;          // stages: producer -> consumers, consumers -> producer
   uint64_t *a_full, *a_empty;      // A slots: unpack -> MMA, MMA (commit) -> unpack
   uint64_t *acc_full, *acc_empty;  // accumulator slices: MMA (commit) -> fold, fold -> MMA
+  uint64_t* epi;                   // [2] gate/up epilogue hand-offs among the fold warps
   uint64_t* fin;
   int* misc;
   WorkList W;
 };
 
 size_t group_carve_bytes(int nmat, int bn, int n_st, int n_groups) {
-  size_t s = (size_t)n_st * ((size_t)bn * 256 + (size_t)nmat * I4_MAT_BYTES);
-  s += sizeof(ItemDesc) * G_ITEM_TAB;
+  size_t s = (size_t)n_st * ((size_t)bn * 256 + (size_t)nmat * I4_MAT_BYTES + 2 * sums_bytes(bn));
+  s += sizeof(ItemDesc) * G_ITEM_TAB + 2 * 4 * 32 * sizeof(float);
   s = align_up(s, 16);
-  s += 8 * (size_t)(2 * n_st + 2 * G_MAX_NA + 2 * G_NBUF + 1);
+  s += 8 * (size_t)(2 * n_st + 2 * G_MAX_NA + 2 * G_MAX_NBUF + 2 + 1);
   s += 4 * (G_MISC + worklist_ints(n_groups));
   return s;
 }
@@ -112,6 +142,14 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err));
 }
 
+// The 8 nibbles of a word as two registers of e4m3 codes q * 2^-9 (a nibble
+// zero-extended to a byte): K positions {0,4,1,5} and {2,6,3,7} of the word's
+// 8 elements (element 2i sits in bits [4i, 4i+4), 2i+1 in [16+4i, 20+4i)).
+__device__ __forceinline__ void e4m3_codes(uint32_t w, uint32_t& a, uint32_t& b) {
+  a = w & 0x0F0F0F0Fu;
+  b = (w >> 4) & 0x0F0F0F0Fu;
+}
+
 }  // namespace
 
 template <int MODE, int GBN>
@@ -120,12 +158,16 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   constexpr bool GATEUP = MODE == G_GATEUP;
   constexpr bool PAIR = MODE != G_DOWN;                // two 128-row matrices per stage
   constexpr int NMAT = PAIR ? 2 : 1;
-  constexpr uint32_t RAW_STAGE = NMAT * I4_MAT_BYTES;
-  constexpr uint32_t A_COLS = NMAT * (QGROUP / 2);     // TMEM columns of one A slot
-  constexpr uint32_t B_HALF = (uint32_t)GBN * 128u;    // one 64-wide K slice of the token rows
-  constexpr uint32_t B_STAGE = 2u * B_HALF;
-  // A slots: 3 where they fit beside the 4 accumulator slices in 512 columns
-  constexpr int NA = (3 * A_COLS + G_NBUF * NMAT * GBN <= 512) ? 3 : 2;
+  constexpr uint32_t SUMS = sums_bytes(GBN);
+  constexpr uint32_t SUMS_OFF = NMAT * I4_MAT_BYTES;   // group sums, then (down) unscale factors
+  constexpr uint32_t RAW_STAGE = NMAT * I4_MAT_BYTES + 2 * SUMS;
+  constexpr uint32_t A_COLS = NMAT * 32;               // TMEM columns of one A slot (128 e4m3 per row)
+  constexpr uint32_t B_BOX = (uint32_t)GBN * 128u;     // one TMA box: GBN rows x 128 bytes
+  constexpr uint32_t B_STAGE = 2u * B_BOX;             // hi rows, then lo rows
+  constexpr int NBUF = 4;                              // accumulator slices
+  constexpr int NA = 3;                                // A slots
+  constexpr uint32_t SLICE = NMAT * GBN;               // TMEM columns of one accumulator slice
+  static_assert(NA * (int)A_COLS + NBUF * (int)SLICE <= 512, "tensor memory columns");
   const int n_st = p.n_raw;
 
   extern __shared__ uint8_t smem_dyn[];
@@ -137,14 +179,17 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   uint8_t* cur = S.raw_ring + (size_t)n_st * RAW_STAGE;
   S.items = reinterpret_cast<ItemDesc*>(cur);
   cur += sizeof(ItemDesc) * G_ITEM_TAB;
+  S.red = reinterpret_cast<float*>(cur);
+  cur += 2 * 4 * 32 * sizeof(float);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + align_up((size_t)(cur - base), 16));
   S.full = bars;
   S.empty = S.full + n_st;
   S.a_full = S.empty + n_st;
   S.a_empty = S.a_full + G_MAX_NA;
   S.acc_full = S.a_empty + G_MAX_NA;
-  S.acc_empty = S.acc_full + G_NBUF;
-  S.fin = S.acc_empty + G_NBUF;
+  S.acc_empty = S.acc_full + G_MAX_NBUF;
+  S.epi = S.acc_empty + G_MAX_NBUF;
+  S.fin = S.epi + 2;
   S.misc = reinterpret_cast<int*>(S.fin + 1);
   S.W.prefix = S.misc + G_MISC;
   S.W.nch = S.W.prefix + (p.n_groups + 1);
@@ -163,10 +208,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       mbar_init(smem_u32(&S.a_full[i]), G_NUP * 32);
       mbar_init(smem_u32(&S.a_empty[i]), 1);
     }
-    for (int i = 0; i < G_NBUF; ++i) {
+    for (int i = 0; i < G_MAX_NBUF; ++i) {
       mbar_init(smem_u32(&S.acc_full[i]), 1);
       mbar_init(smem_u32(&S.acc_empty[i]), G_NFOLD * 32);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&S.epi[i]), G_NFOLD * 32);
     mbar_init(smem_u32(S.fin), G_NMMA);
     for (int i = 1; i < G_MISC; ++i)
       if (i != 2) S.misc[i] = 0;   // [0] written by tcgen05.alloc, [2] by the first unpack warp
@@ -198,9 +244,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 
   if (warp == 0) {
     // ================================================================ producer
-    // Per group one stage: the NMAT nibble blocks and the two 64-wide K
-    // slices of the token rows, on one barrier.  In the paired down mode the
-    // item's tile index mt names the output tiles 2mt and 2mt + 1.
+    // Per group one stage: the NMAT nibble blocks and the token tile (hi rows
+    // at y = r0, lo rows at y = rows_total + r0), on one barrier.  In the
+    // paired down mode the item's tile index mt names the output tiles 2mt
+    // and 2mt + 1.
     if (lane == 0) {
       Ring rs{0, 0, n_st};
       int issued = 0;
@@ -214,8 +261,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         for (int kg = g0; kg < g1; ++kg) {
           if (!(ok = mbar_wait(smem_u32(&S.empty[rs.i]), rs.ph ^ 1u, abort_flag, p.err))) break;
           const uint32_t bar = smem_u32(&S.full[rs.i]);
-          mbar_arrive_expect_tx(bar, RAW_STAGE + B_STAGE);
+          mbar_arrive_expect_tx(bar, NMAT * I4_MAT_BYTES + (GATEUP ? 1 : 2) * SUMS + B_STAGE);
           const uint32_t raw = smem_u32(S.raw_ring + (size_t)rs.i * RAW_STAGE);
+          int off;
+          bulk_g2s(raw + SUMS_OFF, sums_src(p.b_sum, p.rows_total, kg, it.r0, off), SUMS, bar);
+          if (!GATEUP) bulk_g2s(raw + SUMS_OFF + SUMS, sums_src(p.b_scale, p.rows_total, kg, it.r0, off), SUMS, bar);
           if (MODE == G_DOWN_PAIR) {
 #pragma unroll
             for (int m = 0; m < 2; ++m)
@@ -223,12 +273,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                             sec + ((size_t)(2 * it.mt + m) * (p.K / QGROUP) + kg) * I4_MAT_BYTES,
                             I4_MAT_BYTES, bar, pol);
           } else {
-            bulk_g2s_hint(raw, sec + ((size_t)it.mt * (p.K / QGROUP) + kg) * RAW_STAGE, RAW_STAGE, bar,
-                          pol);
+            bulk_g2s_hint(raw, sec + ((size_t)it.mt * (p.K / QGROUP) + kg) * (NMAT * I4_MAT_BYTES),
+                          NMAT * I4_MAT_BYTES, bar, pol);
           }
           const uint32_t dst = smem_u32(S.b_ring + (size_t)rs.i * B_STAGE);
-          tma_load_2d(dst, &tmap_b, (2 * kg) * KSTEP, it.r0, bar);
-          tma_load_2d(dst + B_HALF, &tmap_b, (2 * kg + 1) * KSTEP, it.r0, bar);
+          tma_load_2d(dst, &tmap_b, kg * QGROUP, it.r0, bar);
+          tma_load_2d(dst + B_BOX, &tmap_b, kg * QGROUP, p.rows_total + it.r0, bar);
           rs.next();
           ++issued;
         }
@@ -238,42 +288,40 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   } else if (warp < G_UP0) {
     // ================================================================ MMA issuers
     // Warp 1 + mw issues the groups with (group counter % 2) == mw.  Group gc
-    // uses A slot gc % NA and accumulator slice gc % 4.  a_full(gc) also
+    // uses A slot gc % NA and accumulator slice gc % NBUF.  a_full(gc) also
     // implies that the group's stage (token tile) has landed: the unpack
     // threads arrive only after seeing it.  The whole warp runs the loop;
     // ring positions advance by one per group, owned or not.
     const int mw = warp - 1;
-    uint32_t gc = 0;
     bool ok = true;
-    Ring rs{0, 0, n_st}, ra{0, 0, NA};
+    Ring rs{0, 0, n_st}, ra{0, 0, NA}, rc{0, 0, NBUF};
     const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(S.b_ring));   // stage 0, K step 0
+    const uint32_t idesc = idesc_f16kind_f32(TILE_M, (uint32_t)GBN, 0u);   // e4m3 x e4m3 -> f32
+    uint32_t gc = 0;
     for (int ii = 0; ii < n_mine && ok; ++ii) {
       const ItemDesc it = get_item(ii, p, S);
       if (!it.slot) continue;
       const int g0 = it.g0, g1 = it.g1;
-      const uint32_t idesc = idesc_f16kind_f32(TILE_M, (uint32_t)((it.n_rows + 15) & ~15), 0u);
-      for (int kg = g0; kg < g1; ++kg, ++gc, rs.next(), ra.next()) {
+      for (int kg = g0; kg < g1; ++kg, ++gc, rs.next(), ra.next(), rc.next()) {
         if ((int)(gc & 1u) != mw) continue;
-        const uint32_t bi = gc % G_NBUF;
         if (!(ok = wait_all(smem_u32(&S.a_full[ra.i]), ra.ph, abort_flag, p.err))) break;
-        if (!(ok = wait_all(smem_u32(&S.acc_empty[bi]), ((gc / G_NBUF) & 1u) ^ 1u, abort_flag, p.err)))
-          break;
+        if (!(ok = wait_all(smem_u32(&S.acc_empty[rc.i]), rc.ph ^ 1u, abort_flag, p.err))) break;
         tc_fence_after();
         // the descriptor's start-address field counts 16-byte units
         const uint64_t bd = bdesc0 + (uint64_t)(((uint32_t)rs.i * B_STAGE) >> 4);
         const uint32_t a_base = tmem_base + (uint32_t)ra.i * A_COLS;
-        const uint32_t d0 = tmem_base + acc0 + bi * (uint32_t)(NMAT * GBN);
+        const uint32_t d0 = tmem_base + acc0 + (uint32_t)rc.i * SLICE;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint64_t bq = bd + (uint64_t)(((q >> 2) * B_HALF + (q & 3) * 32) >> 4);
+        for (int q = 0; q < 8; ++q) {   // K steps of 32: hi tile, then the same steps on the lo tile
+          const uint64_t bq = bd + (uint64_t)(((q >> 2) * B_BOX + (q & 3) * 32) >> 4);
+          const uint32_t ak = a_base + (uint32_t)((q & 3) * 8);
           if (NMAT == 2)
-            mma2_ta_elect(d0, d0 + GBN, a_base + q * 8, a_base + (QGROUP / 2) + q * 8, bq, idesc,
-                          q > 0 ? 1u : 0u);
+            mma2_f8_ta_elect(d0, d0 + GBN, ak, ak + 32, bq, idesc, q > 0 ? 1u : 0u);
           else
-            mma_ta_elect(d0, a_base + q * 8, bq, idesc, q > 0 ? 1u : 0u);
+            mma_f8_ta_elect(d0, ak, bq, idesc, q > 0 ? 1u : 0u);
         }
         mma_commit_elect(smem_u32(&S.a_empty[ra.i]));
-        mma_commit_elect(smem_u32(&S.acc_full[bi]));
+        mma_commit_elect(smem_u32(&S.acc_full[rc.i]));
       }
     }
   } else if (warp < G_FOLD0) {
@@ -285,8 +333,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const int quad = warp & 3;               // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;          // weight row of the tile = TMEM lane
     const int hw = wr >> 2;                  // which of the quadrant's two unpack warps
-    const int m_own = PAIR ? hw : 0;         // matrix ...
-    const int j_own = PAIR ? 0 : hw;         // ... and K quad of each half (single down)
+    const int m_own = PAIR ? hw : 0;         // matrix (two-matrix modes) ...
+    const int h_own = PAIR ? 0 : hw;         // ... or K half (single down)
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
     Ring rs{0, 0, n_st}, ra{0, 0, NA};
     bool ok = true, full_ready = false, a_ready = false;
@@ -299,34 +347,29 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         if (!a_ready && !(ok = wait_all(smem_u32(&S.a_empty[ra.i]), ra.ph ^ 1u, abort_flag, p.err))) break;
         tc_fence_after();
         const uint8_t* mat = S.raw_ring + (size_t)rs.i * RAW_STAGE + m_own * I4_MAT_BYTES;
-        const uint32_t sz = *reinterpret_cast<const uint32_t*>(mat + I4_PACKED_BYTES + r * 4);
-        const float zf = __half2float(__ushort_as_half((unsigned short)(sz >> 16)));
-        const __half2 za = __float2half2_rn(-(1024.f + zf)), zb = __float2half2_rn(-(64.f + zf));
-        const uint32_t nz_a = *reinterpret_cast<const uint32_t*>(&za);
-        const uint32_t nz_b = *reinterpret_cast<const uint32_t*>(&zb);
-        const uint32_t ta = lane_base + (uint32_t)ra.i * A_COLS + (uint32_t)(m_own * (QGROUP / 2));
+        const uint32_t ta = lane_base + (uint32_t)ra.i * A_COLS + (uint32_t)(m_own * 32);
+        if (PAIR) {   // all 128 codes of my row: column h*16 + j*8 + 2w (+1)
+          uint32_t v[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {   // K halves of the group: 64 codes of my row each
-          if (PAIR) {
-            uint32_t v[32];
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-              const uint4 wq = *reinterpret_cast<const uint4*>(mat + ((h * 2 + jj) * TILE_M + r) * 16);
-              codes_minus_zero(wq.x, nz_a, nz_b, &v[jj * 16 + 0]);
-              codes_minus_zero(wq.y, nz_a, nz_b, &v[jj * 16 + 4]);
-              codes_minus_zero(wq.z, nz_a, nz_b, &v[jj * 16 + 8]);
-              codes_minus_zero(wq.w, nz_a, nz_b, &v[jj * 16 + 12]);
-            }
-            tmem_st_32(ta + (uint32_t)(h * 32), v);
-          } else {
-            uint32_t v[16];
-            const uint4 wq = *reinterpret_cast<const uint4*>(mat + ((h * 2 + j_own) * TILE_M + r) * 16);
-            codes_minus_zero(wq.x, nz_a, nz_b, &v[0]);
-            codes_minus_zero(wq.y, nz_a, nz_b, &v[4]);
-            codes_minus_zero(wq.z, nz_a, nz_b, &v[8]);
-            codes_minus_zero(wq.w, nz_a, nz_b, &v[12]);
-            tmem_st_16(ta + (uint32_t)(h * 32 + j_own * 16), v);
+          for (int hj = 0; hj < 4; ++hj) {   // quad (h, j) = (hj >> 1, hj & 1)
+            const uint4 wq = *reinterpret_cast<const uint4*>(mat + (hj * TILE_M + r) * 16);
+            e4m3_codes(wq.x, v[hj * 8 + 0], v[hj * 8 + 1]);
+            e4m3_codes(wq.y, v[hj * 8 + 2], v[hj * 8 + 3]);
+            e4m3_codes(wq.z, v[hj * 8 + 4], v[hj * 8 + 5]);
+            e4m3_codes(wq.w, v[hj * 8 + 6], v[hj * 8 + 7]);
           }
+          tmem_st_32(ta, v);
+        } else {      // my K half: 64 codes of my row
+          uint32_t v[16];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint4 wq = *reinterpret_cast<const uint4*>(mat + ((h_own * 2 + j) * TILE_M + r) * 16);
+            e4m3_codes(wq.x, v[j * 8 + 0], v[j * 8 + 1]);
+            e4m3_codes(wq.y, v[j * 8 + 2], v[j * 8 + 3]);
+            e4m3_codes(wq.z, v[j * 8 + 4], v[j * 8 + 5]);
+            e4m3_codes(wq.w, v[j * 8 + 6], v[j * 8 + 7]);
+          }
+          tmem_st_16(ta + (uint32_t)(h_own * 16), v);
         }
         mbar_arrive(smem_u32(&S.empty[rs.i]));   // my reads of the stage are done
         {   // while the stores drain, test what the next group waits for
@@ -350,75 +393,157 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     // ================================================================ fold + epilogue
     // One warp per TMEM lane quadrant; each thread owns weight row r of every
     // matrix and all the item's token columns.  Group gc: wait for its
-    // accumulator slice, fold it with the group's scales (read from the
-    // stage, which this warp releases afterwards), free the slice.
+    // accumulator slice, fold it with the group's scale and zero (read from
+    // the stage, which this warp releases afterwards) and the token rows'
+    // group sums, free the slice.
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
+    const int c0 = ((warp - G_FOLD0) >> 2) * (GBN / 2);   // my token columns [c0, c0 + GBN/2)
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
-    constexpr int CH = 16;   // columns per tcgen05.ld
-    Ring rs{0, 0, n_st};
-    uint32_t gc = 0;
+    constexpr int CW = GBN / 2;                        // token columns per fold thread
+    constexpr int CH = CW >= 16 ? 16 : 8;              // columns per tcgen05.ld (and per chunk)
+    Ring rs{0, 0, n_st}, rc{0, 0, NBUF};
+    uint32_t it_count = 0;
     bool ok = true;
     for (int ii = 0; ii < n_mine && ok; ++ii) {
       const ItemDesc it = get_item(ii, p, S);
       if (!it.slot) continue;
       const int g0 = it.g0, g1 = it.g1;
-      const int nc = it.n_rows;   // token columns of this item (<= GBN)
-      float acc[NMAT][GBN];
+      const int nc = max(0, min(CW, it.n_rows - c0));   // my token columns of this item
+      float acc[NMAT][CW];
 #pragma unroll
       for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-        for (int i = 0; i < GBN; ++i) acc[m][i] = 0.f;
-      for (int kg = g0; kg < g1 && ok; ++kg, ++gc) {
-        const uint32_t bi = gc % G_NBUF;
+        for (int i = 0; i < CW; ++i) acc[m][i] = 0.f;
+      for (int kg = g0; kg < g1 && ok; ++kg) {
         if (!(ok = wait_all(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err))) break;
         const uint8_t* raw = S.raw_ring + (size_t)rs.i * RAW_STAGE;
-        float sc[NMAT];
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m)
-          sc[m] = __half2float(__ushort_as_half(
-              *reinterpret_cast<const unsigned short*>(raw + m * I4_MAT_BYTES + I4_PACKED_BYTES + r * 4)));
-        if (!(ok = wait_all(smem_u32(&S.acc_full[bi]), (gc / G_NBUF) & 1u, abort_flag, p.err))) break;
-        tc_fence_after();
-        const uint32_t ta = lane_base + acc0 + bi * (uint32_t)(NMAT * GBN);
+        // per matrix: 2^9 s (the codes are q 2^-9) and s z
+        float s9[NMAT], sz[NMAT];
 #pragma unroll
         for (int m = 0; m < NMAT; ++m) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(raw + m * I4_MAT_BYTES + I4_PACKED_BYTES + r * 4);
+          const float sc = __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+          s9[m] = 512.f * sc;
+          sz[m] = sc * __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+        }
+        int off;
+        sums_src(p.b_sum, p.rows_total, kg, it.r0, off);
+        const float* bsum = reinterpret_cast<const float*>(raw + SUMS_OFF) + off + c0;
+        const float* bscl = reinterpret_cast<const float*>(raw + SUMS_OFF + SUMS) + off + c0;
+        if (!(ok = wait_all(smem_u32(&S.acc_full[rc.i]), rc.ph, abort_flag, p.err))) break;
+        tc_fence_after();
+        const uint32_t ta = lane_base + acc0 + (uint32_t)rc.i * SLICE;
 #pragma unroll
-          for (int ch = 0; ch < GBN / CH; ++ch) {
-            if (ch * CH < nc) {
-              uint32_t d[CH];
-              tmem_ld_16(ta + (uint32_t)(m * GBN + ch * CH), d);
-              tmem_ld_wait_regs(d);
+        for (int ch = 0; ch < CW / CH; ++ch) {
+          if (ch * CH < nc) {
+            uint32_t dv[NMAT][CH];
 #pragma unroll
-              for (int i = 0; i < CH; ++i)
-                acc[m][ch * CH + i] = fmaf(sc[m], __uint_as_float(d[i]), acc[m][ch * CH + i]);
+            for (int m = 0; m < NMAT; ++m) {
+              if (CH == 16) tmem_ld_16(ta + (uint32_t)(m * GBN + c0 + ch * CH), *reinterpret_cast<uint32_t(*)[16]>(dv[m]));
+              else tmem_ld_8(ta + (uint32_t)(m * GBN + c0 + ch * CH), *reinterpret_cast<uint32_t(*)[8]>(dv[m]));
+            }
+            // token factors (shared by the matrices) while the loads are in flight
+            float bs[CH], bu[CH];
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+              const float u = GATEUP ? 1.f : bscl[ch * CH + i];
+              bu[i] = u;
+              bs[i] = u * bsum[ch * CH + i];
+            }
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) {
+              tmem_ld_wait_regs(dv[m]);
+#pragma unroll
+              for (int i = 0; i < CH; ++i) {
+                const int n = ch * CH + i;
+                const float sd = GATEUP ? s9[m] : s9[m] * bu[i];
+                acc[m][n] = fmaf(sd, __uint_as_float(dv[m][i]), fmaf(-sz[m], bs[i], acc[m][n]));
+              }
             }
           }
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&S.acc_empty[bi]));
+        mbar_arrive(smem_u32(&S.acc_empty[rc.i]));
         mbar_arrive(smem_u32(&S.empty[rs.i]));
         rs.next();
+        rc.next();
       }
       if (!ok) break;
 
       // ---- item epilogue from the register accumulators
       if (GATEUP) {
-        __half* hout = reinterpret_cast<__half*>(p.out);
-        const int f = it.mt * TILE_M + r;
+        // h = silu(gate) * up for my feature row, then its e4m3 hi/lo form for
+        // the down GEMM: per token, a power-of-two scale from the largest |h|
+        // over the tile's 128 features, the two bytes, and the sum of hi + lo
+        // over the 128 features.  The four fold warps combine their partial
+        // maxima and sums through shared memory (bounded mbarrier hand-offs).
+        const uint32_t par = it_count & 1u;
+        float hv[CW];
+        const float* ue = p.b_scale + it.r0 + c0;   // the token rows' unscale factors
 #pragma unroll
-        for (int i = 0; i < GBN; ++i)
-          if (i < nc) hout[(size_t)(it.r0 + i) * p.out_ld + f] = to_half_sat(silu_f(acc[0][i]) * acc[1][i]);
+        for (int i = 0; i < CW; ++i) {
+          hv[i] = 0.f;
+          if (i < nc) {
+            const float u = __ldg(ue + i);
+            hv[i] = silu_f(acc[0][i] * u) * (acc[1][i] * u);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+          float m = fabsf(hv[i]);
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+          if (lane == i) S.red[quad * 32 + c0 + i] = m;
+        }
+        mbar_arrive(smem_u32(&S.epi[0]));
+        if (!(ok = wait_all(smem_u32(&S.epi[0]), par, abort_flag, p.err))) break;
+        uint8_t* hq = p.q_out;
+        const int f = it.mt * TILE_M + (r & ~7) + k_slot(r & 7);   // stored position of my feature
+        float ssum[CW];
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+          ssum[i] = 0.f;
+          if (i < nc) {
+            const int t = c0 + i;   // token column
+            const float am = fmaxf(fmaxf(S.red[t], S.red[32 + t]), fmaxf(S.red[64 + t], S.red[96 + t]));
+            int ex = 0;
+            if (am > 0.f) frexpf(am, &ex);
+            const int e = max(-126, min(127, am > 0.f ? 8 - ex : 0));
+            const float x = hv[i] * __int_as_float((127 + e) << 23);
+            const uint16_t hb = f32x2_to_e4m3x2(x, 0.f);
+            const float hf = e4m3x2_to_f32x2(hb).x;
+            const uint16_t lb = f32x2_to_e4m3x2(x - hf, 0.f);
+            ssum[i] = hf + e4m3x2_to_f32x2(lb).x;
+            hq[(size_t)(it.r0 + t) * p.out_ld + f] = (uint8_t)(hb & 0xFFu);
+            hq[(size_t)(p.rows_total + it.r0 + t) * p.out_ld + f] = (uint8_t)(lb & 0xFFu);
+            if (quad == 0 && lane == i)
+              p.scale_out[(size_t)it.mt * p.rows_total + it.r0 + t] = __int_as_float((127 - e) << 23);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+          float v = ssum[i];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+          if (lane == i) S.red[128 + quad * 32 + c0 + i] = v;
+        }
+        mbar_arrive(smem_u32(&S.epi[1]));
+        if (!(ok = wait_all(smem_u32(&S.epi[1]), par, abort_flag, p.err))) break;
+        if (quad == 0 && lane < nc)
+          p.sum_out[(size_t)it.mt * p.rows_total + it.r0 + c0 + lane] =
+              S.red[128 + c0 + lane] + S.red[160 + c0 + lane] + S.red[192 + c0 + lane] + S.red[224 + c0 + lane];
       } else {
         float* y = reinterpret_cast<float*>(p.out) + (size_t)it.ks * p.out_split_stride;
 #pragma unroll
         for (int m = 0; m < NMAT; ++m) {
           const int f = (MODE == G_DOWN_PAIR ? 2 * it.mt + m : it.mt) * TILE_M + r;
 #pragma unroll
-          for (int i = 0; i < GBN; ++i)
-            if (i < nc) y[(size_t)(it.r0 + i) * p.out_ld + f] = acc[m][i];
+          for (int i = 0; i < CW; ++i)
+            if (i < nc) y[(size_t)(it.r0 + c0 + i) * p.out_ld + f] = acc[m][i];
         }
       }
+      ++it_count;
     }
   }
 
@@ -457,14 +582,10 @@ GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups, int n_mt) {
   pl.n_raw = n_st;   // stages (nibbles + token rows)
   pl.n_b = n_st;
   pl.smem_bytes = group_carve_bytes(nmat, bn, n_st, n_groups) + 1024;
-  // A slots: 3 where they fit beside the 4 accumulator slices in 512 columns
-  // (the kernel derives the same number from its template arguments)
-  const uint32_t acc_cols = (uint32_t)(G_NBUF * nmat * bn);
-  pl.n_a = (uint32_t)(3 * nmat * (QGROUP / 2)) + acc_cols <= 512u ? 3 : 2;
-  const uint32_t need = (uint32_t)(pl.n_a * nmat * (QGROUP / 2)) + acc_cols;
-  uint32_t cols = 32;
-  while (cols < need) cols <<= 1;
-  pl.tmem_cols = cols;
+  // the kernel derives its A slot and accumulator slice counts from its
+  // template arguments so that they fit 512 columns
+  pl.n_a = G_MAX_NA;
+  pl.tmem_cols = 512;
   return pl;
 }
 

@@ -28,6 +28,10 @@ constexpr int QGROUP = 128;          // int4 quantisation group
 constexpr int BF16_TILE_BYTES = TILE_M * KSTEP * 2;          // 16384
 constexpr int I4_PACKED_BYTES = TILE_M * QGROUP / 2;         // 8192
 constexpr int I4_MAT_BYTES = I4_PACKED_BYTES + TILE_M * 4;   // 8704
+// Readable bytes that must follow a [groups][rows] float array the int4
+// decode GEMM reads per stage (group sums, unscale factors): it copies each
+// item's row range as a 16-byte-aligned superset of bn + 4 floats.
+constexpr int SUMS_PAD_BYTES = 256;
 
 __host__ __device__ inline size_t gateup_section_bytes(int fmt, int d, int F) {
   return fmt == MOE_W_INT4_G128
@@ -65,6 +69,16 @@ struct GemmArgs {
   int out_ld;                           // elements per output row
   unsigned long long out_split_stride;  // elements between K-split partial buffers
   int* err;                             // device error word
+  // int4 decode GEMM (e4m3 B operand, see gemm_group.cu): per (group, row) sums
+  // of the B rows [K/128][rows_total]; the rows' unscale factors (gate/up:
+  // [rows_total]; down: per (group, row) [K/128][rows_total]); and, for
+  // gate/up, where h goes in the same form: bytes [2*rows_total][out_ld],
+  // sums and unscale factors [out_ld/128][rows_total].
+  const float* b_sum;
+  const float* b_scale;
+  uint8_t* q_out;
+  float* sum_out;
+  float* scale_out;
   int n_a, n_b, n_raw;                  // pipeline depths
   uint32_t tmem_cols;                   // TMEM columns (power of two >= 32)
 };
@@ -137,6 +151,11 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
                                int d, uint16_t* x_perm, bool to_fp16, int n_sm, cudaStream_t s,
                                bool pdl = false);
+// The int4 decode GEMM's e4m3 form of the gathered rows (see permute.cu):
+// xq [2*rows][d] bytes (hi rows, then lo rows), xs [d/128][rows], xe [rows].
+cudaError_t launch_gather_rows_fp8(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
+                                   int d, uint8_t* xq, float* xs, float* xe, int n_sm, cudaStream_t s,
+                                   bool pdl = false);
 cudaError_t launch_combine_partials(const float* part, int n_split, size_t split_stride,
                                     const int32_t* row_of_assign, const float* topk_w, int T,
                                     int k, int d, int shared_row0, uint16_t* out, cudaStream_t s,

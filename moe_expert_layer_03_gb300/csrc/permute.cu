@@ -176,6 +176,85 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Same gather for the int4 decode GEMM, whose B operand is e4m3: each row r
+// is scaled by a power of two 2^e_r (its largest magnitude lands in
+// [128, 256)) and split into hi = e4m3(x 2^e) and lo = e4m3(x 2^e - hi),
+// which together hold a bf16 value exactly.  Within every 8-element block the
+// elements are stored in the order {0,4,1,5,2,6,3,7}, the K order in which
+// the GEMM unpacks the weight nibbles.  Writes xq [2*rows][d] (hi rows, then
+// lo rows), xs [d/128][rows] (per-group sums of hi + lo) and xe [rows] (2^-e).
+__global__ void __launch_bounds__(256)
+    gather_rows_fp8_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ token_of_row,
+                           int rows, int T, int d, uint8_t* __restrict__ xq, float* __restrict__ xs,
+                           float* __restrict__ xe) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int nvec = d / 8;   // 8-element blocks per row (a multiple of 16)
+  for (int r = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); r < rows;
+       r += (int)((gridDim.x * blockDim.x) >> 5)) {
+    const int t = token_of_row != nullptr ? token_of_row[r] : r;
+    const bool valid = (t >= 0 && t < T);
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(valid ? t : 0) * d);
+    float m = 0.f;
+    if (valid)
+      for (int i = lane; i < nvec; i += 32) {
+        const uint4 v = __ldg(src + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+      }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    int ex = 0;
+    if (m > 0.f) frexpf(m, &ex);               // m = f * 2^ex, f in [0.5, 1)
+    int sc = m > 0.f ? 8 - ex : 0;             // m * 2^sc in [128, 256)
+    sc = max(-126, min(127, sc));
+    const float mul = __int_as_float((127 + sc) << 23);
+    const float inv = __int_as_float((127 - sc) << 23);
+    uint8_t* hi_row = xq + (size_t)r * d;
+    uint8_t* lo_row = xq + ((size_t)rows + r) * d;
+    for (int base = 0; base < nvec; base += 32) {   // every lane runs every iteration
+      const int i = base + lane;
+      const bool act = i < nvec;   // nvec % 16 == 0: whole half-warps
+      float sum = 0.f;
+      if (act) {
+        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (valid) {
+          const uint4 v = __ldg(src + i);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            f[2 * j] = __uint_as_float(w[j] << 16) * mul;
+            f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u) * mul;
+          }
+        }
+        // element order within the block: {0,4,1,5,2,6,3,7}
+        constexpr int PERM[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+        uint32_t hw[2] = {0u, 0u}, lw[2] = {0u, 0u};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float a = f[PERM[2 * q]], b = f[PERM[2 * q + 1]];
+          const uint16_t h = f32x2_to_e4m3x2(a, b);
+          const float2 hf = e4m3x2_to_f32x2(h);
+          const uint16_t l = f32x2_to_e4m3x2(a - hf.x, b - hf.y);
+          const float2 lf = e4m3x2_to_f32x2(l);
+          sum += (hf.x + lf.x) + (hf.y + lf.y);
+          hw[q >> 1] |= (uint32_t)h << (16 * (q & 1));
+          lw[q >> 1] |= (uint32_t)l << (16 * (q & 1));
+        }
+        *reinterpret_cast<uint2*>(hi_row + (size_t)i * 8) = make_uint2(hw[0], hw[1]);
+        *reinterpret_cast<uint2*>(lo_row + (size_t)i * 8) = make_uint2(lw[0], lw[1]);
+      }
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if (act && (lane & 15) == 0) xs[(size_t)(i >> 4) * rows + r] = sum;
+    }
+    if (lane == 0) xe[r] = inv;
+  }
+}
+
 cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_shared,
                                  int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
                                  int32_t* token_of_row, int* err, cudaStream_t s, bool pdl) {
@@ -197,6 +276,16 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, i
 }
 
 __global__ void clear_word_kernel(int* p) { *p = 0; }
+cudaError_t launch_gather_rows_fp8(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
+                                   int d, uint8_t* xq, float* xs, float* xe, int n_sm, cudaStream_t s,
+                                   bool pdl) {
+  if (rows <= 0) return cudaSuccess;
+  int blocks = (rows + 7) / 8;   // 8 warps (rows) per block
+  if (blocks > 4 * n_sm) blocks = 4 * n_sm;
+  return launch_kernel(gather_rows_fp8_kernel, dim3(blocks), dim3(256), 0, s, pdl, x, token_of_row, rows,
+                       T, d, xq, xs, xe);
+}
+
 cudaError_t launch_clear_word(int* p, cudaStream_t s) {
   clear_word_kernel<<<1, 1, 0, s>>>(p);
   return cudaGetLastError();

@@ -264,6 +264,29 @@ MOE_DEV void mma_ss_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint3
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// kind::f8f6f4 (K = 32 per instruction), A from TMEM, issued from a converged
+// warp; A and B are e4m3 here.
+MOE_DEV void mma_f8_ta_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+MOE_DEV void mma2_f8_ta_elect(uint32_t d0, uint32_t d1, uint32_t a0, uint32_t a1, uint64_t bdesc,
+                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%2], %4, %5, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%1], [%3], %4, %5, p;\n\t}" ::"r"(d0),
+      "r"(d1), "r"(a0), "r"(a1), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives once on `bar` when every tcgen05 op this thread issued so far is done.
 MOE_DEV void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -333,6 +356,21 @@ MOE_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: 
 // Barrier among a subset of the CTA's warps (id 1..15; nthreads a multiple of 32).
 MOE_DEV void named_barrier(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------------------ fp8 (e4m3) conversion
+// Two fp32 -> a packed e4m3 pair (round to nearest even, saturating): `lo`
+// goes to the low byte, `hi` to the high byte.
+MOE_DEV uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// A packed e4m3 pair -> the two values as fp32 (exact), low byte first.
+MOE_DEV float2 e4m3x2_to_f32x2(uint16_t v) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
 // ------------------------------------------------------------------ misc
