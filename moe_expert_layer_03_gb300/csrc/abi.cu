@@ -122,16 +122,17 @@ int choose_ksplit(int A, int E, bool has_shared, int bn, int fmt, int d, int F) 
 }
 
 // The int4 decode GEMMs' e4m3 operands (see gemm_group.cu): the gathered rows
-// and h as hi/lo byte rows [2*rows][K], per (group, row) sums [K/128][rows]
-// and unscale factors ([rows] for x, [F/128][rows] for h).
+// and h as hi/lo byte rows [2*rows][K]; for x per (group, row) sums
+// [d/128][rows] and per-row unscale factors [rows]; for h per (group, row)
+// (sum, unscale factor) pairs [F/128][rows][2].
 struct Fp8Rows {
   uint8_t* xq;
   float *xs, *xe;
   uint8_t* hq;
-  float *hs, *he;
+  float* hs;
 };
 struct Fp8Offsets {
-  size_t xq, xs, xe, hq, hs, he;
+  size_t xq, xs, xe, hq, hs;
 };
 // Appends the e4m3 regions at offset o (1 KB aligned) and returns the new end.
 size_t fp8_regions(Fp8Offsets& f, size_t o, int rows, int d, int F) {
@@ -139,13 +140,11 @@ size_t fp8_regions(Fp8Offsets& f, size_t o, int rows, int d, int F) {
   f.xs = o;  o = up1k(o + (size_t)(d / QGROUP) * rows * 4 + SUMS_PAD_BYTES);
   f.xe = o;  o = up1k(o + (size_t)rows * 4);
   f.hq = o;  o = up1k(o + 2 * (size_t)rows * F);
-  f.hs = o;  o = up1k(o + (size_t)(F / QGROUP) * rows * 4 + SUMS_PAD_BYTES);
-  f.he = o;  o = up1k(o + (size_t)(F / QGROUP) * rows * 4 + SUMS_PAD_BYTES);
+  f.hs = o;  o = up1k(o + (size_t)(F / QGROUP) * rows * 8 + SUMS_PAD_BYTES);
   return o;
 }
 Fp8Rows fp8_rows(uint8_t* W, const Fp8Offsets& f) {
-  return Fp8Rows{W + f.xq, (float*)(W + f.xs), (float*)(W + f.xe),
-                 W + f.hq, (float*)(W + f.hs), (float*)(W + f.he)};
+  return Fp8Rows{W + f.xq, (float*)(W + f.xs), (float*)(W + f.xe), W + f.hq, (float*)(W + f.hs)};
 }
 
 struct LayerLayout {
@@ -242,7 +241,6 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
     g.b_scale = f8->xe;
     g.q_out = f8->hq;
     g.sum_out = f8->hs;
-    g.scale_out = f8->he;
   }
   if (launch_grouped_gemm(fmt, true, mx, g, plan_gemm(fmt, true, bn, n_groups, F / TILE_M), grid, s,
                           pdl) != cudaSuccess)
@@ -259,7 +257,6 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
   dn.out_split_stride = (unsigned long long)rows * d;
   if (f8) {
     dn.b_sum = f8->hs;
-    dn.b_scale = f8->he;
   }
   if (launch_grouped_gemm(fmt, false, mh, dn, plan_gemm(fmt, false, bn, n_groups, d / TILE_M), grid, s,
                           pdl && !ev_mid) != cudaSuccess)

@@ -30,7 +30,7 @@
 //   * one pipeline stage = one quantisation group: the int4 blocks of two
 //     128-row matrices (gate and up of one output tile, or two adjacent down
 //     tiles when d/128 is even), the token tile and the token rows' group
-//     sums (and, for down, their per-group unscale factors), on one barrier;
+//     sums (for down: (sum, unscale factor) pairs), on one barrier;
 //   * the warps that feed the MMAs (unpack) and the warps that consume them
 //     (fold + epilogue) are separate; two MMA warps take alternate groups and
 //     issue from a converged warp (elect.sync).
@@ -81,26 +81,30 @@ struct ItemDesc {
 };
 constexpr int G_ITEM_TAB = 64;   // items per CTA kept in the table; later ones are decoded on the fly
 
-// Per stage the producer also copies the token rows' group sums (and, for
-// down, unscale factors) of the item's rows: a 16-byte-aligned superset of
-// bn + 4 floats each, so the arrays need SUMS_PAD_BYTES of readable slack.
-__host__ __device__ constexpr uint32_t sums_bytes(int bn) { return (uint32_t)(bn + 4) * 4u; }
+// Per stage the producer also copies the item rows' entries of the token
+// rows' per-group array: floats (the group sums of x, [groups][rows_total])
+// for gate/up, (sum, unscale factor) pairs ([groups][rows_total][2], for h)
+// for down; a 16-byte-aligned superset of the row range, so the arrays need
+// SUMS_PAD_BYTES of readable slack.
+__host__ __device__ constexpr uint32_t sums_bytes(int bn, bool pairs) {
+  return pairs ? (uint32_t)(bn + 2) * 8u : (uint32_t)(bn + 4) * 4u;
+}
 
-// Where the row range [r0, r0 + bn) of row `kg` of a [groups][rows_total]
-// float array starts: a 16-byte-aligned address at or below it, and the float
-// offset of r0 from that address.
-__device__ __forceinline__ const float* sums_src(const float* arr, int rows_total, int kg, int r0, int& off) {
-  const float* a = arr + (size_t)kg * rows_total + r0;
-  const uintptr_t u = reinterpret_cast<uintptr_t>(a);
-  off = (int)((u & 15u) >> 2);
-  return reinterpret_cast<const float*>(u & ~(uintptr_t)15);
+// Where the entries [r0, r0 + bn) of row `kg` of a [groups][rows_total] array
+// of `esz`-byte entries start: a 16-byte-aligned address at or below them, and
+// r0's entry offset from that address.
+__device__ __forceinline__ const void* sums_src(const float* arr, int esz, int rows_total, int kg, int r0,
+                                                int& off) {
+  const uintptr_t u = reinterpret_cast<uintptr_t>(arr) + ((size_t)kg * rows_total + r0) * esz;
+  off = (int)((u & 15u) / (uintptr_t)esz);
+  return reinterpret_cast<const void*>(u & ~(uintptr_t)15);
 }
 
 struct GShared {
   ItemDesc* items;     // [G_ITEM_TAB]
   uint8_t* b_ring;     // [n_st][2 * bn * 128]  token rows (hi, then lo), SW128 K-major
-  uint8_t* raw_ring;   // [n_st][nmat * I4_MAT_BYTES + 2 * sums_bytes]  nibbles + scale/zero
-                       // words, then the token rows' group sums and unscale factors
+  uint8_t* raw_ring;   // [n_st][nmat * I4_MAT_BYTES + sums_bytes]  nibbles + scale/zero
+                       // words, then the token rows' group sums (and unscale factors)
   float* red;          // gate/up epilogue: [2][4][32] per-quadrant partial max / sum
   uint64_t *full, *empty;          // stages: producer -> consumers, consumers -> producer
   uint64_t *a_full, *a_empty;      // A slots: unpack -> MMA, MMA (commit) -> unpack
@@ -112,7 +116,7 @@ struct GShared {
 };
 
 size_t group_carve_bytes(int nmat, int bn, int n_st, int n_groups) {
-  size_t s = (size_t)n_st * ((size_t)bn * 256 + (size_t)nmat * I4_MAT_BYTES + 2 * sums_bytes(bn));
+  size_t s = (size_t)n_st * ((size_t)bn * 256 + (size_t)nmat * I4_MAT_BYTES + sums_bytes(bn, true));
   s += sizeof(ItemDesc) * G_ITEM_TAB + 2 * 4 * 32 * sizeof(float);
   s = align_up(s, 16);
   s += 8 * (size_t)(2 * n_st + 2 * G_MAX_NA + 2 * G_MAX_NBUF + 2 + 1);
@@ -158,9 +162,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   constexpr bool GATEUP = MODE == G_GATEUP;
   constexpr bool PAIR = MODE != G_DOWN;                // two 128-row matrices per stage
   constexpr int NMAT = PAIR ? 2 : 1;
-  constexpr uint32_t SUMS = sums_bytes(GBN);
-  constexpr uint32_t SUMS_OFF = NMAT * I4_MAT_BYTES;   // group sums, then (down) unscale factors
-  constexpr uint32_t RAW_STAGE = NMAT * I4_MAT_BYTES + 2 * SUMS;
+  constexpr int ESZ = GATEUP ? 4 : 8;                  // bytes per token entry of the per-group array
+  constexpr uint32_t SUMS = sums_bytes(GBN, !GATEUP);
+  constexpr uint32_t SUMS_OFF = NMAT * I4_MAT_BYTES;   // the token rows' per-group entries
+  constexpr uint32_t RAW_STAGE = NMAT * I4_MAT_BYTES + SUMS;
   constexpr uint32_t A_COLS = NMAT * 32;               // TMEM columns of one A slot (128 e4m3 per row)
   constexpr uint32_t B_BOX = (uint32_t)GBN * 128u;     // one TMA box: GBN rows x 128 bytes
   constexpr uint32_t B_STAGE = 2u * B_BOX;             // hi rows, then lo rows
@@ -261,11 +266,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         for (int kg = g0; kg < g1; ++kg) {
           if (!(ok = mbar_wait(smem_u32(&S.empty[rs.i]), rs.ph ^ 1u, abort_flag, p.err))) break;
           const uint32_t bar = smem_u32(&S.full[rs.i]);
-          mbar_arrive_expect_tx(bar, NMAT * I4_MAT_BYTES + (GATEUP ? 1 : 2) * SUMS + B_STAGE);
+          mbar_arrive_expect_tx(bar, RAW_STAGE + B_STAGE);
           const uint32_t raw = smem_u32(S.raw_ring + (size_t)rs.i * RAW_STAGE);
           int off;
-          bulk_g2s(raw + SUMS_OFF, sums_src(p.b_sum, p.rows_total, kg, it.r0, off), SUMS, bar);
-          if (!GATEUP) bulk_g2s(raw + SUMS_OFF + SUMS, sums_src(p.b_scale, p.rows_total, kg, it.r0, off), SUMS, bar);
+          bulk_g2s(raw + SUMS_OFF, sums_src(p.b_sum, ESZ, p.rows_total, kg, it.r0, off), SUMS, bar);
           if (MODE == G_DOWN_PAIR) {
 #pragma unroll
             for (int m = 0; m < 2; ++m)
@@ -428,9 +432,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           sz[m] = sc * __half2float(__ushort_as_half((unsigned short)(w >> 16)));
         }
         int off;
-        sums_src(p.b_sum, p.rows_total, kg, it.r0, off);
-        const float* bsum = reinterpret_cast<const float*>(raw + SUMS_OFF) + off + c0;
-        const float* bscl = reinterpret_cast<const float*>(raw + SUMS_OFF + SUMS) + off + c0;
+        sums_src(p.b_sum, ESZ, p.rows_total, kg, it.r0, off);
+        // gate/up: sums; down: (sum, unscale) pairs
+        const float* bsum = reinterpret_cast<const float*>(raw + SUMS_OFF) + (off + c0) * (ESZ / 4);
         if (!(ok = wait_all(smem_u32(&S.acc_full[rc.i]), rc.ph, abort_flag, p.err))) break;
         tc_fence_after();
         const uint32_t ta = lane_base + acc0 + (uint32_t)rc.i * SLICE;
@@ -447,9 +451,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             float bs[CH], bu[CH];
 #pragma unroll
             for (int i = 0; i < CH; ++i) {
-              const float u = GATEUP ? 1.f : bscl[ch * CH + i];
+              const float u = GATEUP ? 1.f : bsum[2 * (ch * CH + i) + 1];
               bu[i] = u;
-              bs[i] = u * bsum[ch * CH + i];
+              bs[i] = u * bsum[(ch * CH + i) * (ESZ / 4)];
             }
 #pragma unroll
             for (int m = 0; m < NMAT; ++m) {
@@ -517,8 +521,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             ssum[i] = hf + e4m3x2_to_f32x2(lb).x;
             hq[(size_t)(it.r0 + t) * p.out_ld + f] = (uint8_t)(hb & 0xFFu);
             hq[(size_t)(p.rows_total + it.r0 + t) * p.out_ld + f] = (uint8_t)(lb & 0xFFu);
-            if (quad == 0 && lane == i)
-              p.scale_out[(size_t)it.mt * p.rows_total + it.r0 + t] = __int_as_float((127 - e) << 23);
+            if (quad == 0 && lane == i)   // h's (sum, unscale) pair: the unscale factor
+              p.sum_out[2 * ((size_t)it.mt * p.rows_total + it.r0 + t) + 1] = __int_as_float((127 - e) << 23);
           }
         }
 #pragma unroll
@@ -530,8 +534,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         }
         mbar_arrive(smem_u32(&S.epi[1]));
         if (!(ok = wait_all(smem_u32(&S.epi[1]), par, abort_flag, p.err))) break;
-        if (quad == 0 && lane < nc)
-          p.sum_out[(size_t)it.mt * p.rows_total + it.r0 + c0 + lane] =
+        if (quad == 0 && lane < nc)   // h's (sum, unscale) pair: the sum
+          p.sum_out[2 * ((size_t)it.mt * p.rows_total + it.r0 + c0 + lane)] =
               S.red[128 + c0 + lane] + S.red[160 + c0 + lane] + S.red[192 + c0 + lane] + S.red[224 + c0 + lane];
       } else {
         float* y = reinterpret_cast<float*>(p.out) + (size_t)it.ks * p.out_split_stride;

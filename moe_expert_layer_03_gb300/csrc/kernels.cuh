@@ -30,8 +30,8 @@ constexpr int I4_PACKED_BYTES = TILE_M * QGROUP / 2;         // 8192
 constexpr int I4_MAT_BYTES = I4_PACKED_BYTES + TILE_M * 4;   // 8704
 // Readable bytes that must follow a [groups][rows] float array the int4
 // decode GEMM reads per stage (group sums, unscale factors): it copies each
-// item's row range as a 16-byte-aligned superset of bn + 4 floats.
-constexpr int SUMS_PAD_BYTES = 256;
+// item's row range as a 16-byte-aligned superset (at most 2 (bn + 1) floats past the end).
+constexpr int SUMS_PAD_BYTES = 512;
 
 __host__ __device__ inline size_t gateup_section_bytes(int fmt, int d, int F) {
   return fmt == MOE_W_INT4_G128
@@ -69,16 +69,15 @@ struct GemmArgs {
   int out_ld;                           // elements per output row
   unsigned long long out_split_stride;  // elements between K-split partial buffers
   int* err;                             // device error word
-  // int4 decode GEMM (e4m3 B operand, see gemm_group.cu): per (group, row) sums
-  // of the B rows [K/128][rows_total]; the rows' unscale factors (gate/up:
-  // [rows_total]; down: per (group, row) [K/128][rows_total]); and, for
-  // gate/up, where h goes in the same form: bytes [2*rows_total][out_ld],
-  // sums and unscale factors [out_ld/128][rows_total].
+  // int4 decode GEMM (e4m3 B operand, see gemm_group.cu).  gate/up: per
+  // (group, row) sums of the B rows [K/128][rows_total] and the rows' unscale
+  // factors [rows_total]; where h goes: bytes [2*rows_total][out_ld] and
+  // (sum, unscale factor) pairs [out_ld/128][rows_total][2].  down: b_sum =
+  // those pairs of h.
   const float* b_sum;
   const float* b_scale;
   uint8_t* q_out;
   float* sum_out;
-  float* scale_out;
   int n_a, n_b, n_raw;                  // pipeline depths
   uint32_t tmem_cols;                   // TMEM columns (power of two >= 32)
 };
