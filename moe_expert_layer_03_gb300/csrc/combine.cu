@@ -32,20 +32,43 @@ __device__ __forceinline__ void store_bf16x4(uint16_t* p, float4 v) {
   *reinterpret_cast<uint2*>(p) = u;
 }
 
-// sum over K splits of the fp32 partial sums of row r, columns [c, c+4)
+// sum over K splits of the fp32 partial sums of row r, columns [c, c+4), in
+// split order.  OVERLAP (small batches, latency-bound): the loads of all
+// splits are issued before the first add so their latencies overlap; else a
+// plain loop (large batches are bandwidth-bound and keep more threads busy).
+template <bool OVERLAP>
 __device__ __forceinline__ float4 y_from_partials(const float* part, int n_split,
                                                   size_t split_stride, int r, int d, int c) {
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = 0; i < n_split; ++i) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(part + i * split_stride + (size_t)r * d + c));
-    s.x += v.x;
-    s.y += v.y;
-    s.z += v.z;
-    s.w += v.w;
+  if (!OVERLAP) {
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < n_split; ++i) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(part + i * split_stride + (size_t)r * d + c));
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    }
+    return s;
   }
+  constexpr int MAXS = 8;   // the largest K split (abi.cu)
+  float4 v[MAXS];
+#pragma unroll
+  for (int i = 0; i < MAXS; ++i)
+    if (i < n_split)
+      v[i] = __ldg(reinterpret_cast<const float4*>(part + i * split_stride + (size_t)r * d + c));
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < MAXS; ++i)
+    if (i < n_split) {
+      s.x += v[i].x;
+      s.y += v[i].y;
+      s.z += v[i].z;
+      s.w += v[i].w;
+    }
   return s;
 }
 
+template <bool OVERLAP>
 __global__ void __launch_bounds__(256)
     combine_partials_kernel(const float* __restrict__ part, int n_split, size_t split_stride,
                             const int32_t* __restrict__ row_of_assign,
@@ -61,14 +84,14 @@ __global__ void __launch_bounds__(256)
     const int r = row_of_assign[t * k + j];
     if (r < 0) continue;   // only after an index error
     const float w = topk_w[t * k + j];
-    const float4 y = y_from_partials(part, n_split, split_stride, r, d, c);
+    const float4 y = y_from_partials<OVERLAP>(part, n_split, split_stride, r, d, c);
     acc.x += w * y.x;
     acc.y += w * y.y;
     acc.z += w * y.z;
     acc.w += w * y.w;
   }
   if (shared_row0 >= 0) {
-    const float4 y = y_from_partials(part, n_split, split_stride, shared_row0 + t, d, c);
+    const float4 y = y_from_partials<OVERLAP>(part, n_split, split_stride, shared_row0 + t, d, c);
     acc.x += y.x;
     acc.y += y.y;
     acc.z += y.z;
@@ -113,7 +136,7 @@ __global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restr
   const int r = blockIdx.x;
   const int c = (blockIdx.y * 256 + threadIdx.x) * 4;
   if (c >= d) return;
-  store_bf16x4(y + (size_t)r * d + c, y_from_partials(part, n_split, split_stride, r, d, c));
+  store_bf16x4(y + (size_t)r * d + c, y_from_partials<false>(part, n_split, split_stride, r, d, c));
 }
 
 static dim3 grid_rows(int rows, int d) { return dim3((unsigned)rows, (unsigned)((d + 1023) / 1024)); }
@@ -123,8 +146,11 @@ cudaError_t launch_combine_partials(const float* part, int n_split, size_t split
                                     int k, int d, int shared_row0, uint16_t* out, cudaStream_t s,
                                     bool pdl) {
   if (T <= 0) return cudaSuccess;
-  return launch_kernel(combine_partials_kernel, grid_rows(T, d), dim3(256), 0, s, pdl, part, n_split,
-                       split_stride, row_of_assign, topk_w, k, d, shared_row0, out);
+  if (T <= 256)
+    return launch_kernel(combine_partials_kernel<true>, grid_rows(T, d), dim3(256), 0, s, pdl, part,
+                         n_split, split_stride, row_of_assign, topk_w, k, d, shared_row0, out);
+  return launch_kernel(combine_partials_kernel<false>, grid_rows(T, d), dim3(256), 0, s, pdl, part,
+                       n_split, split_stride, row_of_assign, topk_w, k, d, shared_row0, out);
 }
 
 cudaError_t launch_combine_bf16(const uint16_t* y_perm, const int32_t* row_of_assign,

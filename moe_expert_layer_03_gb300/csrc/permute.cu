@@ -183,22 +183,24 @@ __global__ void __launch_bounds__(256)
 // elements are stored in the order {0,4,1,5,2,6,3,7}, the K order in which
 // the GEMM unpacks the weight nibbles.  Writes xq [2*rows][d] (hi rows, then
 // lo rows), xs [d/128][rows] (per-group sums of hi + lo) and xe [rows] (2^-e).
-__global__ void __launch_bounds__(256)
+// One 128-thread block per row; a half-warp covers one 128-element group.
+constexpr int FP8_GATHER_THREADS = 128;
+__global__ void __launch_bounds__(FP8_GATHER_THREADS)
     gather_rows_fp8_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ token_of_row,
                            int rows, int T, int d, uint8_t* __restrict__ xq, float* __restrict__ xs,
                            float* __restrict__ xe) {
   griddep_wait();
   griddep_launch_dependents();
-  const int lane = threadIdx.x & 31;
+  __shared__ float wmax[FP8_GATHER_THREADS / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nvec = d / 8;   // 8-element blocks per row (a multiple of 16)
-  for (int r = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); r < rows;
-       r += (int)((gridDim.x * blockDim.x) >> 5)) {
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const int t = token_of_row != nullptr ? token_of_row[r] : r;
     const bool valid = (t >= 0 && t < T);
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(valid ? t : 0) * d);
     float m = 0.f;
     if (valid)
-      for (int i = lane; i < nvec; i += 32) {
+      for (int i = threadIdx.x; i < nvec; i += FP8_GATHER_THREADS) {
         const uint4 v = __ldg(src + i);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -207,6 +209,10 @@ __global__ void __launch_bounds__(256)
       }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) wmax[warp] = m;
+    __syncthreads();
+    m = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    __syncthreads();   // wmax is rewritten for the next row
     int ex = 0;
     if (m > 0.f) frexpf(m, &ex);               // m = f * 2^ex, f in [0.5, 1)
     int sc = m > 0.f ? 8 - ex : 0;             // m * 2^sc in [128, 256)
@@ -215,8 +221,8 @@ __global__ void __launch_bounds__(256)
     const float inv = __int_as_float((127 - sc) << 23);
     uint8_t* hi_row = xq + (size_t)r * d;
     uint8_t* lo_row = xq + ((size_t)rows + r) * d;
-    for (int base = 0; base < nvec; base += 32) {   // every lane runs every iteration
-      const int i = base + lane;
+    for (int base = 0; base < nvec; base += FP8_GATHER_THREADS) {   // every thread runs every iteration
+      const int i = base + threadIdx.x;
       const bool act = i < nvec;   // nvec % 16 == 0: whole half-warps
       float sum = 0.f;
       if (act) {
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(256)
       for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
       if (act && (lane & 15) == 0) xs[(size_t)(i >> 4) * rows + r] = sum;
     }
-    if (lane == 0) xe[r] = inv;
+    if (threadIdx.x == 0) xe[r] = inv;
   }
 }
 
@@ -280,10 +286,9 @@ cudaError_t launch_gather_rows_fp8(const uint16_t* x, const int32_t* token_of_ro
                                    int d, uint8_t* xq, float* xs, float* xe, int n_sm, cudaStream_t s,
                                    bool pdl) {
   if (rows <= 0) return cudaSuccess;
-  int blocks = (rows + 7) / 8;   // 8 warps (rows) per block
-  if (blocks > 4 * n_sm) blocks = 4 * n_sm;
-  return launch_kernel(gather_rows_fp8_kernel, dim3(blocks), dim3(256), 0, s, pdl, x, token_of_row, rows,
-                       T, d, xq, xs, xe);
+  const int blocks = rows < 16 * n_sm ? rows : 16 * n_sm;   // one block per row
+  return launch_kernel(gather_rows_fp8_kernel, dim3(blocks), dim3(FP8_GATHER_THREADS), 0, s, pdl, x,
+                       token_of_row, rows, T, d, xq, xs, xe);
 }
 
 cudaError_t launch_clear_word(int* p, cudaStream_t s) {
