@@ -145,6 +145,13 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
 cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_shared,
                                  int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
                                  int32_t* token_of_row, int* err, cudaStream_t s, bool pdl = false);
+// Routing and permutation in one launch (one CTA), for batches of up to
+// FUSED_ROUTE_MAX_T tokens: same outputs as launch_route_topk followed by
+// launch_permute_index.
+constexpr int FUSED_ROUTE_MAX_T = 64;
+cudaError_t launch_route_permute(const float* logits, int T, int k, int E, int t_shared, int32_t* idx,
+                                 float* w, int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
+                                 int32_t* token_of_row, int* err, cudaStream_t s, bool pdl = false);
 // x_perm[r] = x[token_of_row[r]].  to_fp16: write fp16 (saturating) instead of
 // bf16.  token_of_row == nullptr: x_perm[r] = x[r].
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,

@@ -11,10 +11,14 @@
 //      count table gives each warp its base.  The row of assignment a is
 //      offsets[e] + (number of earlier assignments with expert e) -- unique, so
 //      the result is independent of scheduling.
+// route_permute_kernel (batches of up to FUSED_ROUTE_MAX_T tokens): the top-k
+//   gating of every token (a warp per token, route_dev.cuh), then the same
+//   three steps, in one CTA and one launch.
 // gather_rows_kernel: x_perm[r] = x[token_of_row[r]], one warp per row, 16-byte
 //   vector loads and stores.
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "route_dev.cuh"
 
 namespace moe {
 
@@ -22,13 +26,12 @@ constexpr int PERM_THREADS = 1024;
 constexpr int PERM_WARPS = PERM_THREADS / 32;
 constexpr int PERM_MAX_E = 256;
 
-__global__ void __launch_bounds__(PERM_THREADS, 1)
-    permute_index_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int t_shared,
-                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                         int32_t* __restrict__ row_of_assign, int32_t* __restrict__ token_of_row,
-                         int* __restrict__ err) {
-  griddep_wait();
-  griddep_launch_dependents();
+// histogram, scan and stable scatter of the A = T*k expert ids, by one CTA of
+// PERM_THREADS threads (which all call it)
+__device__ __forceinline__ void permute_cta(const int32_t* __restrict__ idx, int T, int k, int E, int t_shared,
+                                            int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                            int32_t* __restrict__ row_of_assign,
+                                            int32_t* __restrict__ token_of_row, int* __restrict__ err) {
   __shared__ int s_cnt[PERM_MAX_E];
   __shared__ int s_base[PERM_MAX_E];
   __shared__ int s_wc[PERM_WARPS][PERM_MAX_E];
@@ -116,6 +119,30 @@ __global__ void __launch_bounds__(PERM_THREADS, 1)
   }
   // rows of the always-on shared expert follow the routed rows, in token order
   for (int t = tid; t < t_shared; t += PERM_THREADS) token_of_row[s_total + t] = t;
+}
+
+__global__ void __launch_bounds__(PERM_THREADS, 1)
+    permute_index_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int t_shared,
+                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                         int32_t* __restrict__ row_of_assign, int32_t* __restrict__ token_of_row,
+                         int* __restrict__ err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  permute_cta(idx, T, k, E, t_shared, counts, offsets, row_of_assign, token_of_row, err);
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(PERM_THREADS, 1)
+    route_permute_kernel(const float* __restrict__ logits, int T, int k, int E, int t_shared,
+                         int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ counts,
+                         int32_t* __restrict__ offsets, int32_t* __restrict__ row_of_assign,
+                         int32_t* __restrict__ token_of_row, int* __restrict__ err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  for (int tok = threadIdx.x >> 5; tok < T; tok += PERM_WARPS)
+    route_one_token<VPL>(logits, tok, E, k, idx, w, threadIdx.x & 31);
+  __syncthreads();   // the block's global writes of idx are visible to it after the barrier
+  permute_cta(idx, T, k, E, t_shared, counts, offsets, row_of_assign, token_of_row, err);
 }
 
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
@@ -266,6 +293,23 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_
                                  int32_t* token_of_row, int* err, cudaStream_t s, bool pdl) {
   return launch_kernel(permute_index_kernel, dim3(1), dim3(PERM_THREADS), 0, s, pdl, idx, T, k, E,
                        t_shared, counts, offsets, row_of_assign, token_of_row, err);
+}
+
+cudaError_t launch_route_permute(const float* logits, int T, int k, int E, int t_shared, int32_t* idx,
+                                 float* w, int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
+                                 int32_t* token_of_row, int* err, cudaStream_t s, bool pdl) {
+  const dim3 g(1), b(PERM_THREADS);
+  if (E <= 32)
+    return launch_kernel(route_permute_kernel<1>, g, b, 0, s, pdl, logits, T, k, E, t_shared, idx, w,
+                         counts, offsets, row_of_assign, token_of_row, err);
+  if (E <= 64)
+    return launch_kernel(route_permute_kernel<2>, g, b, 0, s, pdl, logits, T, k, E, t_shared, idx, w,
+                         counts, offsets, row_of_assign, token_of_row, err);
+  if (E <= 128)
+    return launch_kernel(route_permute_kernel<4>, g, b, 0, s, pdl, logits, T, k, E, t_shared, idx, w,
+                         counts, offsets, row_of_assign, token_of_row, err);
+  return launch_kernel(route_permute_kernel<8>, g, b, 0, s, pdl, logits, T, k, E, t_shared, idx, w,
+                       counts, offsets, row_of_assign, token_of_row, err);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
