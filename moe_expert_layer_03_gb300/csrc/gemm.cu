@@ -192,16 +192,12 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
             const uint32_t bar = smem_u32(&S.raw_full[rr.i]);
             mbar_arrive_expect_tx(bar, RAW_STAGE);
             const uint32_t raw = smem_u32(S.raw_ring + (size_t)rr.i * RAW_STAGE);
-            if (PAIR) {
-#pragma unroll
-              for (int m = 0; m < 2; ++m)
-                bulk_g2s_hint(raw + m * I4_MAT_BYTES,
-                              sec + ((size_t)(2 * it.mt + m) * (p.K / QGROUP) + kg) * I4_MAT_BYTES,
-                              I4_MAT_BYTES, bar, pol);
-            } else {
-              bulk_g2s_hint(raw, sec + ((size_t)it.mt * (p.K / QGROUP) + kg) * RAW_STAGE, RAW_STAGE, bar,
-                            pol);
-            }
+            // gate/up: gate and up blocks of (mt, kg); down: tile mt's block, or
+            // both blocks of the pair it.mt, contiguous in the down section
+            const size_t off = GATEUP ? ((size_t)it.mt * (p.K / QGROUP) + kg) * RAW_STAGE
+                               : PAIR ? ((size_t)it.mt * (p.K / QGROUP) + kg) * RAW_STAGE
+                                      : i4_down_block(it.mt, kg, p.K / QGROUP, p.n_mt);
+            bulk_g2s_hint(raw, sec + off, RAW_STAGE, bar, pol);
             rr.next();
             ++issued_raw;
           }

@@ -270,16 +270,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           const uint32_t raw = smem_u32(S.raw_ring + (size_t)rs.i * RAW_STAGE);
           int off;
           bulk_g2s(raw + SUMS_OFF, sums_src(p.b_sum, ESZ, p.rows_total, kg, it.r0, off), SUMS, bar);
-          if (MODE == G_DOWN_PAIR) {
-#pragma unroll
-            for (int m = 0; m < 2; ++m)
-              bulk_g2s_hint(raw + m * I4_MAT_BYTES,
-                            sec + ((size_t)(2 * it.mt + m) * (p.K / QGROUP) + kg) * I4_MAT_BYTES,
-                            I4_MAT_BYTES, bar, pol);
-          } else {
-            bulk_g2s_hint(raw, sec + ((size_t)it.mt * (p.K / QGROUP) + kg) * (NMAT * I4_MAT_BYTES),
-                          NMAT * I4_MAT_BYTES, bar, pol);
-          }
+          // gate/up: gate and up blocks of (mt, kg); down: tile mt's block, or
+          // both blocks of the pair it.mt, contiguous in the down section
+          const size_t woff = MODE == G_DOWN ? i4_down_block(it.mt, kg, p.K / QGROUP, p.n_mt)
+                                             : ((size_t)it.mt * (p.K / QGROUP) + kg) * (NMAT * I4_MAT_BYTES);
+          bulk_g2s_hint(raw, sec + woff, NMAT * I4_MAT_BYTES, bar, pol);
           const uint32_t dst = smem_u32(S.b_ring + (size_t)rs.i * B_STAGE);
           tma_load_2d(dst, &tmap_b, kg * QGROUP, it.r0, bar);
           tma_load_2d(dst + B_BOX, &tmap_b, kg * QGROUP, p.rows_total + it.r0, bar);

@@ -22,6 +22,10 @@ namespace moe {
 //         (32 K each) form 16 bytes at ((h*2 + j)*128 + r)*16; each 32-bit word
 //         w of a quad covers K elements 8w..8w+7 with element 2i in bits
 //         [4i, 4i+4) and element 2i+1 in bits [16+4i, 20+4i).
+//         The down section stores output tiles in pairs: per (pair 2p, 2p+1,
+//         group g) the two tiles' blocks back to back, so that a GEMM step over
+//         both tiles is one contiguous copy; with an odd tile count the last
+//         tile follows alone, one block per group (i4_down_block).
 constexpr int TILE_M = 128;          // weight rows per MMA tile (the MMA's M)
 constexpr int KSTEP = 64;            // K elements per pipeline stage (one 128-byte row)
 constexpr int QGROUP = 128;          // int4 quantisation group
@@ -37,6 +41,13 @@ __host__ __device__ inline size_t gateup_section_bytes(int fmt, int d, int F) {
   return fmt == MOE_W_INT4_G128
              ? (size_t)(F / TILE_M) * (d / QGROUP) * (2 * I4_MAT_BYTES)
              : (size_t)(F / TILE_M) * (d / KSTEP) * (2 * BF16_TILE_BYTES);
+}
+// Byte offset, within the int4 down section, of output tile mt's block for
+// quantisation group g (G groups per row, n_mt output tiles).
+__host__ __device__ inline size_t i4_down_block(int mt, int g, int G, int n_mt) {
+  const int p0 = mt & ~1;
+  return p0 + 1 < n_mt ? ((size_t)p0 * G + 2 * g + (mt & 1)) * I4_MAT_BYTES
+                       : ((size_t)mt * G + g) * I4_MAT_BYTES;
 }
 __host__ __device__ inline size_t down_section_bytes(int fmt, int d, int F) {
   return fmt == MOE_W_INT4_G128 ? (size_t)(d / TILE_M) * (F / QGROUP) * I4_MAT_BYTES

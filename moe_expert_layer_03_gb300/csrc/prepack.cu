@@ -26,7 +26,8 @@ __global__ void prepack_bf16_kernel(const uint16_t* __restrict__ w0, const uint1
   }
 }
 
-// int4: destination block b = (mt * G + g) * NMAT + m of I4_MAT_BYTES.  Chunks
+// int4: gate/up (NMAT = 2) block b = (mt * G + g) * 2 + m of I4_MAT_BYTES; the
+// down matrix (NMAT = 1) block at i4_down_block(mt, g).  Chunks
 // 0..511 are the nibble quads (h, j, r) at ((h*2+j)*128 + r); chunks 512..543
 // carry the (scale | zero << 16) words, 4 rows per chunk.
 __global__ void prepack_int4_kernel(const uint8_t* __restrict__ q0, const uint16_t* __restrict__ s0,
@@ -72,7 +73,8 @@ __global__ void prepack_int4_kernel(const uint8_t* __restrict__ q0, const uint16
         out[w] = (uint32_t)sc[gi] | ((uint32_t)zr[gi] << 16);
       }
     }
-    *reinterpret_cast<uint4*>(dst + i * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+    const size_t blk_off = nmat == 2 ? blk * I4_MAT_BYTES : i4_down_block(mt, g, G, rows / TILE_M);
+    *reinterpret_cast<uint4*>(dst + blk_off + (size_t)c * 16) = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
 
