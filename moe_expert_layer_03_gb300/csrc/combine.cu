@@ -74,15 +74,37 @@ __global__ void __launch_bounds__(256)
                             const int32_t* __restrict__ row_of_assign,
                             const float* __restrict__ topk_w, int k, int d, int shared_row0,
                             uint16_t* __restrict__ out) {
-  griddep_wait();
-  griddep_launch_dependents();
   const int t = blockIdx.x;
   const int c = (blockIdx.y * 256 + threadIdx.x) * 4;
+  // The token's rows and weights come from the routing kernels, which finished
+  // before the GEMM that precedes this kernel passed its own dependency wait,
+  // so they are read before this kernel's wait (only the partial sums come
+  // from the preceding kernel).
+  constexpr int PRE = 8;
+  int rj[PRE];
+  float wj[PRE];
+#pragma unroll
+  for (int j = 0; j < PRE; ++j)
+    if (j < k) {
+      rj[j] = row_of_assign[t * k + j];
+      wj[j] = topk_w[t * k + j];
+    }
+  griddep_wait();
+  griddep_launch_dependents();
   if (c >= d) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < k; ++j) {
+#pragma unroll
+  for (int j = 0; j < PRE; ++j) {
+    if (j >= k || rj[j] < 0) continue;   // r < 0 only after an index error
+    const float4 y = y_from_partials<OVERLAP>(part, n_split, split_stride, rj[j], d, c);
+    acc.x += wj[j] * y.x;
+    acc.y += wj[j] * y.y;
+    acc.z += wj[j] * y.z;
+    acc.w += wj[j] * y.w;
+  }
+  for (int j = PRE; j < k; ++j) {
     const int r = row_of_assign[t * k + j];
-    if (r < 0) continue;   // only after an index error
+    if (r < 0) continue;
     const float w = topk_w[t * k + j];
     const float4 y = y_from_partials<OVERLAP>(part, n_split, split_stride, r, d, c);
     acc.x += w * y.x;
