@@ -20,6 +20,7 @@ Recipes (the values the layer sees; all seeded):
   * expert weights ~ N(0, 0.02) drawn in fp32 and rounded to bf16 ("source"),
     one independent torch Generator stream per (expert, matrix) so any single
     expert can be regenerated alone on any device.
+  * router weight (optional router GEMM) [E, d] ~ N(0, 0.02), rounded to bf16.
   * router logits fp32, per row resampled until the gap between the k-th and
     (k+1)-th largest value is >= 1e-3 so the top-k set is unambiguous.
       - "normal": i.i.d. N(0,1).
@@ -87,6 +88,15 @@ def _rng(seed: int, *stream: int) -> np.random.Generator:
 def make_x(cfg: LayerConfig) -> torch.Tensor:
     """Token activations, bf16 [T, d] on the CPU."""
     v = _rng(cfg.seed, 1).standard_normal((cfg.T, cfg.d), dtype=np.float32)
+    return torch.from_numpy(v).to(torch.bfloat16)
+
+
+# ----------------------------------------------------------------------------- router weight
+def make_router_weight(cfg: LayerConfig) -> torch.Tensor:
+    """Router weight for the optional router GEMM, bf16 [E, d] on the CPU:
+    N(0, 0.02) drawn in fp32 and rounded to bf16 (same recipe as the expert
+    weights), its own seeded stream."""
+    v = _rng(cfg.seed, 5).standard_normal((cfg.E, cfg.d), dtype=np.float32) * np.float32(0.02)
     return torch.from_numpy(v).to(torch.bfloat16)
 
 

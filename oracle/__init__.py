@@ -57,6 +57,7 @@ def lib():
             L.oracle_fp16_to_double.argtypes = [C.c_uint16]
             L.oracle_weight.restype = C.c_double
             L.oracle_weight.argtypes = [C.POINTER(Matrix), C.c_int, C.c_int]
+            L.oracle_router_logits.argtypes = [P, P, C.c_int, C.c_int, C.c_int, P]
             L.oracle_route_topk.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
             L.oracle_permute.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P, P, P]
             L.oracle_expert_ffn.argtypes = [P, C.c_int, C.c_int, C.POINTER(Expert), P, P]
@@ -109,6 +110,21 @@ class ExpertRef:
 
 
 # ----------------------------------------------------------------------------- API
+def router_logits(x, w_router):
+    """float64 [T, E] logits of bf16 x [T, d] against bf16 router rows [E, d]."""
+    xb = _np(x, np.uint16)
+    wb = _np(w_router, np.uint16)
+    T, d = xb.shape
+    E = wb.shape[0]
+    if wb.shape[1] != d:
+        raise ValueError("router_logits: x and w_router disagree on d")
+    out = np.zeros((T, E), np.float64)
+    rc = lib().oracle_router_logits(_ptr(xb), _ptr(wb), T, d, E, _ptr(out))
+    if rc:
+        raise ValueError("oracle_router_logits: bad arguments")
+    return out
+
+
 def route_topk(logits, k: int):
     lg = _np(logits, np.float32)
     T, E = lg.shape

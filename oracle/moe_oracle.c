@@ -44,6 +44,25 @@ double oracle_weight(const oracle_matrix* m, int row, int col) {
   return ((double)q - z) * s;
 }
 
+/* ------------------------------------------------------------------ router */
+
+/* Router logits ([CoInf] sec. 2.1, sec. 5.1): the plain dot product of each
+ * token row with each expert's router row, in fp64 (a product of two bf16
+ * values is exact in fp64, and so is every partial sum up to d = 2^20). */
+int oracle_router_logits(const uint16_t* x, const uint16_t* w_router, int T, int d, int E,
+                         double* logits) {
+  if (!x || !w_router || !logits || T < 0 || d < 1 || E < 1) return -1;
+  for (int t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int i = 0; i < d; ++i)
+        acc += oracle_bf16_to_double(x[(size_t)t * d + i]) *
+               oracle_bf16_to_double(w_router[(size_t)e * d + i]);
+      logits[(size_t)t * E + e] = acc;
+    }
+  return 0;
+}
+
 /* ------------------------------------------------------------------ gating */
 
 /* Top-k gating ([Mira] sec. 4.2; [Strata] sec. 1.1): the k largest fp32 logits

@@ -54,6 +54,13 @@ double oracle_bf16_to_double(uint16_t b);
 double oracle_fp16_to_double(uint16_t h);
 double oracle_weight(const oracle_matrix* m, int row, int col);   /* dequantised value */
 
+/* Router logits ([CoInf] sec. 2.1 router resident on the GPU; sec. 5.1 router
+ * kept at full precision): logits[t][e] = sum_i x[t][i] * w_router[e][i] for
+ * bf16 x [T][d] and w_router [E][d] (both row-major, the input dim contiguous),
+ * summed exactly in fp64.  Returns 0, or -1 on bad args. */
+int oracle_router_logits(const uint16_t* x, const uint16_t* w_router, int T, int d, int E,
+                         double* logits /* [T][E] */);
+
 /* Top-k gating: idx [T][k] int32, w [T][k] fp32.  Returns 0, or -1 on bad args. */
 int oracle_route_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w);
 

@@ -96,6 +96,56 @@ def test_int4_error_bound_random_groups():
     assert np.all(err <= bound)
 
 
+# ----------------------------------------------------------------------------- router logits
+def _bf16_bits_of(values) -> np.ndarray:
+    return _bits(torch.tensor(np.asarray(values, np.float32)).to(torch.bfloat16))
+
+
+def test_router_one_hot_rows_select_router_columns():
+    """x[t] = c_t * unit vector i_t selects column i_t of the router weight, scaled
+    by c_t (a power of two, exact): catches a transposed operand or a wrong index."""
+    rng = np.random.default_rng(11)
+    T, d, E = 6, 40, 5
+    w = _bits(torch.from_numpy(rng.standard_normal((E, d)).astype(np.float32) * 0.02).to(torch.bfloat16))
+    cols = [0, 39, 7, 7, 21, 13]
+    scale = [1.0, 2.0, -0.5, 4.0, 1.0, -1.0]
+    x = np.zeros((T, d), np.float32)
+    for t in range(T):
+        x[t, cols[t]] = scale[t]
+    lg = oracle.router_logits(_bf16_bits_of(x), w)
+    for t in range(T):
+        np.testing.assert_array_equal(lg[t], scale[t] * bf(w[:, cols[t]]).astype(np.float64))
+
+
+def test_router_small_integers_bruteforce():
+    """Integer-valued bf16 inputs: the logits are exact integers, checked against a
+    pure-Python integer triple loop."""
+    rng = np.random.default_rng(12)
+    T, d, E = 3, 9, 4
+    xi = rng.integers(-4, 5, (T, d))
+    wi = rng.integers(-4, 5, (E, d))
+    lg = oracle.router_logits(_bf16_bits_of(xi), _bf16_bits_of(wi))
+    for t in range(T):
+        for e in range(E):
+            assert lg[t, e] == sum(int(xi[t, i]) * int(wi[e, i]) for i in range(d))
+
+
+def test_router_random_matches_exact_rational_sum():
+    """N(0,1) tokens against N(0,0.02) router rows: the fp64 logit equals the exact
+    rational dot product rounded once (the partial sums here need well under 53 bits)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(13)
+    T, d, E = 2, 64, 3
+    x = _bits(torch.from_numpy(rng.standard_normal((T, d)).astype(np.float32)).to(torch.bfloat16))
+    w = _bits(torch.from_numpy(rng.standard_normal((E, d)).astype(np.float32) * 0.02).to(torch.bfloat16))
+    lg = oracle.router_logits(x, w)
+    xf, wf = bf(x), bf(w)
+    for t in range(T):
+        for e in range(E):
+            exact = sum(Fraction(float(xf[t, i])) * Fraction(float(wf[e, i])) for i in range(d))
+            assert lg[t, e] == float(exact)
+
+
 # ----------------------------------------------------------------------------- top-k
 def _golden_topk():
     for line in open(os.path.join(GOLD, "topk_cases.txt")):
