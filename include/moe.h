@@ -122,6 +122,17 @@ moe_status moe_prepack_expert(int fmt, int d_model, int d_ff, const moe_expert_s
 
 /* ---------------------------------------------------------------- hot path */
 
+/* Router logits ([CoInf] sec. 2.1: the router runs on the GPU; sec. 5.1: the
+ * router network keeps full precision):
+ *   logits[t][e] = sum_i x[t][i] * w_router[e][i]
+ * x bf16 [T][d] and w_router bf16 [E][d], both row-major with the input dim
+ * contiguous; logits fp32 [T][E].  Products and sums in fp32 (the order is
+ * fixed, so results are reproducible run to run).  Requires d % 8 == 0,
+ * 1 <= E <= 256, 16-byte aligned pointers; otherwise MOE_ERR_INVALID_ARG /
+ * MOE_ERR_UNSUPPORTED and nothing is launched.  One kernel launch. */
+moe_status moe_router_logits(const uint16_t* x, const uint16_t* w_router, int T, int d, int E,
+                             float* logits, moe_stream_t stream);
+
 /* Top-k gating ([Mira] sec. 4.2; [Strata] sec. 1.1).
  * logits: fp32 [T][E].  For each token the k largest logits (the lower expert
  * index first among equal logits), in descending order -> topk_idx int32 [T][k];
@@ -175,6 +186,15 @@ size_t moe_layer_workspace_bytes(int T, int k, const moe_pool* routed, const moe
 moe_status moe_layer_forward(const uint16_t* x, const float* logits, int T, int k,
                              const moe_pool* routed, const moe_pool* shared, uint16_t* out,
                              void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The whole layer from the token rows and the router weight: moe_router_logits
+ * into `logits` (caller-owned fp32 [T][E], written; E = routed->n_experts),
+ * then moe_layer_forward on those logits.  w_router bf16 [E][d_model].  Same
+ * workspace, checks and results as moe_layer_forward; one launch more. */
+moe_status moe_layer_forward_router(const uint16_t* x, const uint16_t* w_router, int T, int k,
+                                    const moe_pool* routed, const moe_pool* shared,
+                                    float* logits, uint16_t* out, void* ws, size_t ws_bytes,
+                                    moe_stream_t stream);
 
 /* Stage boundaries of moe_layer_forward, for timing with CUDA events. */
 enum {

@@ -35,7 +35,7 @@ EXPORTS = ("moe_status_str", "moe_slot_bytes", "moe_prepack_expert", "moe_route_
            "moe_permute_workspace_bytes", "moe_permute", "moe_grouped_ffn_workspace_bytes",
            "moe_grouped_ffn", "moe_combine", "moe_layer_workspace_bytes", "moe_layer_forward",
            "moe_layer_forward_timed", "moe_layer_launch_count", "moe_last_device_error",
-           "moe_layer_forward_noalloc")
+           "moe_layer_forward_noalloc", "moe_router_logits", "moe_layer_forward_router")
 
 
 class MoeError(RuntimeError):
@@ -70,6 +70,9 @@ def lib() -> C.CDLL:
             L.moe_slot_bytes.restype = S
             L.moe_slot_bytes.argtypes = [I, I, I]
             L.moe_prepack_expert.argtypes = [I, I, I, C.POINTER(ExpertSrc), P, P]
+            L.moe_router_logits.argtypes = [P, P, I, I, I, P, P]
+            L.moe_layer_forward_router.argtypes = [P, P, I, I, C.POINTER(MoePool),
+                                                   C.POINTER(MoePool), P, P, P, S, P]
             L.moe_route_topk.argtypes = [P, I, I, I, P, P, P]
             L.moe_permute_workspace_bytes.restype = S
             L.moe_permute_workspace_bytes.argtypes = []
@@ -185,6 +188,17 @@ def last_device_error(ws: torch.Tensor, stream=None) -> int:
 
 
 # ----------------------------------------------------------------------------- hot path
+def router_logits(x: torch.Tensor, w_router: torch.Tensor, logits=None, stream=None):
+    """fp32 [T, E] logits = x (bf16 [T, d]) . w_router (bf16 [E, d]) per row."""
+    T, d = x.shape
+    E = w_router.shape[0]
+    logits = logits if logits is not None else torch.empty(T, E, dtype=torch.float32,
+                                                           device=x.device)
+    _check(lib().moe_router_logits(_ptr(x), _ptr(w_router), T, d, E, _ptr(logits),
+                                   _stream(stream)), "moe_router_logits")
+    return logits
+
+
 def route_topk(logits: torch.Tensor, k: int, idx=None, w=None, stream=None):
     T, E = logits.shape
     idx = idx if idx is not None else torch.empty(T, k, dtype=torch.int32, device=logits.device)
@@ -259,6 +273,27 @@ def layer_forward(x: torch.Tensor, logits: torch.Tensor, k: int, routed: PoolVie
                                            _ptr(ws), ws.numel(), _stream(stream), arr)
     _check(st, "moe_layer_forward")
     return out, ws
+
+
+def layer_forward_router(x: torch.Tensor, w_router: torch.Tensor, k: int, routed: PoolView,
+                         shared: PoolView | None = None, logits=None, out=None, ws=None,
+                         stream=None):
+    """The layer from the token rows and the router weight (bf16 [E, d]): returns
+    (out bf16 [T, d], logits fp32 [T, E], ws)."""
+    T, d = x.shape
+    E = routed.struct.n_experts
+    out = out if out is not None else torch.empty(T, d, dtype=torch.bfloat16, device=x.device)
+    logits = logits if logits is not None else torch.empty(T, E, dtype=torch.float32,
+                                                           device=x.device)
+    need = layer_workspace_bytes(T, k, routed, shared)
+    if need == 0:
+        raise MoeError("moe_layer_workspace_bytes: invalid layer description")
+    ws = ws if ws is not None else workspace(need, x.device)
+    sh = shared.ref if shared is not None else None
+    _check(lib().moe_layer_forward_router(_ptr(x), _ptr(w_router), T, k, routed.ref, sh,
+                                          _ptr(logits), _ptr(out), _ptr(ws), ws.numel(),
+                                          _stream(stream)), "moe_layer_forward_router")
+    return out, logits, ws
 
 
 def layer_launch_count(T: int, k: int, routed: PoolView, shared: PoolView | None = None) -> int:

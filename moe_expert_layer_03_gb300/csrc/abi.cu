@@ -274,9 +274,12 @@ moe_status check_route_args(const float* logits, int T, int E, int k, const void
   return MOE_OK;
 }
 
+// route_pdl: the routing kernel follows a kernel of the same call (the router
+// GEMM) and may start early.
 moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int k,
                               const moe_pool* routed, const moe_pool* shared, uint16_t* out,
-                              void* ws, size_t ws_bytes, cudaStream_t s, void* const* ev) {
+                              void* ws, size_t ws_bytes, cudaStream_t s, void* const* ev,
+                              bool route_pdl = false) {
   moe_status st = check_pool(routed, false);
   if (st != MOE_OK) return st;
   if (shared) {
@@ -314,12 +317,13 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
 
   if (!rec(MOE_STAGE_ROUTE)) return MOE_ERR_CUDA;
   if (T <= FUSED_ROUTE_MAX_T) {   // one launch; its time is reported as the routing stage
-    if (launch_route_permute(logits, T, k, E, L.Tsh, idx, w, counts, offsets, roa, tor, err, s) !=
-        cudaSuccess)
+    if (launch_route_permute(logits, T, k, E, L.Tsh, idx, w, counts, offsets, roa, tor, err, s,
+                             route_pdl && pdl) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (!rec(MOE_STAGE_PERMUTE)) return MOE_ERR_CUDA;
   } else {
-    if (launch_route_topk(logits, T, E, k, idx, w, nullptr, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_route_topk(logits, T, E, k, idx, w, nullptr, s, route_pdl && pdl) != cudaSuccess)
+      return MOE_ERR_CUDA;
     if (!rec(MOE_STAGE_PERMUTE)) return MOE_ERR_CUDA;
     if (launch_permute_index(idx, T, k, E, L.Tsh, counts, offsets, roa, tor, err, s, pdl) != cudaSuccess)
       return MOE_ERR_CUDA;
@@ -378,6 +382,25 @@ moe_status moe_prepack_expert(int fmt, int d_model, int d_ff, const moe_expert_s
     if (fmt == MOE_W_INT4_G128 && (!src->scale[m] || !src->zero[m])) return MOE_ERR_INVALID_ARG;
   }
   return launch_prepack(fmt, d_model, d_ff, *src, (uint8_t*)slot_dst, (cudaStream_t)stream) ==
+                 cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+moe_status check_router_args(const uint16_t* x, const uint16_t* w_router, int T, int d, int E,
+                             const float* logits) {
+  if (!x || !w_router || !logits) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || d < 8 || d % 8 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (E > MAX_E || d > MAX_DIM) return MOE_ERR_UNSUPPORTED;
+  if (!al16(x) || !al16(w_router) || !al16(logits)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status moe_router_logits(const uint16_t* x, const uint16_t* w_router, int T, int d, int E,
+                             float* logits, moe_stream_t stream) {
+  const moe_status st = check_router_args(x, w_router, T, d, E, logits);
+  if (st != MOE_OK) return st;
+  return launch_router_logits(x, w_router, T, d, E, logits, sm_count(), (cudaStream_t)stream) ==
                  cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
@@ -509,6 +532,25 @@ moe_status moe_layer_forward(const uint16_t* x, const float* logits, int T, int 
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
   return layer_forward_impl(x, logits, T, k, routed, shared, out, ws, ws_bytes,
                             (cudaStream_t)stream, nullptr);
+}
+
+moe_status moe_layer_forward_router(const uint16_t* x, const uint16_t* w_router, int T, int k,
+                                    const moe_pool* routed, const moe_pool* shared,
+                                    float* logits, uint16_t* out, void* ws, size_t ws_bytes,
+                                    moe_stream_t stream) {
+  moe_status st = check_pool(routed, false);
+  if (st != MOE_OK) return st;
+  if ((st = check_router_args(x, w_router, T, routed->d_model, routed->n_experts, logits)) != MOE_OK)
+    return st;
+  // every check of the layer runs before the first launch
+  if (!out || !ws || k < 1 || k > routed->n_experts) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_layer_workspace_bytes(T, k, routed, shared)) return MOE_ERR_WORKSPACE;
+  if (moe_layer_workspace_bytes(T, k, routed, shared) == 0) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (launch_router_logits(x, w_router, T, routed->d_model, routed->n_experts, logits, sm_count(), s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return layer_forward_impl(x, logits, T, k, routed, shared, out, ws, ws_bytes, s, nullptr, true);
 }
 
 moe_status moe_layer_forward_timed(const uint16_t* x, const float* logits, int T, int k,

@@ -145,9 +145,12 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 }
 
 // ------------------------------------------------------------------ other kernels
+// logits[t][e] = x[t] . w_router[e] (bf16 inputs, fp32 sums; router.cu).
+cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w_router, int T, int d, int E,
+                                 float* logits, int n_sm, cudaStream_t s, bool pdl = false);
 // err_clear (nullable): error word zeroed by the first thread (first launch of a forward).
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
-                              int* err_clear, cudaStream_t s);
+                              int* err_clear, cudaStream_t s, bool pdl = false);
 // The launches below take pdl = true when the previous kernel in the stream
 // belongs to the same call (programmatic dependent launch: this kernel's
 // prologue overlaps that kernel's tail; it reads nothing before

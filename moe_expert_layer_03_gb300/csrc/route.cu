@@ -12,6 +12,8 @@ template <int VPL>   // logits per lane = ceil(E / 32)
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
                                                          int E, int k, int32_t* __restrict__ idx,
                                                          float* __restrict__ w, int* err_clear) {
+  griddep_wait();
+  griddep_launch_dependents();
   if (err_clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *err_clear = 0;
   const int tok = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   if (tok >= T) return;
@@ -19,18 +21,16 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 }
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
-                              int* err_clear, cudaStream_t s) {
+                              int* err_clear, cudaStream_t s, bool pdl) {
   const dim3 block(256);
   const dim3 grid((unsigned)((T + 7) / 8));
   if (E <= 32)
-    route_topk_kernel<1><<<grid, block, 0, s>>>(logits, T, E, k, idx, w, err_clear);
-  else if (E <= 64)
-    route_topk_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, idx, w, err_clear);
-  else if (E <= 128)
-    route_topk_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, idx, w, err_clear);
-  else
-    route_topk_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, idx, w, err_clear);
-  return cudaGetLastError();
+    return launch_kernel(route_topk_kernel<1>, grid, block, 0, s, pdl, logits, T, E, k, idx, w, err_clear);
+  if (E <= 64)
+    return launch_kernel(route_topk_kernel<2>, grid, block, 0, s, pdl, logits, T, E, k, idx, w, err_clear);
+  if (E <= 128)
+    return launch_kernel(route_topk_kernel<4>, grid, block, 0, s, pdl, logits, T, E, k, idx, w, err_clear);
+  return launch_kernel(route_topk_kernel<8>, grid, block, 0, s, pdl, logits, T, E, k, idx, w, err_clear);
 }
 
 }  // namespace moe

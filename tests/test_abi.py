@@ -76,3 +76,23 @@ def test_host_checks_reject_before_launch(L):
     assert L.moe_route_topk(None, 4, 8, 2, P(0x10), P(0x20), None) == 1
     assert L.moe_route_topk(lg, 4, 300, 2, P(0x10), P(0x20), None) == 2               # E > 256
     assert L.moe_combine(P(0x10), P(0x20), P(0x30), None, 4, 2, 100, P(0x40), None) == 1
+
+
+def test_router_host_checks_reject_before_launch(L):
+    p = _fake_pool()
+    P = C.c_void_p
+    x, wr, lg, out, ws = P(0x30000000), P(0x38000000), P(0x40000000), P(0x50000000), P(0x60000000)
+    rl = L.moe_router_logits
+    rl.argtypes = [P, P, C.c_int, C.c_int, C.c_int, P, P]
+    assert rl(None, wr, 4, 256, 8, lg, None) == 1                    # null x
+    assert rl(x, wr, 0, 256, 8, lg, None) == 1                       # T = 0
+    assert rl(x, wr, 4, 100, 8, lg, None) == 1                       # d % 8 != 0
+    assert rl(x, wr, 4, 256, 0, lg, None) == 1                       # E = 0
+    assert rl(x, wr, 4, 256, 300, lg, None) == 2                     # E > 256
+    assert rl(x, P(0x38000008), 4, 256, 8, lg, None) == 1            # misaligned router weight
+    need = L.moe_layer_workspace_bytes(16, 2, C.byref(p), None)
+    fr = L.moe_layer_forward_router
+    fr.argtypes = [P, P, C.c_int, C.c_int, C.c_void_p, C.c_void_p, P, P, P, C.c_size_t, P]
+    assert fr(x, None, 16, 2, C.byref(p), None, lg, out, ws, need, None) == 1        # null router
+    assert fr(x, wr, 16, 9, C.byref(p), None, lg, out, ws, need, None) == 1          # k > E
+    assert fr(x, wr, 16, 2, C.byref(p), None, lg, out, ws, need - 1, None) == 3      # small ws

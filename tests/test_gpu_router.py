@@ -1,0 +1,113 @@
+"""GPU parity of the router GEMM (logits[t][e] = x[t] . w_router[e], bf16 inputs,
+fp32 sums) against the oracle's exact fp64 dot products, and of the layer
+forward that starts from the token rows and the router weight.
+
+Tolerance, from the kernel's arithmetic: every logit is one fixed-order fp32
+sum whose longest chain has n = 8 * ceil(d / 2048) + 5 + 8 roundings (a
+thread's FMAs over its K vectors, the 5-step warp butterfly, the 8 warps' sums),
+so |got - exact| <= gamma_n * sum_i |x_i w_i| with gamma_n = n u / (1 - n u),
+u = 2^-24 (the bf16 products themselves are exact in fp32)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_03_gb300 as moe
+import moe_synth as ms
+import oracle
+from layer_setup import GpuLayer, assert_close_rms
+
+pytestmark = pytest.mark.gpu
+
+U = 2.0 ** -24
+
+
+def _gamma(d: int) -> float:
+    n = 8 * math.ceil(d / 2048) + 5 + 8
+    return n * U / (1 - n * U)
+
+
+def _abs_dot(x: torch.Tensor, w: torch.Tensor) -> np.ndarray:
+    """sum_i |x[t][i] w[e][i]| (the scale of the summation error), [T, E]."""
+    xa = x.cpu().double().abs().numpy()
+    wa = w.cpu().double().abs().numpy()
+    return xa @ wa.T
+
+
+def _draw(T, d, E, seed):
+    g = np.random.default_rng(seed)
+    x = torch.from_numpy(g.standard_normal((T, d), dtype=np.float32)).to(torch.bfloat16)
+    w = torch.from_numpy(g.standard_normal((E, d), dtype=np.float32) * np.float32(0.02)).to(torch.bfloat16)
+    return x, w
+
+
+def _check_logits(got: torch.Tensor, x: torch.Tensor, w: torch.Tensor, what: str):
+    want = oracle.router_logits(x.cpu(), w.cpu())
+    bound = _gamma(x.shape[1]) * _abs_dot(x, w) + 1e-30
+    err = np.abs(got.double().cpu().numpy() - want)
+    worst = np.unravel_index(np.argmax(err / bound), err.shape)
+    assert np.all(err <= bound), f"{what}: |err| {err[worst]:.3e} > bound {bound[worst]:.3e} at {worst}"
+    return want, bound
+
+
+@pytest.mark.parametrize("T,d,E", [
+    (16, 4096, 8),      # Mixtral-shaped decode
+    (16, 5120, 128),    # 125B-class decode
+    (2048, 4096, 8),    # Mixtral-shaped prefill chunk
+    (37, 392, 5),       # ragged: T not a tile multiple, d not a multiple of 128, E < 8
+    (1, 256, 1),        # one token, one expert
+    (301, 1024, 256),   # the largest E, ragged last token tile
+    (9, 8, 13),         # d = one 16-byte vector
+])
+def test_router_logits_vs_oracle(T, d, E):
+    x, w = _draw(T, d, E, seed=T * 7 + E)
+    xd, wd = x.cuda(), w.cuda()
+    got = moe.router_logits(xd, wd)
+    torch.cuda.synchronize()
+    _check_logits(got, x, w, f"T={T} d={d} E={E}")
+
+
+def test_router_logits_reproducible_and_row_independent():
+    """Fixed summation order: the same call twice gives the same bits, and a
+    token's logits do not depend on which other tokens share its launch."""
+    x, w = _draw(64, 2048, 24, seed=5)
+    xd, wd = x.cuda(), w.cuda()
+    a = moe.router_logits(xd, wd)
+    b = moe.router_logits(xd, wd)
+    one = moe.router_logits(xd[17:18].contiguous(), wd)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert torch.equal(a[17:18], one)
+
+
+@pytest.mark.parametrize("name", ["tiny_int4", "int4_shared_perm", "int4_ragged"])
+def test_layer_forward_router(name):
+    """The layer from x and the router weight: logits within the bound above,
+    then every token whose top-k choice is unambiguous under that bound routed as
+    the oracle routes its own logits, and its output within 2e-2 RMS."""
+    from test_gpu_layer import SMALL
+    cfg = SMALL[name]
+    L = GpuLayer(cfg)
+    wr = ms.make_router_weight(cfg)
+    out, logits, ws = moe.layer_forward_router(L.x, wr.to(L.dev), cfg.k, L.routed, L.shared)
+    torch.cuda.synchronize()
+    assert moe.last_device_error(ws) == 0
+    want_lg, bound = _check_logits(logits, L.x, wr, name)
+
+    # tokens whose k + 1 largest exact logits are pairwise further apart than two
+    # bounds (the chosen set and its order cannot depend on the rounding)
+    toks = []
+    for t in range(cfg.T):
+        s = np.sort(want_lg[t])[::-1][: cfg.k + 1]
+        if np.all(np.diff(s) < -2 * bound[t].max()):
+            toks.append(t)
+    assert len(toks) >= cfg.T - 1, "synthetic router logits should be unambiguous"
+
+    lg32 = want_lg.astype(np.float32)
+    idx_gpu, _ = moe.route_topk(logits, cfg.k)
+    idx_ref, _ = oracle.route_topk(lg32, cfg.k)
+    np.testing.assert_array_equal(idx_gpu.cpu().numpy()[toks], idx_ref[toks])
+
+    L.logits_np = lg32
+    assert_close_rms(out.float().cpu().numpy()[toks], L.oracle_forward(toks), what=name)
