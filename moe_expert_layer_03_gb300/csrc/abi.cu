@@ -317,24 +317,26 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
 
   if (!rec(MOE_STAGE_ROUTE)) return MOE_ERR_CUDA;
   if (T <= FUSED_ROUTE_MAX_T) {   // one launch; its time is reported as the routing stage
-    if (launch_route_permute(logits, T, k, E, L.Tsh, idx, w, counts, offsets, roa, tor, err, s,
-                             route_pdl && pdl) != cudaSuccess)
+    const GatherDst dst{xperm, f8.xq, f8.xs, f8.xe};
+    const int out_kind = L.fp8 ? GATHER_FP8 : f16 ? GATHER_F16 : GATHER_BF16;
+    if (launch_route_gather(logits, T, k, E, L.Tsh, x, L.d, idx, w, counts, offsets, roa, tor, err,
+                            out_kind, dst, sm_count(), s, route_pdl && pdl) != cudaSuccess)
       return MOE_ERR_CUDA;
-    if (!rec(MOE_STAGE_PERMUTE)) return MOE_ERR_CUDA;
+    if (!rec(MOE_STAGE_PERMUTE) || !rec(MOE_STAGE_GATHER)) return MOE_ERR_CUDA;
   } else {
     if (launch_route_topk(logits, T, E, k, idx, w, nullptr, s, route_pdl && pdl) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (!rec(MOE_STAGE_PERMUTE)) return MOE_ERR_CUDA;
     if (launch_permute_index(idx, T, k, E, L.Tsh, counts, offsets, roa, tor, err, s, pdl) != cudaSuccess)
       return MOE_ERR_CUDA;
-  }
-  if (!rec(MOE_STAGE_GATHER)) return MOE_ERR_CUDA;
-  if (L.fp8) {
-    if (launch_gather_rows_fp8(x, tor, L.rows, T, L.d, f8.xq, f8.xs, f8.xe, sm_count(), s, pdl) !=
-        cudaSuccess)
+    if (!rec(MOE_STAGE_GATHER)) return MOE_ERR_CUDA;
+    if (L.fp8) {
+      if (launch_gather_rows_fp8(x, tor, L.rows, T, L.d, f8.xq, f8.xs, f8.xe, sm_count(), s, pdl) !=
+          cudaSuccess)
+        return MOE_ERR_CUDA;
+    } else if (launch_gather_rows(x, tor, L.rows, T, L.d, xperm, f16, sm_count(), s, pdl) != cudaSuccess) {
       return MOE_ERR_CUDA;
-  } else if (launch_gather_rows(x, tor, L.rows, T, L.d, xperm, f16, sm_count(), s, pdl) != cudaSuccess) {
-    return MOE_ERR_CUDA;
+    }
   }
   if (!rec(MOE_STAGE_GATE_UP)) return MOE_ERR_CUDA;
   st = run_ffn(xperm, offsets, E + (shared ? 1 : 0), L.rows, routed, shared, L.bn, L.ksplit, h, part,
@@ -563,8 +565,8 @@ moe_status moe_layer_forward_timed(const uint16_t* x, const float* logits, int T
 
 int moe_layer_launch_count(int T, int k, const moe_pool* routed, const moe_pool* shared) {
   if (moe_layer_workspace_bytes(T, k, routed, shared) == 0) return 0;
-  // route (+) permute, gather, gate/up, down, combine
-  return T <= FUSED_ROUTE_MAX_T ? 5 : 6;
+  // route + permute + gather in one launch for small batches; gate/up, down, combine
+  return T <= FUSED_ROUTE_MAX_T ? 4 : 6;
 }
 
 moe_status moe_last_device_error(const void* ws, int* code, moe_stream_t stream) {

@@ -159,13 +159,22 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
 cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_shared,
                                  int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
                                  int32_t* token_of_row, int* err, cudaStream_t s, bool pdl = false);
-// Routing and permutation in one launch (one CTA), for batches of up to
-// FUSED_ROUTE_MAX_T tokens: same outputs as launch_route_topk followed by
-// launch_permute_index.
+// Routing, permutation and row gather in one launch, for batches of up to
+// FUSED_ROUTE_MAX_T tokens: the outputs of launch_route_topk,
+// launch_permute_index and the row gather (out: GATHER_BF16 / GATHER_F16 into
+// dst.x16 [rows][d], or GATHER_FP8 into dst.xq/xs/xe, the int4 decode GEMM's
+// e4m3 form), rows = T*k (+ t_shared).
 constexpr int FUSED_ROUTE_MAX_T = 64;
-cudaError_t launch_route_permute(const float* logits, int T, int k, int E, int t_shared, int32_t* idx,
-                                 float* w, int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
-                                 int32_t* token_of_row, int* err, cudaStream_t s, bool pdl = false);
+enum { GATHER_BF16 = 0, GATHER_F16 = 1, GATHER_FP8 = 2 };
+struct GatherDst {
+  uint16_t* x16;
+  uint8_t* xq;
+  float *xs, *xe;
+};
+cudaError_t launch_route_gather(const float* logits, int T, int k, int E, int t_shared, const uint16_t* x,
+                                int d, int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
+                                int32_t* row_of_assign, int32_t* token_of_row, int* err, int out,
+                                const GatherDst& dst, int n_sm, cudaStream_t s, bool pdl = false);
 // x_perm[r] = x[token_of_row[r]].  to_fp16: write fp16 (saturating) instead of
 // bf16.  token_of_row == nullptr: x_perm[r] = x[r].
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,

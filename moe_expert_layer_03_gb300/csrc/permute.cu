@@ -11,11 +11,17 @@
 //      count table gives each warp its base.  The row of assignment a is
 //      offsets[e] + (number of earlier assignments with expert e) -- unique, so
 //      the result is independent of scheduling.
-// route_permute_kernel (batches of up to FUSED_ROUTE_MAX_T tokens): the top-k
-//   gating of every token (a warp per token, route_dev.cuh), then the same
-//   three steps, in one CTA and one launch.
+// route_gather_kernel (batches of up to FUSED_ROUTE_MAX_T tokens): routing,
+//   permutation and the row gather in one launch.  Every CTA routes all tokens
+//   (a warp per token, route_dev.cuh) and runs the three steps above on its
+//   own copy in shared memory -- a few hundred assignments, cheaper than any
+//   hand-off between CTAs -- then gathers its share of the rows; CTA 0 also
+//   publishes the routing results.
 // gather_rows_kernel: x_perm[r] = x[token_of_row[r]], one warp per row, 16-byte
 //   vector loads and stores.
+// The gathers release their dependent kernel before their own dependency wait:
+// the dependent (a GEMM) only reads their output after its own wait, and its
+// large CTAs get their set-up done while the gather waits and runs.
 #include "kernels.cuh"
 #include "ptx.cuh"
 #include "route_dev.cuh"
@@ -27,31 +33,33 @@ constexpr int PERM_WARPS = PERM_THREADS / 32;
 constexpr int PERM_MAX_E = 256;
 
 // histogram, scan and stable scatter of the A = T*k expert ids, by one CTA of
-// PERM_THREADS threads (which all call it)
-__device__ __forceinline__ void permute_cta(const int32_t* __restrict__ idx, int T, int k, int E, int t_shared,
-                                            int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                                            int32_t* __restrict__ row_of_assign,
-                                            int32_t* __restrict__ token_of_row, int* __restrict__ err) {
+// NT threads (which all call it).  The arrays may be global or shared memory.
+// err (nullable): cleared first (first kernel of the pipeline that reports
+// device errors), then ORed with MOE_DEVERR_EXPERT_RANGE for an id outside [0, E).
+template <int NT>
+__device__ __forceinline__ void permute_cta(const int32_t* idx, int T, int k, int E, int t_shared,
+                                            int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
+                                            int32_t* token_of_row, int* err) {
+  constexpr int NW = NT / 32;
   __shared__ int s_cnt[PERM_MAX_E];
   __shared__ int s_base[PERM_MAX_E];
-  __shared__ int s_wc[PERM_WARPS][PERM_MAX_E];
+  __shared__ int s_wc[NW][PERM_MAX_E];
   __shared__ int s_total;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int A = T * k;
 
-  // first kernel of the pipeline that reports device errors: clear the word
-  if (tid == 0) *err = 0;
-  for (int e = tid; e < E; e += PERM_THREADS) s_cnt[e] = 0;
+  if (err != nullptr && tid == 0) *err = 0;
+  for (int e = tid; e < E; e += NT) s_cnt[e] = 0;
   __syncthreads();
   bool bad = false;
-  for (int a = tid; a < A; a += PERM_THREADS) {
+  for (int a = tid; a < A; a += NT) {
     const int e = idx[a];
     if (e < 0 || e >= E)
       bad = true;
     else
       atomicAdd(&s_cnt[e], 1);
   }
-  if (bad) atomicOr(err, MOE_DEVERR_EXPERT_RANGE);
+  if (bad && err != nullptr) atomicOr(err, MOE_DEVERR_EXPERT_RANGE);
   __syncthreads();
 
   // exclusive scan by warp 0: lane l owns experts [8l, 8l+8)
@@ -90,8 +98,8 @@ __device__ __forceinline__ void permute_cta(const int32_t* __restrict__ idx, int
   __syncthreads();
 
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int base = 0; base < A; base += PERM_THREADS) {
-    for (int i = tid; i < PERM_WARPS * E; i += PERM_THREADS) s_wc[i / E][i % E] = 0;
+  for (int base = 0; base < A; base += NT) {
+    for (int i = tid; i < NW * E; i += NT) s_wc[i / E][i % E] = 0;
     __syncthreads();
     const int a = base + tid;
     int e = a < A ? idx[a] : -1;
@@ -110,15 +118,15 @@ __device__ __forceinline__ void permute_cta(const int32_t* __restrict__ idx, int
       row_of_assign[a] = -1;
     }
     __syncthreads();
-    for (int ee = tid; ee < E; ee += PERM_THREADS) {
+    for (int ee = tid; ee < E; ee += NT) {
       int s = 0;
-      for (int w = 0; w < PERM_WARPS; ++w) s += s_wc[w][ee];
+      for (int w = 0; w < NW; ++w) s += s_wc[w][ee];
       s_base[ee] += s;
     }
     __syncthreads();
   }
   // rows of the always-on shared expert follow the routed rows, in token order
-  for (int t = tid; t < t_shared; t += PERM_THREADS) token_of_row[s_total + t] = t;
+  for (int t = tid; t < t_shared; t += NT) token_of_row[s_total + t] = t;
 }
 
 __global__ void __launch_bounds__(PERM_THREADS, 1)
@@ -128,29 +136,15 @@ __global__ void __launch_bounds__(PERM_THREADS, 1)
                          int* __restrict__ err) {
   griddep_wait();
   griddep_launch_dependents();
-  permute_cta(idx, T, k, E, t_shared, counts, offsets, row_of_assign, token_of_row, err);
-}
-
-template <int VPL>
-__global__ void __launch_bounds__(PERM_THREADS, 1)
-    route_permute_kernel(const float* __restrict__ logits, int T, int k, int E, int t_shared,
-                         int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ counts,
-                         int32_t* __restrict__ offsets, int32_t* __restrict__ row_of_assign,
-                         int32_t* __restrict__ token_of_row, int* __restrict__ err) {
-  griddep_wait();
-  griddep_launch_dependents();
-  for (int tok = threadIdx.x >> 5; tok < T; tok += PERM_WARPS)
-    route_one_token<VPL>(logits, tok, E, k, idx, w, threadIdx.x & 31);
-  __syncthreads();   // the block's global writes of idx are visible to it after the barrier
-  permute_cta(idx, T, k, E, t_shared, counts, offsets, row_of_assign, token_of_row, err);
+  permute_cta<PERM_THREADS>(idx, T, k, E, t_shared, counts, offsets, row_of_assign, token_of_row, err);
 }
 
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ token_of_row,
                                                           int rows, int T, int d,
                                                           uint16_t* __restrict__ x_perm) {
-  griddep_wait();
   griddep_launch_dependents();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int nvec = d / 8;   // 16-byte vectors per row
   for (int r = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); r < rows;
@@ -179,8 +173,8 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
 __global__ void __launch_bounds__(256)
     gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ token_of_row,
                            int rows, int T, int d, uint16_t* __restrict__ x_perm) {
-  griddep_wait();
   griddep_launch_dependents();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int nvec = d / 8;
   for (int r = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); r < rows;
@@ -203,88 +197,172 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// Same gather for the int4 decode GEMM, whose B operand is e4m3: each row r
-// is scaled by a power of two 2^e_r (its largest magnitude lands in
-// [128, 256)) and split into hi = e4m3(x 2^e) and lo = e4m3(x 2^e - hi),
-// which together hold a bf16 value exactly.  Within every 8-element block the
-// elements are stored in the order {0,4,1,5,2,6,3,7}, the K order in which
-// the GEMM unpacks the weight nibbles.  Writes xq [2*rows][d] (hi rows, then
-// lo rows), xs [d/128][rows] (per-group sums of hi + lo) and xe [rows] (2^-e).
-// One 128-thread block per row; a half-warp covers one 128-element group.
+// The int4 decode GEMM's B operand is e4m3: each gathered row r is scaled by
+// a power of two 2^e_r (its largest magnitude lands in [128, 256)) and split
+// into hi = e4m3(x 2^e) and lo = e4m3(x 2^e - hi), which together hold a bf16
+// value exactly.  Within every 8-element block the elements are stored in the
+// order {0,4,1,5,2,6,3,7}, the K order in which the GEMM unpacks the weight
+// nibbles.  Writes xq [2*rows][d] (hi rows, then lo rows), xs [d/128][rows]
+// (per-group sums of hi + lo) and xe [rows] (2^-e).
+// fp8_row: one row by the NT threads of a CTA (src == nullptr: a zero row);
+// a half-warp covers one 128-element group.  red: NT/32 floats of shared memory.
+template <int NT>
+__device__ __forceinline__ void fp8_row(const uint16_t* __restrict__ src, int r, int rows, int d,
+                                        uint8_t* __restrict__ xq, float* __restrict__ xs,
+                                        float* __restrict__ xe, float* red) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nvec = d / 8;   // 8-element blocks per row (a multiple of 16)
+  const uint4* vsrc = reinterpret_cast<const uint4*>(src);
+  uint4 first = make_uint4(0, 0, 0, 0);   // the thread's first block, kept for the second pass
+  float m = 0.f;
+  if (src != nullptr)
+    for (int i = threadIdx.x; i < nvec; i += NT) {
+      const uint4 v = __ldg(vsrc + i);
+      if (i == (int)threadIdx.x) first = v;
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+    }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  m = red[0];
+#pragma unroll
+  for (int i = 1; i < NW; ++i) m = fmaxf(m, red[i]);
+  __syncthreads();   // red is rewritten for the next row
+  int ex = 0;
+  if (m > 0.f) frexpf(m, &ex);               // m = f * 2^ex, f in [0.5, 1)
+  int sc = m > 0.f ? 8 - ex : 0;             // m * 2^sc in [128, 256)
+  sc = max(-126, min(127, sc));
+  const float mul = __int_as_float((127 + sc) << 23);
+  const float inv = __int_as_float((127 - sc) << 23);
+  uint8_t* hi_row = xq + (size_t)r * d;
+  uint8_t* lo_row = xq + ((size_t)rows + r) * d;
+  for (int base = 0; base < nvec; base += NT) {   // every thread runs every iteration
+    const int i = base + threadIdx.x;
+    const bool act = i < nvec;   // nvec % 16 == 0: whole half-warps
+    float sum = 0.f;
+    if (act) {
+      float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (src != nullptr) {
+        const uint4 v = base == 0 ? first : __ldg(vsrc + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          f[2 * j] = __uint_as_float(w[j] << 16) * mul;
+          f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u) * mul;
+        }
+      }
+      constexpr int PERM[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+      uint32_t hw[2] = {0u, 0u}, lw[2] = {0u, 0u};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float a = f[PERM[2 * q]], b = f[PERM[2 * q + 1]];
+        const uint16_t h = f32x2_to_e4m3x2(a, b);
+        const float2 hf = e4m3x2_to_f32x2(h);
+        const uint16_t l = f32x2_to_e4m3x2(a - hf.x, b - hf.y);
+        const float2 lf = e4m3x2_to_f32x2(l);
+        sum += (hf.x + lf.x) + (hf.y + lf.y);
+        hw[q >> 1] |= (uint32_t)h << (16 * (q & 1));
+        lw[q >> 1] |= (uint32_t)l << (16 * (q & 1));
+      }
+      *reinterpret_cast<uint2*>(hi_row + (size_t)i * 8) = make_uint2(hw[0], hw[1]);
+      *reinterpret_cast<uint2*>(lo_row + (size_t)i * 8) = make_uint2(lw[0], lw[1]);
+    }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (act && (lane & 15) == 0) xs[(size_t)(i >> 4) * rows + r] = sum;
+  }
+  if (threadIdx.x == 0) xe[r] = inv;
+}
+
+// One 128-thread block per row.
 constexpr int FP8_GATHER_THREADS = 128;
 __global__ void __launch_bounds__(FP8_GATHER_THREADS)
     gather_rows_fp8_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ token_of_row,
                            int rows, int T, int d, uint8_t* __restrict__ xq, float* __restrict__ xs,
                            float* __restrict__ xe) {
-  griddep_wait();
   griddep_launch_dependents();
-  __shared__ float wmax[FP8_GATHER_THREADS / 32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nvec = d / 8;   // 8-element blocks per row (a multiple of 16)
+  griddep_wait();
+  __shared__ float red[FP8_GATHER_THREADS / 32];
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const int t = token_of_row != nullptr ? token_of_row[r] : r;
     const bool valid = (t >= 0 && t < T);
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(valid ? t : 0) * d);
-    float m = 0.f;
-    if (valid)
-      for (int i = threadIdx.x; i < nvec; i += FP8_GATHER_THREADS) {
-        const uint4 v = __ldg(src + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+    fp8_row<FP8_GATHER_THREADS>(valid ? x + (size_t)t * d : nullptr, r, rows, d, xq, xs, xe, red);
+  }
+}
+
+// x_perm row = x row (bf16 copy, or saturating fp16 conversion), by the NT
+// threads of a CTA; src == nullptr: a zero row.
+template <int NT, bool F16>
+__device__ __forceinline__ void copy_row(const uint16_t* __restrict__ src, int d, uint16_t* __restrict__ dst) {
+  const uint4* vs = reinterpret_cast<const uint4*>(src);
+  uint4* vd = reinterpret_cast<uint4*>(dst);
+  for (int i = threadIdx.x; i < d / 8; i += NT) {
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if (src != nullptr) {
+      o = __ldg(vs + i);
+      if (F16) {
+        o.x = bf16x2_to_f16x2(o.x);
+        o.y = bf16x2_to_f16x2(o.y);
+        o.z = bf16x2_to_f16x2(o.z);
+        o.w = bf16x2_to_f16x2(o.w);
       }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if (lane == 0) wmax[warp] = m;
-    __syncthreads();
-    m = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
-    __syncthreads();   // wmax is rewritten for the next row
-    int ex = 0;
-    if (m > 0.f) frexpf(m, &ex);               // m = f * 2^ex, f in [0.5, 1)
-    int sc = m > 0.f ? 8 - ex : 0;             // m * 2^sc in [128, 256)
-    sc = max(-126, min(127, sc));
-    const float mul = __int_as_float((127 + sc) << 23);
-    const float inv = __int_as_float((127 - sc) << 23);
-    uint8_t* hi_row = xq + (size_t)r * d;
-    uint8_t* lo_row = xq + ((size_t)rows + r) * d;
-    for (int base = 0; base < nvec; base += FP8_GATHER_THREADS) {   // every thread runs every iteration
-      const int i = base + threadIdx.x;
-      const bool act = i < nvec;   // nvec % 16 == 0: whole half-warps
-      float sum = 0.f;
-      if (act) {
-        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (valid) {
-          const uint4 v = __ldg(src + i);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            f[2 * j] = __uint_as_float(w[j] << 16) * mul;
-            f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u) * mul;
-          }
-        }
-        // element order within the block: {0,4,1,5,2,6,3,7}
-        constexpr int PERM[8] = {0, 4, 1, 5, 2, 6, 3, 7};
-        uint32_t hw[2] = {0u, 0u}, lw[2] = {0u, 0u};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float a = f[PERM[2 * q]], b = f[PERM[2 * q + 1]];
-          const uint16_t h = f32x2_to_e4m3x2(a, b);
-          const float2 hf = e4m3x2_to_f32x2(h);
-          const uint16_t l = f32x2_to_e4m3x2(a - hf.x, b - hf.y);
-          const float2 lf = e4m3x2_to_f32x2(l);
-          sum += (hf.x + lf.x) + (hf.y + lf.y);
-          hw[q >> 1] |= (uint32_t)h << (16 * (q & 1));
-          lw[q >> 1] |= (uint32_t)l << (16 * (q & 1));
-        }
-        *reinterpret_cast<uint2*>(hi_row + (size_t)i * 8) = make_uint2(hw[0], hw[1]);
-        *reinterpret_cast<uint2*>(lo_row + (size_t)i * 8) = make_uint2(lw[0], lw[1]);
-      }
-#pragma unroll
-      for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      if (act && (lane & 15) == 0) xs[(size_t)(i >> 4) * rows + r] = sum;
     }
-    if (threadIdx.x == 0) xe[r] = inv;
+    vd[i] = o;
+  }
+}
+
+// ------------------------------------------------------------------ fused
+constexpr int RG_THREADS = 512;
+constexpr int RG_MAX_A = FUSED_ROUTE_MAX_T * 16;            // T * k, k <= 16
+constexpr int RG_MAX_ROWS = RG_MAX_A + FUSED_ROUTE_MAX_T;   // + the shared expert's rows
+
+template <int VPL, int OUT>
+__global__ void __launch_bounds__(RG_THREADS, 1)
+    route_gather_kernel(const float* __restrict__ logits, int T, int k, int E, int t_shared,
+                        const uint16_t* __restrict__ x, int d, int32_t* __restrict__ idx,
+                        float* __restrict__ w, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ row_of_assign, int32_t* __restrict__ token_of_row,
+                        int* __restrict__ err, GatherDst dst) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ int32_t s_idx[RG_MAX_A];
+  __shared__ float s_w[RG_MAX_A];
+  __shared__ int32_t s_roa[RG_MAX_A];
+  __shared__ int32_t s_tor[RG_MAX_ROWS];
+  __shared__ int32_t s_counts[PERM_MAX_E];
+  __shared__ int32_t s_offsets[PERM_MAX_E + 2];
+  __shared__ float s_red[RG_THREADS / 32];
+  const int A = T * k, rows = A + t_shared;
+  const bool lead = blockIdx.x == 0;
+  for (int i = threadIdx.x; i < rows; i += RG_THREADS) s_tor[i] = -1;   // rows of bad ids stay -1
+  for (int tok = threadIdx.x >> 5; tok < T; tok += RG_THREADS / 32)
+    route_one_token<VPL>(logits, tok, E, k, s_idx, s_w, threadIdx.x & 31);
+  __syncthreads();
+  permute_cta<RG_THREADS>(s_idx, T, k, E, t_shared, s_counts, s_offsets, s_roa, s_tor,
+                          lead ? err : nullptr);
+  __syncthreads();
+  if (lead) {
+    for (int i = threadIdx.x; i < A; i += RG_THREADS) {
+      idx[i] = s_idx[i];
+      w[i] = s_w[i];
+      row_of_assign[i] = s_roa[i];
+    }
+    for (int i = threadIdx.x; i < rows; i += RG_THREADS) token_of_row[i] = s_tor[i];
+    for (int i = threadIdx.x; i < E; i += RG_THREADS) counts[i] = s_counts[i];
+    for (int i = threadIdx.x; i <= E + (t_shared > 0 ? 1 : 0); i += RG_THREADS) offsets[i] = s_offsets[i];
+  }
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const int t = s_tor[r];
+    const uint16_t* src = (t >= 0 && t < T) ? x + (size_t)t * d : nullptr;
+    if (OUT == GATHER_FP8)
+      fp8_row<RG_THREADS>(src, r, rows, d, dst.xq, dst.xs, dst.xe, s_red);
+    else
+      copy_row<RG_THREADS, OUT == GATHER_F16>(src, d, dst.x16 + (size_t)r * d);
   }
 }
 
@@ -295,21 +373,40 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_
                        t_shared, counts, offsets, row_of_assign, token_of_row, err);
 }
 
-cudaError_t launch_route_permute(const float* logits, int T, int k, int E, int t_shared, int32_t* idx,
-                                 float* w, int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
-                                 int32_t* token_of_row, int* err, cudaStream_t s, bool pdl) {
-  const dim3 g(1), b(PERM_THREADS);
+template <int VPL>
+static cudaError_t launch_route_gather_vpl(int out, dim3 g, cudaStream_t s, bool pdl, const float* logits,
+                                           int T, int k, int E, int t_shared, const uint16_t* x, int d,
+                                           int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
+                                           int32_t* roa, int32_t* tor, int* err, const GatherDst& dst) {
+  const dim3 b(RG_THREADS);
+  if (out == GATHER_FP8)
+    return launch_kernel(route_gather_kernel<VPL, GATHER_FP8>, g, b, 0, s, pdl, logits, T, k, E, t_shared,
+                         x, d, idx, w, counts, offsets, roa, tor, err, dst);
+  if (out == GATHER_F16)
+    return launch_kernel(route_gather_kernel<VPL, GATHER_F16>, g, b, 0, s, pdl, logits, T, k, E, t_shared,
+                         x, d, idx, w, counts, offsets, roa, tor, err, dst);
+  return launch_kernel(route_gather_kernel<VPL, GATHER_BF16>, g, b, 0, s, pdl, logits, T, k, E, t_shared,
+                       x, d, idx, w, counts, offsets, roa, tor, err, dst);
+}
+
+cudaError_t launch_route_gather(const float* logits, int T, int k, int E, int t_shared, const uint16_t* x,
+                                int d, int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
+                                int32_t* row_of_assign, int32_t* token_of_row, int* err, int out,
+                                const GatherDst& dst, int n_sm, cudaStream_t s, bool pdl) {
+  if (T < 1 || T > FUSED_ROUTE_MAX_T || k < 1 || k > 16 || E < 1 || E > PERM_MAX_E) return cudaErrorInvalidValue;
+  const int rows = T * k + t_shared;
+  const dim3 g((unsigned)(rows < n_sm ? rows : n_sm));
   if (E <= 32)
-    return launch_kernel(route_permute_kernel<1>, g, b, 0, s, pdl, logits, T, k, E, t_shared, idx, w,
-                         counts, offsets, row_of_assign, token_of_row, err);
+    return launch_route_gather_vpl<1>(out, g, s, pdl, logits, T, k, E, t_shared, x, d, idx, w, counts,
+                                      offsets, row_of_assign, token_of_row, err, dst);
   if (E <= 64)
-    return launch_kernel(route_permute_kernel<2>, g, b, 0, s, pdl, logits, T, k, E, t_shared, idx, w,
-                         counts, offsets, row_of_assign, token_of_row, err);
+    return launch_route_gather_vpl<2>(out, g, s, pdl, logits, T, k, E, t_shared, x, d, idx, w, counts,
+                                      offsets, row_of_assign, token_of_row, err, dst);
   if (E <= 128)
-    return launch_kernel(route_permute_kernel<4>, g, b, 0, s, pdl, logits, T, k, E, t_shared, idx, w,
-                         counts, offsets, row_of_assign, token_of_row, err);
-  return launch_kernel(route_permute_kernel<8>, g, b, 0, s, pdl, logits, T, k, E, t_shared, idx, w,
-                       counts, offsets, row_of_assign, token_of_row, err);
+    return launch_route_gather_vpl<4>(out, g, s, pdl, logits, T, k, E, t_shared, x, d, idx, w, counts,
+                                      offsets, row_of_assign, token_of_row, err, dst);
+  return launch_route_gather_vpl<8>(out, g, s, pdl, logits, T, k, E, t_shared, x, d, idx, w, counts,
+                                    offsets, row_of_assign, token_of_row, err, dst);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
