@@ -16,11 +16,13 @@
 //   * the B operand is the token rows in e4m3 too, each row scaled by a power
 //     of two and split into hi + lo parts that hold a bf16 value exactly (the
 //     gather kernel and this kernel's gate/up epilogue write them); the hi
-//     and lo tiles go through two MMAs into the same accumulator;
+//     tile and the lo tile below it form one B operand of 2 x bn rows, so
+//     one MMA per K step and matrix covers both, and the fold adds the hi and
+//     lo columns of the accumulator;
 //   * the MMA is tcgen05.mma kind::f8f6f4 (K = 32), A from TMEM;
 //   * each quantisation group (K = 128) accumulates into its own TMEM slice,
 //     folded into fp32 registers with the group's scale s and zero z:
-//         acc += s * (2^9 * D - z * S),
+//         acc += s * (2^9 * (D_hi + D_lo) - z * S),
 //     S the group's sum of the (scaled) token row; the token row's scale is
 //     undone at the end (gate/up) or per group (down, where h is scaled per
 //     128-feature block);
@@ -169,9 +171,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   constexpr uint32_t A_COLS = NMAT * 32;               // TMEM columns of one A slot (128 e4m3 per row)
   constexpr uint32_t B_BOX = (uint32_t)GBN * 128u;     // one TMA box: GBN rows x 128 bytes
   constexpr uint32_t B_STAGE = 2u * B_BOX;             // hi rows, then lo rows
-  constexpr int NBUF = 4;                              // accumulator slices
   constexpr int NA = 3;                                // A slots
-  constexpr uint32_t SLICE = NMAT * GBN;               // TMEM columns of one accumulator slice
+  constexpr uint32_t SLICE = NMAT * 2 * GBN;           // TMEM columns of one accumulator slice (hi, lo)
+  constexpr int NBUF = (512 - NA * (int)A_COLS) / (int)SLICE < G_MAX_NBUF
+                           ? (512 - NA * (int)A_COLS) / (int)SLICE
+                           : G_MAX_NBUF;               // accumulator slices
   static_assert(NA * (int)A_COLS + NBUF * (int)SLICE <= 512, "tensor memory columns");
   const int n_st = p.n_raw;
 
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     bool ok = true;
     Ring rs{0, 0, n_st}, ra{0, 0, NA}, rc{0, 0, NBUF};
     const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(S.b_ring));   // stage 0, K step 0
-    const uint32_t idesc = idesc_f16kind_f32(TILE_M, (uint32_t)GBN, 0u);   // e4m3 x e4m3 -> f32
+    const uint32_t idesc = idesc_f16kind_f32(TILE_M, (uint32_t)(2 * GBN), 0u);   // e4m3 x e4m3 -> f32
     uint32_t gc = 0;
     for (int ii = 0; ii < n_mine && ok; ++ii) {
       const ItemDesc it = get_item(ii, p, S);
@@ -311,11 +315,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         const uint32_t a_base = tmem_base + (uint32_t)ra.i * A_COLS;
         const uint32_t d0 = tmem_base + acc0 + (uint32_t)rc.i * SLICE;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {   // K steps of 32: hi tile, then the same steps on the lo tile
-          const uint64_t bq = bd + (uint64_t)(((q >> 2) * B_BOX + (q & 3) * 32) >> 4);
-          const uint32_t ak = a_base + (uint32_t)((q & 3) * 8);
+        for (int q = 0; q < 4; ++q) {   // K steps of 32 over the hi and lo rows at once
+          const uint64_t bq = bd + (uint64_t)((q * 32) >> 4);
+          const uint32_t ak = a_base + (uint32_t)(q * 8);
           if (NMAT == 2)
-            mma2_f8_ta_elect(d0, d0 + GBN, ak, ak + 32, bq, idesc, q > 0 ? 1u : 0u);
+            mma2_f8_ta_elect(d0, d0 + 2 * GBN, ak, ak + 32, bq, idesc, q > 0 ? 1u : 0u);
           else
             mma_f8_ta_elect(d0, ak, bq, idesc, q > 0 ? 1u : 0u);
         }
@@ -436,11 +440,17 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 #pragma unroll
         for (int ch = 0; ch < CW / CH; ++ch) {
           if (ch * CH < nc) {
-            uint32_t dv[NMAT][CH];
+            uint32_t dv[NMAT][CH], dl[NMAT][CH];   // hi and lo columns
 #pragma unroll
             for (int m = 0; m < NMAT; ++m) {
-              if (CH == 16) tmem_ld_16(ta + (uint32_t)(m * GBN + c0 + ch * CH), *reinterpret_cast<uint32_t(*)[16]>(dv[m]));
-              else tmem_ld_8(ta + (uint32_t)(m * GBN + c0 + ch * CH), *reinterpret_cast<uint32_t(*)[8]>(dv[m]));
+              const uint32_t col = ta + (uint32_t)(m * 2 * GBN + c0 + ch * CH);
+              if (CH == 16) {
+                tmem_ld_16(col, *reinterpret_cast<uint32_t(*)[16]>(dv[m]));
+                tmem_ld_16(col + GBN, *reinterpret_cast<uint32_t(*)[16]>(dl[m]));
+              } else {
+                tmem_ld_8(col, *reinterpret_cast<uint32_t(*)[8]>(dv[m]));
+                tmem_ld_8(col + GBN, *reinterpret_cast<uint32_t(*)[8]>(dl[m]));
+              }
             }
             // token factors (shared by the matrices) while the loads are in flight
             float bs[CH], bu[CH];
@@ -453,11 +463,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 #pragma unroll
             for (int m = 0; m < NMAT; ++m) {
               tmem_ld_wait_regs(dv[m]);
+              tmem_ld_wait_regs(dl[m]);
 #pragma unroll
               for (int i = 0; i < CH; ++i) {
                 const int n = ch * CH + i;
                 const float sd = GATEUP ? s9[m] : s9[m] * bu[i];
-                acc[m][n] = fmaf(sd, __uint_as_float(dv[m][i]), fmaf(-sz[m], bs[i], acc[m][n]));
+                const float dsum = __uint_as_float(dv[m][i]) + __uint_as_float(dl[m][i]);
+                acc[m][n] = fmaf(sd, dsum, fmaf(-sz[m], bs[i], acc[m][n]));
               }
             }
           }
