@@ -58,7 +58,7 @@ using namespace gemm;
 namespace {
 
 constexpr int G_MAX_NBUF = 4;   // accumulator slices (fewer where TMEM is short)
-constexpr int G_MAX_NA = 3;     // A slots in tensor memory
+constexpr int G_MAX_NA = 4;     // A slots in tensor memory
 constexpr int G_MISC = 8;       // [0] tmem [1] abort [2] items [3] stages issued [4] stays 0
 constexpr int G_NMMA = 2;       // MMA-issuing warps (alternate groups)
 constexpr int G_NUP = 8;        // unpack warps
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   constexpr uint32_t A_COLS = NMAT * 32;               // TMEM columns of one A slot (128 e4m3 per row)
   constexpr uint32_t B_BOX = (uint32_t)GBN * 128u;     // one TMA box: GBN rows x 128 bytes
   constexpr uint32_t B_STAGE = 2u * B_BOX;             // hi rows, then lo rows
-  constexpr int NA = 3;                                // A slots
+  constexpr int NA = G_MAX_NA;                         // A slots
   constexpr uint32_t SLICE = NMAT * 2 * GBN;           // TMEM columns of one accumulator slice (hi, lo)
   constexpr int NBUF = (512 - NA * (int)A_COLS) / (int)SLICE < G_MAX_NBUF
                            ? (512 - NA * (int)A_COLS) / (int)SLICE
@@ -394,17 +394,20 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     }
   } else {
     // ================================================================ fold + epilogue
-    // One warp per TMEM lane quadrant; each thread owns weight row r of every
-    // matrix and all the item's token columns.  Group gc: wait for its
-    // accumulator slice, fold it with the group's scale and zero (read from
-    // the stage, which this warp releases afterwards) and the token rows'
-    // group sums, free the slice.
+    // Two warps per TMEM lane quadrant; each thread owns weight row r of every
+    // matrix and half the item's token columns (the SwiGLU epilogue needs gate
+    // and up of a token together; for the paired down GEMM a split by output
+    // tile measured slower).  Group gc: wait for its accumulator slice, fold
+    // it with the group's scale and zero (read from the stage, which this warp
+    // releases afterwards) and the token rows' group sums, free the slice.
+    constexpr int NM = NMAT;                           // matrices per fold warp
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int c0 = ((warp - G_FOLD0) >> 2) * (GBN / 2);   // my token columns [c0, c0 + GBN/2)
+    const int m0 = 0;                                  // my first matrix
+    const int c0 = ((warp - G_FOLD0) >> 2) * (GBN / 2);   // my token columns [c0, c0 + CW)
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
     constexpr int CW = GBN / 2;                        // token columns per fold thread
-    constexpr int CH = CW >= 16 ? 16 : 8;              // columns per tcgen05.ld (and per chunk)
+    constexpr int CH = 8;                              // columns per tcgen05.ld (and per chunk)
     Ring rs{0, 0, n_st}, rc{0, 0, NBUF};
     uint32_t it_count = 0;
     bool ok = true;
@@ -413,19 +416,19 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       if (!it.slot) continue;
       const int g0 = it.g0, g1 = it.g1;
       const int nc = max(0, min(CW, it.n_rows - c0));   // my token columns of this item
-      float acc[NMAT][CW];
+      float acc[NM][CW];
 #pragma unroll
-      for (int m = 0; m < NMAT; ++m)
+      for (int m = 0; m < NM; ++m)
 #pragma unroll
         for (int i = 0; i < CW; ++i) acc[m][i] = 0.f;
       for (int kg = g0; kg < g1 && ok; ++kg) {
         if (!(ok = wait_all(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err))) break;
         const uint8_t* raw = S.raw_ring + (size_t)rs.i * RAW_STAGE;
         // per matrix: 2^9 s (the codes are q 2^-9) and s z
-        float s9[NMAT], sz[NMAT];
+        float s9[NM], sz[NM];
 #pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(raw + m * I4_MAT_BYTES + I4_PACKED_BYTES + r * 4);
+        for (int m = 0; m < NM; ++m) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(raw + (m0 + m) * I4_MAT_BYTES + I4_PACKED_BYTES + r * 4);
           const float sc = __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
           s9[m] = 512.f * sc;
           sz[m] = sc * __half2float(__ushort_as_half((unsigned short)(w >> 16)));
@@ -440,10 +443,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 #pragma unroll
         for (int ch = 0; ch < CW / CH; ++ch) {
           if (ch * CH < nc) {
-            uint32_t dv[NMAT][CH], dl[NMAT][CH];   // hi and lo columns
+            uint32_t dv[NM][CH], dl[NM][CH];   // hi and lo columns
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m) {
-              const uint32_t col = ta + (uint32_t)(m * 2 * GBN + c0 + ch * CH);
+            for (int m = 0; m < NM; ++m) {
+              const uint32_t col = ta + (uint32_t)((m0 + m) * 2 * GBN + c0 + ch * CH);
               if (CH == 16) {
                 tmem_ld_16(col, *reinterpret_cast<uint32_t(*)[16]>(dv[m]));
                 tmem_ld_16(col + GBN, *reinterpret_cast<uint32_t(*)[16]>(dl[m]));
@@ -461,7 +464,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
               bs[i] = u * bsum[(ch * CH + i) * (ESZ / 4)];
             }
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m) {
+            for (int m = 0; m < NM; ++m) {
               tmem_ld_wait_regs(dv[m]);
               tmem_ld_wait_regs(dl[m]);
 #pragma unroll
@@ -483,7 +486,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       if (!ok) break;
 
       // ---- item epilogue from the register accumulators
-      if (GATEUP) {
+      if constexpr (GATEUP) {
         // h = silu(gate) * up for my feature row, then its e4m3 hi/lo form for
         // the down GEMM: per token, a power-of-two scale from the largest |h|
         // over the tile's 128 features, the two bytes, and the sum of hi + lo
@@ -547,8 +550,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       } else {
         float* y = reinterpret_cast<float*>(p.out) + (size_t)it.ks * p.out_split_stride;
 #pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-          const int f = (MODE == G_DOWN_PAIR ? 2 * it.mt + m : it.mt) * TILE_M + r;
+        for (int m = 0; m < NM; ++m) {
+          const int f = (MODE == G_DOWN_PAIR ? 2 * it.mt + m0 + m : it.mt) * TILE_M + r;
 #pragma unroll
           for (int i = 0; i < CW; ++i)
             if (i < nc) y[(size_t)(it.r0 + c0 + i) * p.out_ld + f] = acc[m][i];

@@ -9,7 +9,11 @@ import moe_expert_layer_03_gb300 as moe
 import moe_synth as ms
 import oracle
 
-TOL = 2e-2   # max|err| <= TOL * RMS(out) for bf16 activations with fp32 accumulation
+# max|err| <= TOL * RMS(out) for bf16 activations with fp32 accumulation; an element
+# whose one bf16 ulp exceeds that (|v| above ~2.5-5 RMS) may instead differ from the
+# exact value by at most one ulp: a bf16 output cannot be closer than half an ulp,
+# and the fp32 sum before its rounding may fall on either side of the midpoint.
+TOL = 2e-2
 
 
 class GpuLayer:
@@ -62,11 +66,20 @@ class GpuLayer:
         return out
 
 
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |v| (8 significant bits; normal range)."""
+    a = np.maximum(np.abs(np.asarray(v, np.float64)), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(a)) - 7)
+
+
 def assert_close_rms(got: np.ndarray, want: np.ndarray, tol: float = TOL, what: str = ""):
     got = np.asarray(got, np.float64)
     want = np.asarray(want, np.float64)
     rms = float(np.sqrt(np.mean(want ** 2)))
-    err = float(np.max(np.abs(got - want)))
+    e = np.abs(got - want)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
-    assert err <= tol * rms, f"{what}: max|err| {err:.4e} > {tol} * RMS {rms:.4e}"
-    return err, rms
+    allowed = np.maximum(tol * rms, bf16_ulp(want))
+    i = np.unravel_index(np.argmax(e / allowed), e.shape)
+    assert np.all(e <= allowed), (f"{what}: |err| {e[i]:.4e} at {i} > max({tol} * RMS {rms:.4e}, "
+                                  f"1 bf16 ulp {bf16_ulp(want[i]):.4e})")
+    return float(e.max()), rms

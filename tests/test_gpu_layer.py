@@ -35,6 +35,13 @@ SMALL = {
     "int4_wide_odd": ms.LayerConfig("int4_wide_odd", T=96, d=384, F=512, E=4, k=2, fmt="int4", seed=7),
     # row chunks of 192, the widest int4 chunk
     "int4_wide192": ms.LayerConfig("int4_wide192", T=200, d=256, F=384, E=2, k=1, fmt="int4", seed=8),
+    # the one-launch routing + gather at its limits: 64 tokens, k = 16, a shared
+    # expert (1088 rows, more than one per CTA), fp16 rows for the int4 prefill kernel
+    "fused_route_max": ms.LayerConfig("fused_route_max", T=64, d=256, F=256, E=16, k=16, fmt="int4",
+                                      shared=True, seed=10),
+    # the same launch writing bf16 rows, k < E
+    "fused_route_bf16": ms.LayerConfig("fused_route_bf16", T=64, d=256, F=256, E=32, k=6, fmt="bf16",
+                                       seed=11),
 }
 
 

@@ -339,3 +339,16 @@ def test_combine_row_hand_values():
     assert out.tolist() == [1.75, 2.5, 0.3125]
     out = oracle.combine_row([one, two], [0.25, 0.75], sh)
     assert out.tolist() == [2.25, 3.0, 0.8125]
+
+
+def test_bf16_ulp_helper_matches_torch_spacing():
+    """The parity tests' one-ulp allowance uses the spacing of bf16 numbers: check it
+    against torch's bf16 rounding (the next representable value up)."""
+    from layer_setup import bf16_ulp
+    rng = np.random.default_rng(21)
+    v = (rng.standard_normal(2000) * np.exp2(rng.integers(-20, 20, 2000))).astype(np.float32)
+    b = torch.from_numpy(v).to(torch.bfloat16)
+    bits = b.view(torch.int16).numpy().view(np.uint16).astype(np.int32)
+    nxt = torch.from_numpy(((bits + 1) & 0xFFFF).astype(np.uint16).view(np.int16)).view(torch.bfloat16)
+    spacing = np.abs(nxt.double().numpy() - b.double().numpy())
+    np.testing.assert_array_equal(bf16_ulp(b.double().numpy()), spacing)
