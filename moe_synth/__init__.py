@@ -52,7 +52,7 @@ class LayerConfig:
     F: int
     E: int
     k: int
-    fmt: str                  # "bf16" or "int4"
+    fmt: str                  # "bf16", "int4" or "fp8"
     logits: str = "normal"    # "normal" | "zipf" | "reuse"
     zipf_s: float = 1.0
     reuse_p: float = 0.44
@@ -201,14 +201,39 @@ def quantize_int4_g128(w: torch.Tensor) -> dict[str, torch.Tensor]:
     return {"q": packed, "scale": s.contiguous(), "zero": z.to(torch.float16).contiguous()}
 
 
+E4M3_MAX = 448.0
+
+
+def quantize_fp8_g128(w: torch.Tensor) -> dict[str, torch.Tensor]:
+    """Offline 8-bit encoding of a bf16 weight matrix [rows, K] (K % 128 == 0):
+    OCP fp8 E4M3 codes with one fp16 scale per row and group of 128 K elements,
+    symmetric (no zero point):
+        s = fp16(max(amax, 1e-8) / 448)            (amax = largest |v| of the group)
+        q = e4m3(clamp(v / s, -448, 448))           (round to nearest even, fp32)
+    Returns {"q": uint8 [rows, K] (the E4M3 bit patterns), "scale": fp16 [rows, K/128]}.
+    """
+    rows, K = w.shape
+    assert K % GROUP == 0
+    v = w.to(torch.float32).reshape(rows, K // GROUP, GROUP)
+    amax = v.abs().amax(dim=2)
+    s = (torch.clamp(amax, min=1e-8) / E4M3_MAX).to(torch.float16)
+    s = torch.where(s > 0, s, torch.full_like(s, 2.0 ** -24))   # a scale that underflowed fp16
+    r = torch.clamp(v / s.to(torch.float32).unsqueeze(2), -E4M3_MAX, E4M3_MAX)
+    q = r.to(torch.float8_e4m3fn).view(torch.uint8).reshape(rows, K)
+    return {"q": q.contiguous(), "scale": s.contiguous()}
+
+
 def expert_weights(cfg: LayerConfig, e: int | str, device="cpu") -> dict[str, dict[str, torch.Tensor]]:
     """The weights the layer consumes for expert e, in the canonical formats:
     bf16: {"gate": {"w": bf16 [F,d]}, "up": ..., "down": {"w": bf16 [d,F]}}
     int4: {"gate": {"q","scale","zero"}, ...}   (see quantize_int4_g128)
+    fp8:  {"gate": {"q","scale"}, ...}          (see quantize_fp8_g128)
     """
     src = expert_source(cfg, e, device)
     if cfg.fmt == "bf16":
         return {m: {"w": src[m]} for m in MATS}
+    if cfg.fmt == "fp8":
+        return {m: quantize_fp8_g128(src[m]) for m in MATS}
     return {m: quantize_int4_g128(src[m]) for m in MATS}
 
 
@@ -216,4 +241,6 @@ def active_expert_bytes(cfg: LayerConfig) -> int:
     """Bytes of one expert's weights in the layer's storage format (algorithmic)."""
     if cfg.fmt == "bf16":
         return 3 * cfg.d * cfg.F * 2
+    if cfg.fmt == "fp8":   # one byte per weight + one fp16 scale per row and group
+        return 3 * cfg.d * cfg.F + 3 * cfg.F * (cfg.d // GROUP) * 2
     return 3 * cfg.d * cfg.F // 2 + 3 * cfg.F * (cfg.d // GROUP) * 4

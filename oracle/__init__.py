@@ -55,6 +55,8 @@ def lib():
             L.oracle_bf16_to_double.argtypes = [C.c_uint16]
             L.oracle_fp16_to_double.restype = C.c_double
             L.oracle_fp16_to_double.argtypes = [C.c_uint16]
+            L.oracle_e4m3_to_double.restype = C.c_double
+            L.oracle_e4m3_to_double.argtypes = [C.c_uint8]
             L.oracle_weight.restype = C.c_double
             L.oracle_weight.argtypes = [C.POINTER(Matrix), C.c_int, C.c_int]
             L.oracle_router_logits.argtypes = [P, P, C.c_int, C.c_int, C.c_int, P]
@@ -99,6 +101,12 @@ class ExpertRef:
                 w = _np(m["w"], np.uint16)
                 self.keep.append(w)
                 mats[name] = Matrix(0, w.shape[0], w.shape[1], _ptr(w).value, None, None, None)
+            elif fmt == "fp8":
+                q = _np(m["q"], np.uint8)
+                s = _np(m["scale"], np.uint16)
+                self.keep += [q, s]
+                mats[name] = Matrix(2, q.shape[0], q.shape[1], None, _ptr(q).value,
+                                    _ptr(s).value, None)
             else:
                 q = _np(m["q"], np.uint8)
                 s = _np(m["scale"], np.uint16)

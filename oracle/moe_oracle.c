@@ -30,12 +30,31 @@ double oracle_fp16_to_double(uint16_t h) {
   return s ? -v : v;
 }
 
+/* OCP 8-bit floating point E4M3: sign, 4 exponent bits (bias 7), 3 mantissa
+ * bits; exponent 0 holds the subnormals m/8 * 2^-6; exponent 15 with mantissa 7
+ * is NaN (the format has no infinities). */
+double oracle_e4m3_to_double(uint8_t b) {
+  int s = (b >> 7) & 1, ex = (b >> 3) & 0xF, man = b & 0x7;
+  double v;
+  if (ex == 15 && man == 7) v = NAN;
+  else if (ex == 0) v = ldexp((double)man, -9);                    /* (m/8) * 2^-6 */
+  else v = ldexp(1.0 + (double)man / 8.0, ex - 7);
+  return s ? -v : v;
+}
+
 /* Dequantised weight [row][col].  int4 group-128 ([Strata] sec. 3.1 per-expert
  * scale and zero-point; [CoInf] sec. 5.1 group quantisation):
  *   w = (q - z) * s, q the nibble of element col (low nibble = even col),
- *   s and z the fp16 scale and zero of group col/128 of that row. */
+ *   s and z the fp16 scale and zero of group col/128 of that row.
+ * 8-bit experts ([CoInf] sec. 5.1: 8-bit quantisation of the expert layers
+ * only, in groups): w = e4m3(q) * s, q the code byte of element col, s the
+ * fp16 scale of group col/128 of that row. */
 double oracle_weight(const oracle_matrix* m, int row, int col) {
   if (m->fmt == ORACLE_W_BF16) return oracle_bf16_to_double(m->w[(size_t)row * m->cols + col]);
+  if (m->fmt == ORACLE_W_FP8_G128) {   /* 8-bit expert weights: w = e4m3(q) * s */
+    double s = oracle_fp16_to_double(m->scale[(size_t)row * (m->cols / 128) + col / 128]);
+    return oracle_e4m3_to_double(m->q[(size_t)row * m->cols + col]) * s;
+  }
   uint8_t byte = m->q[(size_t)row * (m->cols / 2) + col / 2];
   int q = (col & 1) ? (byte >> 4) : (byte & 0xF);
   size_t g = (size_t)row * (m->cols / 128) + col / 128;

@@ -32,15 +32,16 @@
 extern "C" {
 #endif
 
-enum { ORACLE_W_BF16 = 0, ORACLE_W_INT4_G128 = 1 };
+enum { ORACLE_W_BF16 = 0, ORACLE_W_INT4_G128 = 1, ORACLE_W_FP8_G128 = 2 };
 
 /* One weight matrix [rows][cols], cols = K contiguous ("[out][in]"). */
 typedef struct {
-  int fmt;                 /* ORACLE_W_BF16 or ORACLE_W_INT4_G128 */
+  int fmt;                 /* ORACLE_W_BF16, ORACLE_W_INT4_G128 or ORACLE_W_FP8_G128 */
   int rows, cols;
   const uint16_t* w;       /* bf16 [rows][cols]                          (fmt 0) */
-  const uint8_t* q;        /* packed [rows][cols/2]; low nibble = even col (fmt 1) */
-  const uint16_t* scale;   /* fp16 [rows][cols/128]                      (fmt 1) */
+  const uint8_t* q;        /* fmt 1: packed [rows][cols/2], low nibble = even col;
+                              fmt 2: e4m3 codes [rows][cols] */
+  const uint16_t* scale;   /* fp16 [rows][cols/128]                      (fmt 1, 2) */
   const uint16_t* zero;    /* fp16 [rows][cols/128], integer values 0..15 (fmt 1) */
 } oracle_matrix;
 
@@ -52,6 +53,7 @@ typedef struct {
 /* Number helpers (exposed so tests can pin them against independent code). */
 double oracle_bf16_to_double(uint16_t b);
 double oracle_fp16_to_double(uint16_t h);
+double oracle_e4m3_to_double(uint8_t b);   /* OCP fp8 E4M3 (bias 7, no infinities; S.1111.111 = NaN) */
 double oracle_weight(const oracle_matrix* m, int row, int col);   /* dequantised value */
 
 /* Router logits ([CoInf] sec. 2.1 router resident on the GPU; sec. 5.1 router

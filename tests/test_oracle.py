@@ -5,6 +5,7 @@ derived by hand (tests/golden), closed forms, invariants, brute force on tiny
 inputs, or a special case that reduces to a library routine (numpy matmul,
 torch's bf16 conversion).
 """
+import ctypes as C
 import math
 import os
 
@@ -44,6 +45,72 @@ def test_fp16_decode_all_patterns():
     assert np.array_equal(got[finite], want[finite])
     assert np.array_equal(np.isnan(got), np.isnan(want))
     assert np.array_equal(np.isinf(got), np.isinf(want))
+
+
+# ----------------------------------------------------------------------------- fp8 (E4M3)
+def test_e4m3_decode_all_patterns_match_torch():
+    """All 256 E4M3 codes against torch's float8_e4m3fn (an independent decoder)."""
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.lib().oracle_e4m3_to_double(int(c)) for c in codes])
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2      # S.1111.111 only
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def _fp8_matrix(q: np.ndarray, s_bits: np.ndarray):
+    q = np.ascontiguousarray(q, np.uint8)
+    s_bits = np.ascontiguousarray(s_bits, np.uint16)
+    m = oracle.Matrix(2, q.shape[0], q.shape[1], None, q.ctypes.data, s_bits.ctypes.data, None)
+    return m, (q, s_bits)
+
+
+def test_fp8_dequant_golden_group():
+    """A hand-derived group (tests/golden/fp8_group.txt): w = e4m3(q) * s."""
+    rows = [l.split() for l in open(os.path.join(GOLD, "fp8_group.txt"))
+            if l.strip() and not l.startswith("#")]
+    s_bits = int(rows[0][1], 16)
+    cases = [(int(c, 16), float(w)) for c, _, w in rows[1:]]
+    q = np.zeros((1, 128), np.uint8)
+    for i, (c, _) in enumerate(cases):
+        q[0, i] = c
+    m, keep = _fp8_matrix(q, np.array([[s_bits]], np.uint16))
+    for i, (_, w) in enumerate(cases):
+        got = oracle.lib().oracle_weight(C.byref(m), 0, i)
+        assert got == w and np.signbit(got) == np.signbit(w), (i, got, w)
+
+
+def test_fp8_quantizer_roundtrip_exact_on_representable_group():
+    """A group whose largest magnitude is 448 * 2^-8 and whose values are E4M3
+    numbers times 2^-8 gets s = 2^-8 exactly and comes back bit for bit."""
+    rng = np.random.default_rng(5)
+    e4 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    finite = e4[np.isfinite(e4)]
+    vals = rng.choice(finite, size=(3, 256)).astype(np.float32)
+    vals[:, 0] = vals[:, 128] = 448.0                # each group's largest magnitude
+    vals *= 2.0 ** -8
+    enc = ms.quantize_fp8_g128(torch.from_numpy(vals).to(torch.bfloat16))
+    assert np.all(enc["scale"].float().numpy() == 2.0 ** -8)
+    m, keep = _fp8_matrix(enc["q"].numpy(), enc["scale"].view(torch.int16).numpy().view(np.uint16))
+    back = np.array([[oracle.lib().oracle_weight(C.byref(m), r, c) for c in range(256)] for r in range(3)])
+    assert np.array_equal(back, vals.astype(np.float64))
+
+
+def test_fp8_quantizer_error_bound_random_groups():
+    """|w - v| <= half an E4M3 ulp of v/s, times s (E4M3 keeps 3 mantissa bits;
+    the subnormal spacing 2^-9 below 2^-6)."""
+    rng = np.random.default_rng(6)
+    v = torch.from_numpy((rng.standard_normal((8, 512)) * 0.02).astype(np.float32)).to(torch.bfloat16)
+    enc = ms.quantize_fp8_g128(v)
+    m, keep = _fp8_matrix(enc["q"].numpy(), enc["scale"].view(torch.int16).numpy().view(np.uint16))
+    vf = v.double().numpy()
+    for r in range(8):
+        for c in range(0, 512, 7):
+            s = float(enc["scale"][r, c // 128])
+            a = abs(vf[r, c]) / s
+            ulp = 2.0 ** -9 if a < 2.0 ** -6 else 2.0 ** (np.floor(np.log2(a)) - 3)
+            assert abs(oracle.lib().oracle_weight(C.byref(m), r, c) - vf[r, c]) <= 0.5 * ulp * s * (1 + 1e-12)
 
 
 # ----------------------------------------------------------------------------- int4
@@ -266,7 +333,13 @@ def _dequant_numpy(enc):
     return (codes - z) * s
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "int4"])
+def _dequant_fp8_numpy(enc):
+    """E4M3 codes decoded through torch's float8 type, times the group scales."""
+    codes = enc["q"].view(torch.float8_e4m3fn).double().numpy()
+    return codes * np.repeat(enc["scale"].double().numpy(), 128, axis=1)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "int4", "fp8"])
 def test_single_expert_reduces_to_dense_swiglu(fmt):
     """E=1, k=1: the layer is one dense SwiGLU FFN (weight 1.0), d != F so a transposed operand fails."""
     cfg = ms.LayerConfig("t", T=6, d=256, F=384, E=1, k=1, fmt=fmt)
@@ -278,6 +351,8 @@ def test_single_expert_reduces_to_dense_swiglu(fmt):
     assert np.all(idx == 0) and np.all(w == 1.0)
     if fmt == "bf16":
         Wg, Wu, Wd = (wts[m]["w"].double().numpy() for m in ("gate", "up", "down"))
+    elif fmt == "fp8":
+        Wg, Wu, Wd = (_dequant_fp8_numpy(wts[m]) for m in ("gate", "up", "down"))
     else:
         Wg, Wu, Wd = (_dequant_numpy(wts[m]) for m in ("gate", "up", "down"))
     h, y = _dense_swiglu(x, Wg, Wu, Wd)
