@@ -52,7 +52,8 @@ def parse():
 
 
 def describe(cfg: ms.LayerConfig) -> dict:
-    w = {"bf16": "bf16", "int4": "int4 asymmetric group-128 (fp16 scale + zero)"}[cfg.fmt]
+    w = {"bf16": "bf16", "int4": "int4 asymmetric group-128 (fp16 scale + zero)",
+         "fp8": "fp8 E4M3 group-128 (fp16 scale)"}[cfg.fmt]
     route = {"normal": "i.i.d. N(0,1) logits", "zipf": f"Zipf(s={cfg.zipf_s}) routing",
              "reuse": f"{int(cfg.reuse_p * 100)}% of tokens reuse the previous token's experts"}[cfg.logits]
     return {"workload": f"{cfg.name}: MoE FFN layer forward, T={cfg.T}, d_model={cfg.d}, "
@@ -217,6 +218,8 @@ def run_reference(args, cfg):
 def gateup_bytes(cfg, n_active: int, rows: int) -> int:
     if cfg.fmt == "int4":
         wb = 2 * (cfg.d * cfg.F // 2 + cfg.F * (cfg.d // 128) * 4)
+    elif cfg.fmt == "fp8":
+        wb = 2 * (cfg.d * cfg.F + cfg.F * (cfg.d // 128) * 2)
     else:
         wb = 2 * cfg.d * cfg.F * 2
     return n_active * wb + rows * cfg.d * 2 + rows * cfg.F * 2
@@ -262,7 +265,9 @@ def dominant_roofline(cfg, n_active, rows, gu_bytes, gu_ms, hbm, tflops, peak_ki
     tensor peak when its arithmetic intensity exceeds the ridge point."""
     flops = 2.0 * 2 * cfg.d * cfg.F * rows               # gate and up, 2 flops per MAC
     kname = "grouped gate/up GEMM + SwiGLU (tcgen05" + (", int4 dequant in the main loop)"
-                                                       if cfg.fmt == "int4" else ")")
+                                                       if cfg.fmt == "int4" else
+                                                       ", fp8 E4M3 weights read by the MMA)" if cfg.fmt == "fp8"
+                                                       else ")")
     ent = {"kernel": kname, "peak_source": peak_kind, "algorithmic_bytes_per_launch": gu_bytes,
            "algorithmic_flops_per_launch": flops, "traffic": kernel_traffic(cfg.name)}
     if flops / gu_bytes > tflops * 1e12 / (hbm * 1e9):

@@ -72,9 +72,12 @@ enum {
 /* Expert weight formats. */
 typedef enum {
   MOE_W_BF16 = 0,       /* bf16 weights */
-  MOE_W_INT4_G128 = 1   /* int4, asymmetric, one fp16 scale + one fp16 zero (integer 0..15)
+  MOE_W_INT4_G128 = 1,  /* int4, asymmetric, one fp16 scale + one fp16 zero (integer 0..15)
                            per row and group of 128 input elements: w = (q - z) * s
                            ([Strata] sec. 3.1; [CoInf] sec. 5.1) */
+  MOE_W_FP8_G128 = 2    /* 8 bits: OCP fp8 E4M3 codes, one fp16 scale per row and group of
+                           128 input elements: w = e4m3(q) * s ([CoInf] sec. 5.1: 8-bit
+                           group quantisation of the expert layers only) */
 } moe_wfmt;
 
 /* The expert pool: n_slots equally sized slots in one device allocation, and
@@ -96,10 +99,12 @@ typedef struct {
  * bf16:  w[0] = W_gate [F][d], w[1] = W_up [F][d], w[2] = W_down [d][F]  (bf16)
  * int4:  w[m] = packed bytes [rows][K/2]: byte j holds element 2j in its low
  *        nibble and 2j+1 in its high nibble; scale[m], zero[m] = fp16
- *        [rows][K/128]; (rows, K) = (F, d) for gate/up and (d, F) for down. */
+ *        [rows][K/128]; (rows, K) = (F, d) for gate/up and (d, F) for down.
+ * fp8:   w[m] = E4M3 code bytes [rows][K]; scale[m] = fp16 [rows][K/128];
+ *        zero[m] unused. */
 typedef struct {
   const void* w[3];
-  const uint16_t* scale[3];   /* int4 only */
+  const uint16_t* scale[3];   /* int4 and fp8 */
   const uint16_t* zero[3];    /* int4 only */
 } moe_expert_src;
 
@@ -108,7 +113,8 @@ typedef struct {
 const char* moe_status_str(int status);
 
 /* Bytes one expert occupies in the prepacked slot layout (no padding):
- * bf16: 6*d*F;  int4: 1.5*d*F + 3*F*(d/128)*4.  0 for unsupported shapes. */
+ * bf16: 6*d*F;  int4: 1.5*d*F + 3*F*(d/128)*4;  fp8: 3*d*F + 3*F*(d/128)*2.
+ * 0 for unsupported shapes. */
 size_t moe_slot_bytes(int fmt, int d_model, int d_ff);
 
 /* ---------------------------------------------------------------- weight preparation

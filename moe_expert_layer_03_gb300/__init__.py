@@ -26,7 +26,8 @@ from .build import LIB, build  # noqa: F401  (build() compiles the library in-tr
 
 W_BF16 = 0
 W_INT4 = 1
-FMT = {"bf16": W_BF16, "int4": W_INT4}
+W_FP8 = 2
+FMT = {"bf16": W_BF16, "int4": W_INT4, "fp8": W_FP8}
 N_STAGES = 6
 STAGES = ("route", "permute", "gather", "gate_up", "down", "combine")
 DEVERR = {1: "timeout", 2: "expert index out of range", 4: "slot out of range", 8: "bad offsets"}
@@ -149,6 +150,10 @@ class ExpertPool:
                 w = wm["w"].contiguous()
                 keep.append(w)
                 src.w[m] = w.data_ptr()
+            elif self.fmt == W_FP8:
+                q, s = (wm[k].contiguous() for k in ("q", "scale"))
+                keep += [q, s]
+                src.w[m], src.scale[m] = q.data_ptr(), s.data_ptr()
             else:
                 q, s, z = (wm[k].contiguous() for k in ("q", "scale", "zero"))
                 keep += [q, s, z]

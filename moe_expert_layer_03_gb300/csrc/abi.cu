@@ -79,7 +79,7 @@ bool make_byte_row_map(CUtensorMap* m, const void* base, int rows, int K, int bo
 
 moe_status check_pool(const moe_pool* p, bool single) {
   if (!p || !p->pool || !p->expert_to_slot) return MOE_ERR_INVALID_ARG;
-  if (p->fmt != MOE_W_BF16 && p->fmt != MOE_W_INT4_G128) return MOE_ERR_INVALID_ARG;
+  if (p->fmt != MOE_W_BF16 && !fmt_quantised(p->fmt)) return MOE_ERR_INVALID_ARG;
   if (p->n_experts < 1 || p->n_slots < 1) return MOE_ERR_INVALID_ARG;
   if (single && p->n_experts != 1) return MOE_ERR_INVALID_ARG;
   if (p->n_experts > MAX_E) return MOE_ERR_UNSUPPORTED;
@@ -368,7 +368,7 @@ const char* moe_status_str(int status) {
 }
 
 size_t moe_slot_bytes(int fmt, int d_model, int d_ff) {
-  if ((fmt != MOE_W_BF16 && fmt != MOE_W_INT4_G128) || d_model < 128 || d_ff < 128 ||
+  if ((fmt != MOE_W_BF16 && !fmt_quantised(fmt)) || d_model < 128 || d_ff < 128 ||
       d_model % 128 || d_ff % 128)
     return 0;
   return gateup_section_bytes(fmt, d_model, d_ff) + down_section_bytes(fmt, d_model, d_ff);
@@ -382,6 +382,7 @@ moe_status moe_prepack_expert(int fmt, int d_model, int d_ff, const moe_expert_s
   for (int m = 0; m < 3; ++m) {
     if (!src->w[m] || !al16(src->w[m])) return MOE_ERR_INVALID_ARG;
     if (fmt == MOE_W_INT4_G128 && (!src->scale[m] || !src->zero[m])) return MOE_ERR_INVALID_ARG;
+    if (fmt == MOE_W_FP8_G128 && !src->scale[m]) return MOE_ERR_INVALID_ARG;
   }
   return launch_prepack(fmt, d_model, d_ff, *src, (uint8_t*)slot_dst, (cudaStream_t)stream) ==
                  cudaSuccess

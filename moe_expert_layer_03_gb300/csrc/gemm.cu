@@ -55,11 +55,13 @@ struct Shared {   // views into the dynamic shared-memory carve-out
   WorkList W;
 };
 
-size_t carve_bytes(int nmat, bool int4, int bn, int n_a, int n_b, int n_raw, int n_groups) {
-  size_t s = (int4 ? 0 : (size_t)n_a * nmat * BF16_TILE_BYTES) + (size_t)n_b * bn * 128;
-  if (int4) s += (size_t)n_raw * nmat * I4_MAT_BYTES;
+// quant_bytes: bytes of one matrix's raw block (int4 or fp8), 0 for bf16.
+size_t carve_bytes(int nmat, int quant_bytes, int bn, int n_a, int n_b, int n_raw, int n_groups) {
+  const bool quant = quant_bytes > 0;
+  size_t s = (quant ? 0 : (size_t)n_a * nmat * BF16_TILE_BYTES) + (size_t)n_b * bn * 128;
+  if (quant) s += (size_t)n_raw * nmat * quant_bytes;
   s = align_up(s, 16);
-  s += 8 * (size_t)(2 * (n_a + n_b + (int4 ? n_raw : 0)) + 3);
+  s += 8 * (size_t)(2 * (n_a + n_b + (quant ? n_raw : 0)) + 3);
   s += 4 * (MISC_INTS + worklist_ints(n_groups));
   return s;
 }
@@ -88,19 +90,46 @@ __device__ __forceinline__ void dequant_words16(const uint4& w0, uint32_t nz_a, 
   }
 }
 
+// fp8: codes of row r for K chunks [c0, c0 + NC) of 16 (a 128-byte-swizzled
+// row: chunk j at j ^ (r % 8); each 8-element block stored in the order
+// {0,4,1,5,2,6,3,7}) -> fp16 pairs e4m3(q) * s in K order, 8 per chunk.
+template <int NC>
+__device__ __forceinline__ void dequant_fp8(const uint8_t* codes, int r, int c0, __half2 s2,
+                                            uint32_t (&v)[8 * NC]) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const uint4 q = *reinterpret_cast<const uint4*>(codes + r * 128 + (((c0 + c) ^ (r & 7)) << 4));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {   // 8-element block b of the chunk: words w[2b] = (e0,e4,e1,e5), w[2b+1] = (e2,e6,e3,e7)
+      const uint32_t lo = w[2 * b], hi = w[2 * b + 1];
+      const uint16_t pr[4] = {(uint16_t)__byte_perm(lo, 0, 0x0020), (uint16_t)__byte_perm(hi, 0, 0x0020),
+                              (uint16_t)__byte_perm(lo, 0, 0x0031), (uint16_t)__byte_perm(hi, 0, 0x0031)};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {   // pairs (e0,e1), (e2,e3), (e4,e5), (e6,e7)
+        const uint32_t f = e4m3x2_to_f16x2(pr[i]);
+        const __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&f), s2);   // one rounding
+        v[c * 8 + b * 4 + i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    }
+  }
+}
+
 }  // namespace
 
 template <int FMT, bool GATEUP, int NDQ, bool PAIR>
 __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs p) {
-  constexpr bool INT4 = (FMT == MOE_W_INT4_G128);
-  static_assert(!PAIR || (INT4 && !GATEUP), "paired output tiles: int4 down GEMM only");
+  constexpr bool F8 = (FMT == MOE_W_FP8_G128);
+  constexpr bool INT4 = (FMT == MOE_W_INT4_G128) || F8;   // quantised: raw blocks, A dequantised into TMEM
+  static_assert(!PAIR || (INT4 && !GATEUP), "paired output tiles: quantised down GEMM only");
   constexpr int NMAT = (GATEUP || PAIR) ? 2 : 1;
-  static_assert(!INT4 || NDQ == 8, "int4 dequantisation assumes 8 warps (2 per TMEM quadrant)");
+  static_assert(!INT4 || NDQ == 8, "dequantisation assumes 8 warps (2 per TMEM quadrant)");
   constexpr uint32_t AB_BF16 = INT4 ? 0u : 1u;   // operand type of the MMA
   constexpr uint32_t A_STAGE = NMAT * BF16_TILE_BYTES;   // bf16: shared-memory A stage
-  constexpr uint32_t A_SLOT = NMAT * A_SLOT_COLS;        // int4: TMEM columns of one A slot
-  constexpr uint32_t RAW_STAGE = NMAT * I4_MAT_BYTES;
+  constexpr uint32_t A_SLOT = NMAT * A_SLOT_COLS;        // quantised: TMEM columns of one A slot
+  constexpr uint32_t MAT_RAW = F8 ? F8_MAT_BYTES : I4_MAT_BYTES;
+  constexpr uint32_t RAW_STAGE = NMAT * MAT_RAW;
   constexpr int NDQ_THREADS = NDQ * 32;
   const uint32_t B_STAGE = (uint32_t)p.bn * 128u;
 
@@ -194,10 +223,17 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
             const uint32_t raw = smem_u32(S.raw_ring + (size_t)rr.i * RAW_STAGE);
             // gate/up: gate and up blocks of (mt, kg); down: tile mt's block, or
             // both blocks of the pair it.mt, contiguous in the down section
-            const size_t off = GATEUP ? ((size_t)it.mt * (p.K / QGROUP) + kg) * RAW_STAGE
-                               : PAIR ? ((size_t)it.mt * (p.K / QGROUP) + kg) * RAW_STAGE
-                                      : i4_down_block(it.mt, kg, p.K / QGROUP, p.n_mt);
-            bulk_g2s_hint(raw, sec + off, RAW_STAGE, bar, pol);
+            if (!GATEUP && !PAIR && F8) {   // one tile of a pair block: its codes, then its scales
+              int mp, bm;
+              const size_t blk = fp8_down_block(it.mt, kg, p.K / QGROUP, p.n_mt, mp, bm);
+              bulk_g2s_hint(raw, sec + blk + (size_t)mp * F8_CODE_BYTES, F8_CODE_BYTES, bar, pol);
+              bulk_g2s_hint(raw + F8_CODE_BYTES, sec + blk + (size_t)bm * F8_CODE_BYTES + mp * TILE_M * 2,
+                            TILE_M * 2, bar, pol);
+            } else {
+              const size_t off = (GATEUP || PAIR) ? ((size_t)it.mt * (p.K / QGROUP) + kg) * RAW_STAGE
+                                                  : i4_down_block(it.mt, kg, p.K / QGROUP, p.n_mt);
+              bulk_g2s_hint(raw, sec + off, RAW_STAGE, bar, pol);
+            }
             rr.next();
             ++issued_raw;
           }
@@ -310,8 +346,12 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
         for (int kg = g0; kg < g1 && ok; ++kg) {
           ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.raw_full[rr.i]), rr.ph, abort_flag, p.err));
           if (!ok) break;
-          const uint8_t* mat = S.raw_ring + (size_t)rr.i * RAW_STAGE + m_own * I4_MAT_BYTES;
-          const uint32_t sz = *reinterpret_cast<const uint32_t*>(mat + I4_PACKED_BYTES + r * 4);
+          const uint8_t* raw = S.raw_ring + (size_t)rr.i * RAW_STAGE;
+          const uint8_t* mat = raw + m_own * (F8 ? F8_CODE_BYTES : I4_MAT_BYTES);
+          // int4: scale | zero << 16 after the nibbles; fp8: the scales after all code tiles
+          const uint32_t sz = F8 ? (uint32_t)*reinterpret_cast<const uint16_t*>(raw + NMAT * F8_CODE_BYTES +
+                                                                               m_own * TILE_M * 2 + r * 2)
+                                 : *reinterpret_cast<const uint32_t*>(mat + I4_PACKED_BYTES + r * 4);
           const __half sh = __ushort_as_half((unsigned short)(sz & 0xFFFFu));
           const float zf = __half2float(__ushort_as_half((unsigned short)(sz >> 16)));
           const __half2 s2 = __halves2half2(sh, sh);
@@ -326,14 +366,22 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
             const uint32_t ta = tl + a_col0 + (uint32_t)ra.i * A_SLOT;
             if (NMAT == 2) {
               uint32_t v[32];
-              const uint4 w0 = *reinterpret_cast<const uint4*>(mat + ((h * 2 + 0) * TILE_M + r) * 16);
-              const uint4 w1 = *reinterpret_cast<const uint4*>(mat + ((h * 2 + 1) * TILE_M + r) * 16);
-              dequant_words(w0, w1, nz_a, nz_b, s2, v);
+              if constexpr (F8) {
+                dequant_fp8<4>(mat, r, 4 * h, s2, v);   // the 64 codes of K half h
+              } else {
+                const uint4 w0 = *reinterpret_cast<const uint4*>(mat + ((h * 2 + 0) * TILE_M + r) * 16);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(mat + ((h * 2 + 1) * TILE_M + r) * 16);
+                dequant_words(w0, w1, nz_a, nz_b, s2, v);
+              }
               tmem_st_32(ta + (uint32_t)(m_own * A_SLOT_COLS), v);
             } else {
               uint32_t v[16];
-              const uint4 w0 = *reinterpret_cast<const uint4*>(mat + ((h * 2 + j_own) * TILE_M + r) * 16);
-              dequant_words16(w0, nz_a, nz_b, s2, v);
+              if constexpr (F8) {
+                dequant_fp8<2>(mat, r, 4 * h + 2 * j_own, s2, v);   // 32 codes: quarter j_own of the half
+              } else {
+                const uint4 w0 = *reinterpret_cast<const uint4*>(mat + ((h * 2 + j_own) * TILE_M + r) * 16);
+                dequant_words16(w0, nz_a, nz_b, s2, v);
+              }
               tmem_st_16(ta + (uint32_t)(j_own * 16), v);
             }
             tmem_st_wait();
@@ -425,13 +473,14 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
 }
 
 // ------------------------------------------------------------------ host side
-GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups, int n_mt);
-cudaError_t launch_grouped_gemm_group(bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
+GemmPlan plan_gemm_group(int fmt, bool gateup, int bn, int n_groups, int n_mt);
+cudaError_t launch_grouped_gemm_group(int fmt, bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
                                       const GemmPlan& plan, int grid, cudaStream_t stream, bool pdl);
 
 GemmPlan plan_gemm(int fmt, bool gateup, int bn, int n_groups, int n_mt) {
-  const bool int4 = fmt == MOE_W_INT4_G128;
-  if (gemm_is_group(fmt, bn)) return plan_gemm_group(gateup, bn, n_groups, n_mt);
+  const bool int4 = fmt_quantised(fmt);   // raw blocks dequantised into TMEM
+  const int qbytes = int4 ? quant_mat_bytes(fmt) : 0;
+  if (gemm_is_group(fmt, bn)) return plan_gemm_group(fmt, gateup, bn, n_groups, n_mt);
   GemmPlan pl{};
   pl.group = false;
   pl.pair = !gateup && down_paired(fmt, n_mt);
@@ -448,17 +497,17 @@ GemmPlan plan_gemm(int fmt, bool gateup, int bn, int n_groups, int n_mt) {
     if (bn >= 128 && pl.n_b < 4) pl.n_b = 4;
     pl.n_raw = 2;
     while (pl.n_raw < 12 &&
-           carve_bytes(nmat, true, bn, pl.n_a, pl.n_b, pl.n_raw + 1, n_groups) <= budget)
+           carve_bytes(nmat, qbytes, bn, pl.n_a, pl.n_b, pl.n_raw + 1, n_groups) <= budget)
       ++pl.n_raw;
     while (cols < (uint32_t)(acc_cols + pl.n_a * nmat * A_SLOT_COLS)) cols <<= 1;
   } else {
     pl.n_raw = 0;
     pl.n_a = 2;
-    while (pl.n_a < 8 && carve_bytes(nmat, false, bn, pl.n_a + 1, pl.n_b, 0, n_groups) <= budget)
+    while (pl.n_a < 8 && carve_bytes(nmat, 0, bn, pl.n_a + 1, pl.n_b, 0, n_groups) <= budget)
       ++pl.n_a;
     while (cols < (uint32_t)(nmat * bn)) cols <<= 1;
   }
-  pl.smem_bytes = carve_bytes(nmat, int4, bn, pl.n_a, pl.n_b, pl.n_raw, n_groups) + 1024;
+  pl.smem_bytes = carve_bytes(nmat, qbytes, bn, pl.n_a, pl.n_b, pl.n_raw, n_groups) + 1024;
   pl.tmem_cols = cols;
   return pl;
 }
@@ -478,12 +527,12 @@ static cudaError_t launch_one(const CUtensorMap& tmap, const GemmArgs& a, const 
 
 cudaError_t launch_grouped_gemm(int fmt, bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
                                 const GemmPlan& plan, int grid, cudaStream_t stream, bool pdl) {
-  if (plan.group) return launch_grouped_gemm_group(gateup, tmap_b, args, plan, grid, stream, pdl);
+  if (plan.group) return launch_grouped_gemm_group(fmt, gateup, tmap_b, args, plan, grid, stream, pdl);
   args.n_a = plan.n_a;
   args.n_b = plan.n_b;
   args.n_raw = plan.n_raw;
   args.tmem_cols = plan.tmem_cols;
-  constexpr int I4 = MOE_W_INT4_G128, B16 = MOE_W_BF16;
+  constexpr int I4 = MOE_W_INT4_G128, F8 = MOE_W_FP8_G128, B16 = MOE_W_BF16;
   if (fmt == I4) {
     if (gateup) return launch_one<I4, true, 8, false>(tmap_b, args, plan, grid, stream, pdl);
     if (plan.pair) {
@@ -491,6 +540,14 @@ cudaError_t launch_grouped_gemm(int fmt, bool gateup, const CUtensorMap& tmap_b,
       return launch_one<I4, false, 8, true>(tmap_b, args, plan, grid, stream, pdl);
     }
     return launch_one<I4, false, 8, false>(tmap_b, args, plan, grid, stream, pdl);
+  }
+  if (fmt == F8) {
+    if (gateup) return launch_one<F8, true, 8, false>(tmap_b, args, plan, grid, stream, pdl);
+    if (plan.pair) {
+      args.n_mt /= 2;
+      return launch_one<F8, false, 8, true>(tmap_b, args, plan, grid, stream, pdl);
+    }
+    return launch_one<F8, false, 8, false>(tmap_b, args, plan, grid, stream, pdl);
   }
   return gateup ? launch_one<B16, true, 4, false>(tmap_b, args, plan, grid, stream, pdl)
                 : launch_one<B16, false, 4, false>(tmap_b, args, plan, grid, stream, pdl);

@@ -46,6 +46,11 @@
 //                token columns of its 32 rows
 // Modes: gate/up (SwiGLU epilogue, h written in the e4m3 form the down GEMM
 // reads), paired down (two output tiles), single down (one tile).
+// fp8 experts (E4M3 codes, one fp16 scale per row and group): the codes are
+// already the MMA's A operand, stored in the tensor core's 128-byte-swizzled
+// image, so the MMAs read A straight from the stage in shared memory; the
+// unpack warps stay idle and the fold drops the zero-point term
+// (acc += s * (D_hi + D_lo)).
 //
 // Every wait is bounded; on a timeout the CTA drains its copies and MMAs,
 // frees TMEM and returns with MOE_DEVERR_TIMEOUT set.
@@ -117,8 +122,15 @@ struct GShared {
   WorkList W;
 };
 
-size_t group_carve_bytes(int nmat, int bn, int n_st, int n_groups) {
-  size_t s = (size_t)n_st * ((size_t)bn * 256 + (size_t)nmat * I4_MAT_BYTES + sums_bytes(bn, true));
+// Bytes of one stage's weights + token-row entries (fp8: rounded up to 1 KB so
+// every stage's code tiles keep the 1 KB alignment of the swizzled image).
+__host__ __device__ constexpr uint32_t group_raw_stage(bool f8w, int nmat, int bn, bool gateup) {
+  return f8w ? (((uint32_t)(nmat * F8_MAT_BYTES) + (gateup ? 0u : sums_bytes(bn, true)) + 1023u) & ~1023u)
+             : (uint32_t)(nmat * I4_MAT_BYTES) + sums_bytes(bn, !gateup);
+}
+
+size_t group_carve_bytes(bool f8w, int nmat, int bn, bool gateup, int n_st, int n_groups) {
+  size_t s = (size_t)n_st * ((size_t)bn * 256 + group_raw_stage(f8w, nmat, bn, gateup));
   s += sizeof(ItemDesc) * G_ITEM_TAB + 2 * 4 * 32 * sizeof(float);
   s = align_up(s, 16);
   s += 8 * (size_t)(2 * n_st + 2 * G_MAX_NA + 2 * G_MAX_NBUF + 2 + 1);
@@ -158,20 +170,24 @@ __device__ __forceinline__ void e4m3_codes(uint32_t w, uint32_t& a, uint32_t& b)
 
 }  // namespace
 
-template <int MODE, int GBN>
+template <int MODE, int GBN, bool F8W>
 __global__ void __launch_bounds__(G_THREADS, 1)
     grouped_gemm_group_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs p) {
   constexpr bool GATEUP = MODE == G_GATEUP;
   constexpr bool PAIR = MODE != G_DOWN;                // two 128-row matrices per stage
   constexpr int NMAT = PAIR ? 2 : 1;
   constexpr int ESZ = GATEUP ? 4 : 8;                  // bytes per token entry of the per-group array
-  constexpr uint32_t SUMS = sums_bytes(GBN, !GATEUP);
-  constexpr uint32_t SUMS_OFF = NMAT * I4_MAT_BYTES;   // the token rows' per-group entries
-  constexpr uint32_t RAW_STAGE = NMAT * I4_MAT_BYTES + SUMS;
+  // int4: gate/up needs the token rows' group sums (zero-point term), down the
+  // (sum, unscale) pairs of h; fp8: only down's unscale factors
+  constexpr uint32_t SUMS = (F8W && GATEUP) ? 0u : sums_bytes(GBN, !GATEUP);
+  constexpr uint32_t W_BYTES = NMAT * (F8W ? F8_MAT_BYTES : I4_MAT_BYTES);   // weights of a stage
+  constexpr uint32_t SUMS_OFF = W_BYTES;               // the token rows' per-group entries
+  constexpr uint32_t RAW_STAGE = group_raw_stage(F8W, NMAT, GBN, GATEUP);
+  constexpr uint32_t LOADED = W_BYTES + SUMS;          // bytes the copies of a stage bring
   constexpr uint32_t A_COLS = NMAT * 32;               // TMEM columns of one A slot (128 e4m3 per row)
   constexpr uint32_t B_BOX = (uint32_t)GBN * 128u;     // one TMA box: GBN rows x 128 bytes
   constexpr uint32_t B_STAGE = 2u * B_BOX;             // hi rows, then lo rows
-  constexpr int NA = G_MAX_NA;                         // A slots
+  constexpr int NA = F8W ? 0 : G_MAX_NA;               // A slots (fp8: A is read from the stage)
   constexpr uint32_t SLICE = NMAT * 2 * GBN;           // TMEM columns of one accumulator slice (hi, lo)
   constexpr int NBUF = (512 - NA * (int)A_COLS) / (int)SLICE < G_MAX_NBUF
                            ? (512 - NA * (int)A_COLS) / (int)SLICE
@@ -211,7 +227,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < n_st; ++i) {
       mbar_init(smem_u32(&S.full[i]), 1);
-      mbar_init(smem_u32(&S.empty[i]), (G_NUP + G_NFOLD) * 32);
+      mbar_init(smem_u32(&S.empty[i]), ((F8W ? 0 : G_NUP) + G_NFOLD) * 32);
     }
     for (int i = 0; i < G_MAX_NA; ++i) {
       mbar_init(smem_u32(&S.a_full[i]), G_NUP * 32);
@@ -270,15 +286,24 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         for (int kg = g0; kg < g1; ++kg) {
           if (!(ok = mbar_wait(smem_u32(&S.empty[rs.i]), rs.ph ^ 1u, abort_flag, p.err))) break;
           const uint32_t bar = smem_u32(&S.full[rs.i]);
-          mbar_arrive_expect_tx(bar, RAW_STAGE + B_STAGE);
+          mbar_arrive_expect_tx(bar, LOADED + B_STAGE);
           const uint32_t raw = smem_u32(S.raw_ring + (size_t)rs.i * RAW_STAGE);
           int off;
-          bulk_g2s(raw + SUMS_OFF, sums_src(p.b_sum, ESZ, p.rows_total, kg, it.r0, off), SUMS, bar);
+          if (SUMS > 0)
+            bulk_g2s(raw + SUMS_OFF, sums_src(p.b_sum, ESZ, p.rows_total, kg, it.r0, off), SUMS, bar);
           // gate/up: gate and up blocks of (mt, kg); down: tile mt's block, or
           // both blocks of the pair it.mt, contiguous in the down section
-          const size_t woff = MODE == G_DOWN ? i4_down_block(it.mt, kg, p.K / QGROUP, p.n_mt)
-                                             : ((size_t)it.mt * (p.K / QGROUP) + kg) * (NMAT * I4_MAT_BYTES);
-          bulk_g2s_hint(raw, sec + woff, NMAT * I4_MAT_BYTES, bar, pol);
+          if (F8W && MODE == G_DOWN) {   // one tile of an fp8 pair block: its codes, then its scales
+            int mp, bm;
+            const size_t blk = fp8_down_block(it.mt, kg, p.K / QGROUP, p.n_mt, mp, bm);
+            bulk_g2s_hint(raw, sec + blk + (size_t)mp * F8_CODE_BYTES, F8_CODE_BYTES, bar, pol);
+            bulk_g2s_hint(raw + F8_CODE_BYTES, sec + blk + (size_t)bm * F8_CODE_BYTES + mp * TILE_M * 2,
+                          TILE_M * 2, bar, pol);
+          } else {
+            const size_t woff = MODE == G_DOWN ? i4_down_block(it.mt, kg, p.K / QGROUP, p.n_mt)
+                                               : ((size_t)it.mt * (p.K / QGROUP) + kg) * W_BYTES;
+            bulk_g2s_hint(raw, sec + woff, W_BYTES, bar, pol);
+          }
           const uint32_t dst = smem_u32(S.b_ring + (size_t)rs.i * B_STAGE);
           tma_load_2d(dst, &tmap_b, kg * QGROUP, it.r0, bar);
           tma_load_2d(dst + B_BOX, &tmap_b, kg * QGROUP, p.rows_total + it.r0, bar);
@@ -297,8 +322,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     // ring positions advance by one per group, owned or not.
     const int mw = warp - 1;
     bool ok = true;
-    Ring rs{0, 0, n_st}, ra{0, 0, NA}, rc{0, 0, NBUF};
+    Ring rs{0, 0, n_st}, ra{0, 0, NA > 0 ? NA : 1}, rc{0, 0, NBUF};
     const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(S.b_ring));   // stage 0, K step 0
+    const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(S.raw_ring));   // fp8: stage 0's first code tile
     const uint32_t idesc = idesc_f16kind_f32(TILE_M, (uint32_t)(2 * GBN), 0u);   // e4m3 x e4m3 -> f32
     uint32_t gc = 0;
     for (int ii = 0; ii < n_mine && ok; ++ii) {
@@ -307,23 +333,41 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       const int g0 = it.g0, g1 = it.g1;
       for (int kg = g0; kg < g1; ++kg, ++gc, rs.next(), ra.next(), rc.next()) {
         if ((int)(gc & 1u) != mw) continue;
-        if (!(ok = wait_all(smem_u32(&S.a_full[ra.i]), ra.ph, abort_flag, p.err))) break;
+        // int4: the unpacked A slot (which implies its stage has landed); fp8:
+        // the stage itself, whose code tiles are the A operand
+        if (!(ok = wait_all(F8W ? smem_u32(&S.full[rs.i]) : smem_u32(&S.a_full[ra.i]), F8W ? rs.ph : ra.ph,
+                            abort_flag, p.err)))
+          break;
         if (!(ok = wait_all(smem_u32(&S.acc_empty[rc.i]), rc.ph ^ 1u, abort_flag, p.err))) break;
         tc_fence_after();
         // the descriptor's start-address field counts 16-byte units
         const uint64_t bd = bdesc0 + (uint64_t)(((uint32_t)rs.i * B_STAGE) >> 4);
-        const uint32_t a_base = tmem_base + (uint32_t)ra.i * A_COLS;
         const uint32_t d0 = tmem_base + acc0 + (uint32_t)rc.i * SLICE;
+        if constexpr (F8W) {
+          const uint64_t ad = adesc0 + (uint64_t)(((uint32_t)rs.i * RAW_STAGE) >> 4);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {   // K steps of 32 over the hi and lo rows at once
-          const uint64_t bq = bd + (uint64_t)((q * 32) >> 4);
-          const uint32_t ak = a_base + (uint32_t)(q * 8);
-          if (NMAT == 2)
-            mma2_f8_ta_elect(d0, d0 + 2 * GBN, ak, ak + 32, bq, idesc, q > 0 ? 1u : 0u);
-          else
-            mma_f8_ta_elect(d0, ak, bq, idesc, q > 0 ? 1u : 0u);
+          for (int q = 0; q < 4; ++q) {   // K steps of 32 over the hi and lo rows at once
+            const uint64_t bq = bd + (uint64_t)((q * 32) >> 4);
+            const uint64_t aq = ad + (uint64_t)((q * 32) >> 4);
+            if (NMAT == 2)
+              mma2_f8_ss_elect(d0, d0 + 2 * GBN, aq, aq + (uint64_t)(F8_CODE_BYTES >> 4), bq, idesc,
+                               q > 0 ? 1u : 0u);
+            else
+              mma_f8_ss_elect(d0, aq, bq, idesc, q > 0 ? 1u : 0u);
+          }
+        } else {
+          const uint32_t a_base = tmem_base + (uint32_t)ra.i * A_COLS;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {   // K steps of 32 over the hi and lo rows at once
+            const uint64_t bq = bd + (uint64_t)((q * 32) >> 4);
+            const uint32_t ak = a_base + (uint32_t)(q * 8);
+            if (NMAT == 2)
+              mma2_f8_ta_elect(d0, d0 + 2 * GBN, ak, ak + 32, bq, idesc, q > 0 ? 1u : 0u);
+            else
+              mma_f8_ta_elect(d0, ak, bq, idesc, q > 0 ? 1u : 0u);
+          }
+          mma_commit_elect(smem_u32(&S.a_empty[ra.i]));
         }
-        mma_commit_elect(smem_u32(&S.a_empty[ra.i]));
         mma_commit_elect(smem_u32(&S.acc_full[rc.i]));
       }
     }
@@ -339,9 +383,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const int m_own = PAIR ? hw : 0;         // matrix (two-matrix modes) ...
     const int h_own = PAIR ? 0 : hw;         // ... or K half (single down)
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
-    Ring rs{0, 0, n_st}, ra{0, 0, NA};
+    Ring rs{0, 0, n_st}, ra{0, 0, NA > 0 ? NA : 1};
     bool ok = true, full_ready = false, a_ready = false;
-    for (int ii = 0; ii < n_mine && ok; ++ii) {
+    for (int ii = 0; ii < (F8W ? 0 : n_mine) && ok; ++ii) {   // fp8: nothing to unpack
       const ItemDesc it = get_item(ii, p, S);
       if (!it.slot) continue;
       const int g0 = it.g0, g1 = it.g1;
@@ -424,14 +468,20 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       for (int kg = g0; kg < g1 && ok; ++kg) {
         if (!(ok = wait_all(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err))) break;
         const uint8_t* raw = S.raw_ring + (size_t)rs.i * RAW_STAGE;
-        // per matrix: 2^9 s (the codes are q 2^-9) and s z
+        // per matrix: int4: 2^9 s (the codes are q 2^-9) and s z; fp8: s and 0
         float s9[NM], sz[NM];
 #pragma unroll
         for (int m = 0; m < NM; ++m) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(raw + (m0 + m) * I4_MAT_BYTES + I4_PACKED_BYTES + r * 4);
-          const float sc = __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
-          s9[m] = 512.f * sc;
-          sz[m] = sc * __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+          if constexpr (F8W) {
+            const uint16_t w = *reinterpret_cast<const uint16_t*>(raw + NMAT * F8_CODE_BYTES + (m0 + m) * TILE_M * 2 + r * 2);
+            s9[m] = __half2float(__ushort_as_half(w));
+            sz[m] = 0.f;
+          } else {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(raw + (m0 + m) * I4_MAT_BYTES + I4_PACKED_BYTES + r * 4);
+            const float sc = __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+            s9[m] = 512.f * sc;
+            sz[m] = sc * __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+          }
         }
         int off;
         sums_src(p.b_sum, ESZ, p.rows_total, kg, it.r0, off);
@@ -461,7 +511,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             for (int i = 0; i < CH; ++i) {
               const float u = GATEUP ? 1.f : bsum[2 * (ch * CH + i) + 1];
               bu[i] = u;
-              bs[i] = u * bsum[(ch * CH + i) * (ESZ / 4)];
+              bs[i] = F8W ? 0.f : u * bsum[(ch * CH + i) * (ESZ / 4)];
             }
 #pragma unroll
             for (int m = 0; m < NM; ++m) {
@@ -472,7 +522,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 const int n = ch * CH + i;
                 const float sd = GATEUP ? s9[m] : s9[m] * bu[i];
                 const float dsum = __uint_as_float(dv[m][i]) + __uint_as_float(dl[m][i]);
-                acc[m][n] = fmaf(sd, dsum, fmaf(-sz[m], bs[i], acc[m][n]));
+                acc[m][n] = F8W ? fmaf(sd, dsum, acc[m][n]) : fmaf(sd, dsum, fmaf(-sz[m], bs[i], acc[m][n]));
               }
             }
           }
@@ -584,18 +634,19 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ host side
-GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups, int n_mt) {
+GemmPlan plan_gemm_group(int fmt, bool gateup, int bn, int n_groups, int n_mt) {
   GemmPlan pl{};
   pl.group = true;
-  pl.pair = !gateup && down_paired(MOE_W_INT4_G128, n_mt);
+  pl.pair = !gateup && down_paired(fmt, n_mt);
   const int nmat = (gateup || pl.pair) ? 2 : 1;
+  const bool f8w = fmt == MOE_W_FP8_G128;
   pl.ndq = G_NUP + G_NFOLD;
   const size_t budget = 227 * 1024 - 1024;
   int n_st = 3;
-  while (n_st < 16 && group_carve_bytes(nmat, bn, n_st + 1, n_groups) <= budget) ++n_st;
-  pl.n_raw = n_st;   // stages (nibbles + token rows)
+  while (n_st < 16 && group_carve_bytes(f8w, nmat, bn, gateup, n_st + 1, n_groups) <= budget) ++n_st;
+  pl.n_raw = n_st;   // stages (weights + token rows)
   pl.n_b = n_st;
-  pl.smem_bytes = group_carve_bytes(nmat, bn, n_st, n_groups) + 1024;
+  pl.smem_bytes = group_carve_bytes(f8w, nmat, bn, gateup, n_st, n_groups) + 1024;
   // the kernel derives its A slot and accumulator slice counts from its
   // template arguments so that they fit 512 columns
   pl.n_a = G_MAX_NA;
@@ -603,10 +654,10 @@ GemmPlan plan_gemm_group(bool gateup, int bn, int n_groups, int n_mt) {
   return pl;
 }
 
-template <int MODE, int GBN>
+template <int MODE, int GBN, bool F8W>
 static cudaError_t launch_group_one(const CUtensorMap& tmap, const GemmArgs& a, const GemmPlan& pl,
                                     int grid, cudaStream_t s, bool pdl) {
-  auto kern = grouped_gemm_group_kernel<MODE, GBN>;
+  auto kern = grouped_gemm_group_kernel<MODE, GBN, F8W>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -616,25 +667,32 @@ static cudaError_t launch_group_one(const CUtensorMap& tmap, const GemmArgs& a, 
   return launch_kernel(kern, dim3(grid), dim3(G_THREADS), pl.smem_bytes, s, pdl, tmap, a);
 }
 
-template <int MODE>
+template <int MODE, bool F8W>
 static cudaError_t launch_group_mode(const CUtensorMap& tmap, const GemmArgs& a, const GemmPlan& pl,
                                      int grid, cudaStream_t s, bool pdl) {
-  return a.bn == 16 ? launch_group_one<MODE, 16>(tmap, a, pl, grid, s, pdl)
-                    : launch_group_one<MODE, 32>(tmap, a, pl, grid, s, pdl);
+  return a.bn == 16 ? launch_group_one<MODE, 16, F8W>(tmap, a, pl, grid, s, pdl)
+                    : launch_group_one<MODE, 32, F8W>(tmap, a, pl, grid, s, pdl);
 }
 
-cudaError_t launch_grouped_gemm_group(bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
+template <bool F8W>
+static cudaError_t launch_group_fmt(bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
+                                    const GemmPlan& plan, int grid, cudaStream_t stream, bool pdl) {
+  if (gateup) return launch_group_mode<G_GATEUP, F8W>(tmap_b, args, plan, grid, stream, pdl);
+  if (plan.pair) {
+    args.n_mt /= 2;   // work items name pairs of output tiles
+    return launch_group_mode<G_DOWN_PAIR, F8W>(tmap_b, args, plan, grid, stream, pdl);
+  }
+  return launch_group_mode<G_DOWN, F8W>(tmap_b, args, plan, grid, stream, pdl);
+}
+
+cudaError_t launch_grouped_gemm_group(int fmt, bool gateup, const CUtensorMap& tmap_b, GemmArgs args,
                                       const GemmPlan& plan, int grid, cudaStream_t stream, bool pdl) {
   args.n_a = plan.n_a;
   args.n_b = plan.n_b;
   args.n_raw = plan.n_raw;
   args.tmem_cols = plan.tmem_cols;
-  if (gateup) return launch_group_mode<G_GATEUP>(tmap_b, args, plan, grid, stream, pdl);
-  if (plan.pair) {
-    args.n_mt /= 2;   // work items name pairs of output tiles
-    return launch_group_mode<G_DOWN_PAIR>(tmap_b, args, plan, grid, stream, pdl);
-  }
-  return launch_group_mode<G_DOWN>(tmap_b, args, plan, grid, stream, pdl);
+  return fmt == MOE_W_FP8_G128 ? launch_group_fmt<true>(gateup, tmap_b, args, plan, grid, stream, pdl)
+                               : launch_group_fmt<false>(gateup, tmap_b, args, plan, grid, stream, pdl);
 }
 
 }  // namespace moe

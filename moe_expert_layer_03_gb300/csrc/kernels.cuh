@@ -26,21 +26,37 @@ namespace moe {
 //         group g) the two tiles' blocks back to back, so that a GEMM step over
 //         both tiles is one contiguous copy; with an odd tile count the last
 //         tile follows alone, one block per group (i4_down_block).
+//   fp8:  per (mt, g) one block of NMAT x 16640 B: the NMAT code tiles first,
+//         each the 128 x 128-byte E4M3 image the tensor core reads (128-byte
+//         swizzle: 16-byte chunk j of row r at chunk j ^ (r % 8)), then NMAT x
+//         128 fp16 scales.  Within every 8-element K block the codes are stored
+//         in the order {0,4,1,5,2,6,3,7} (the K order of the int4 decode path,
+//         so both read the same token operand).  The down section pairs output
+//         tiles like int4 (fp8_down_block).
 constexpr int TILE_M = 128;          // weight rows per MMA tile (the MMA's M)
 constexpr int KSTEP = 64;            // K elements per pipeline stage (one 128-byte row)
 constexpr int QGROUP = 128;          // int4 quantisation group
 constexpr int BF16_TILE_BYTES = TILE_M * KSTEP * 2;          // 16384
 constexpr int I4_PACKED_BYTES = TILE_M * QGROUP / 2;         // 8192
 constexpr int I4_MAT_BYTES = I4_PACKED_BYTES + TILE_M * 4;   // 8704
+constexpr int F8_CODE_BYTES = TILE_M * QGROUP;                // 16384
+constexpr int F8_MAT_BYTES = F8_CODE_BYTES + TILE_M * 2;       // 16640
 // Readable bytes that must follow a [groups][rows] float array the int4
 // decode GEMM reads per stage (group sums, unscale factors): it copies each
 // item's row range as a 16-byte-aligned superset (at most 2 (bn + 1) floats past the end).
 constexpr int SUMS_PAD_BYTES = 512;
 
+// Bytes of one matrix block (one 128-row tile, one quantisation group) of a
+// quantised format.
+__host__ __device__ inline int quant_mat_bytes(int fmt) {
+  return fmt == MOE_W_FP8_G128 ? F8_MAT_BYTES : I4_MAT_BYTES;
+}
+__host__ __device__ inline bool fmt_quantised(int fmt) {
+  return fmt == MOE_W_INT4_G128 || fmt == MOE_W_FP8_G128;
+}
 __host__ __device__ inline size_t gateup_section_bytes(int fmt, int d, int F) {
-  return fmt == MOE_W_INT4_G128
-             ? (size_t)(F / TILE_M) * (d / QGROUP) * (2 * I4_MAT_BYTES)
-             : (size_t)(F / TILE_M) * (d / KSTEP) * (2 * BF16_TILE_BYTES);
+  return fmt_quantised(fmt) ? (size_t)(F / TILE_M) * (d / QGROUP) * (2 * quant_mat_bytes(fmt))
+                            : (size_t)(F / TILE_M) * (d / KSTEP) * (2 * BF16_TILE_BYTES);
 }
 // Byte offset, within the int4 down section, of output tile mt's block for
 // quantisation group g (G groups per row, n_mt output tiles).
@@ -49,9 +65,23 @@ __host__ __device__ inline size_t i4_down_block(int mt, int g, int G, int n_mt) 
   return p0 + 1 < n_mt ? ((size_t)p0 * G + 2 * g + (mt & 1)) * I4_MAT_BYTES
                        : ((size_t)mt * G + g) * I4_MAT_BYTES;
 }
+// fp8 down section, output tile mt, group g: where its block (one tile, or
+// the pair holding it) starts, and the tile's place in it (0 alone or first,
+// 1 second) and the number of tiles in the block.
+__host__ __device__ inline size_t fp8_down_block(int mt, int g, int G, int n_mt, int& m, int& nmat) {
+  const int p0 = mt & ~1;
+  if (p0 + 1 < n_mt) {
+    m = mt & 1;
+    nmat = 2;
+    return ((size_t)p0 * G + 2 * g) * F8_MAT_BYTES;
+  }
+  m = 0;
+  nmat = 1;
+  return ((size_t)mt * G + g) * F8_MAT_BYTES;
+}
 __host__ __device__ inline size_t down_section_bytes(int fmt, int d, int F) {
-  return fmt == MOE_W_INT4_G128 ? (size_t)(d / TILE_M) * (F / QGROUP) * I4_MAT_BYTES
-                                : (size_t)(d / TILE_M) * (F / KSTEP) * BF16_TILE_BYTES;
+  return fmt_quantised(fmt) ? (size_t)(d / TILE_M) * (F / QGROUP) * quant_mat_bytes(fmt)
+                            : (size_t)(d / TILE_M) * (F / KSTEP) * BF16_TILE_BYTES;
 }
 
 // ------------------------------------------------------------------ grouped GEMM
@@ -102,24 +132,24 @@ struct GemmPlan {
   uint32_t tmem_cols;
 };
 
-// int4 layers run their GEMMs on fp16 operands (x_perm and h are fp16); bf16
-// layers on bf16 operands.
-inline bool gemm_uses_fp16(int fmt) { return fmt == MOE_W_INT4_G128; }
+// Quantised layers run their prefill-size GEMMs on fp16 operands (x_perm and h
+// are fp16); bf16 layers on bf16 operands.
+inline bool gemm_uses_fp16(int fmt) { return fmt_quantised(fmt); }
 
-// Uses the group-scaled decode kernel (int4, row chunks of <= 32)?
-inline bool gemm_is_group(int fmt, int bn) { return fmt == MOE_W_INT4_G128 && bn <= 32; }
+// Uses the group-scaled decode kernel (int4 or fp8, row chunks of <= 32)?
+inline bool gemm_is_group(int fmt, int bn) { return fmt_quantised(fmt) && bn <= 32; }
 // Work tiles per (group, row chunk, K split) of the down GEMM with n_mt output
-// tiles: the int4 kernels pair adjacent tiles when n_mt is even.
-inline bool down_paired(int fmt, int n_mt) { return fmt == MOE_W_INT4_G128 && n_mt % 2 == 0; }
+// tiles: the quantised kernels pair adjacent tiles when n_mt is even.
+inline bool down_paired(int fmt, int n_mt) { return fmt_quantised(fmt) && n_mt % 2 == 0; }
 inline int down_work_tiles(int fmt, int n_mt) { return down_paired(fmt, n_mt) ? n_mt / 2 : n_mt; }
 // Row-chunk width (the GEMMs' N): a power of two >= twice the mean rows per
-// expert, 16..256; int4 layers stop at 192 so that the gate and up
+// expert, 16..256; quantised layers stop at 192 so that the gate and up
 // accumulators (2 x 192 TMEM columns) leave room for the dequantised A tiles.
 inline int choose_bn(int A, int E, int fmt) {
   const int mean = (A + E - 1) / E;
   int bn = 16;
   while (bn < 2 * mean && bn < 256) bn <<= 1;
-  if (fmt == MOE_W_INT4_G128 && bn > 128) bn = 192;
+  if (fmt_quantised(fmt) && bn > 128) bn = 192;
   return bn;
 }
 

@@ -78,6 +78,72 @@ __global__ void prepack_int4_kernel(const uint8_t* __restrict__ q0, const uint16
   }
 }
 
+// fp8: the block of (mt, g) holds NMAT code tiles then NMAT x 128 fp16 scales
+// (layout in kernels.cuh).  Chunk (m, r, p) of a code tile holds the codes of
+// row mt*128 + r for K elements g*128 + 16j .. +16, j = p ^ (r % 8), each
+// 8-element block in the order {0,4,1,5,2,6,3,7}; the scale part is
+// NMAT * 16 chunks of 8 scales.  down (NMAT = 1): the blocks of a tile pair
+// share one 2-matrix block (fp8_down_block).
+__global__ void prepack_fp8_kernel(const uint8_t* __restrict__ q0, const uint16_t* __restrict__ s0,
+                                   const uint8_t* __restrict__ q1, const uint16_t* __restrict__ s1,
+                                   int nmat, int rows, int K, uint8_t* __restrict__ dst) {
+  const int G = K / QGROUP, n_mt = rows / TILE_M;
+  constexpr int CODE_CH = F8_CODE_BYTES / 16;   // 1024 chunks per code tile
+  constexpr int SC_CH = TILE_M * 2 / 16;        // 16 chunks of scales per matrix
+  const size_t n_chunks = (size_t)n_mt * G * nmat * (CODE_CH + SC_CH);
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_chunks;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % (CODE_CH + SC_CH));   // chunk within the matrix's share
+    const size_t t2 = i / (CODE_CH + SC_CH);
+    const int m = (int)(t2 % nmat);
+    const size_t t3 = t2 / nmat;
+    const int g = (int)(t3 % G);
+    const int mt = (int)(t3 / G);
+    // where the matrix sits: gate/up blocks hold both matrices of (mt, g);
+    // the down section pairs output tiles
+    size_t blk;
+    int mpos, bmat;
+    if (nmat == 2) {
+      blk = ((size_t)mt * G + g) * (2 * F8_MAT_BYTES);
+      mpos = m;
+      bmat = 2;
+    } else {
+      blk = fp8_down_block(mt, g, G, n_mt, mpos, bmat);
+    }
+    const uint8_t* q = m == 0 ? q0 : q1;
+    const uint16_t* sc = m == 0 ? s0 : s1;
+    uint32_t out[4];
+    size_t off;
+    if (c < CODE_CH) {
+      const int r = c >> 3, pch = c & 7, j = pch ^ (r & 7);
+      const uint8_t* src = q + (size_t)(mt * TILE_M + r) * K + g * QGROUP + j * 16;
+      uint8_t b[16];
+#pragma unroll
+      for (int blk8 = 0; blk8 < 2; ++blk8)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int slot = e < 4 ? 2 * e : 2 * (e - 4) + 1;   // stored position of element e
+          b[blk8 * 8 + slot] = src[blk8 * 8 + e];
+        }
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        out[w] = (uint32_t)b[4 * w] | ((uint32_t)b[4 * w + 1] << 8) | ((uint32_t)b[4 * w + 2] << 16) |
+                 ((uint32_t)b[4 * w + 3] << 24);
+      off = blk + (size_t)mpos * F8_CODE_BYTES + (size_t)c * 16;
+    } else {
+      const int r0 = (c - CODE_CH) * 8;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t lo = sc[(size_t)(mt * TILE_M + r0 + 2 * w) * G + g];
+        const uint32_t hi = sc[(size_t)(mt * TILE_M + r0 + 2 * w + 1) * G + g];
+        out[w] = lo | (hi << 16);
+      }
+      off = blk + (size_t)bmat * F8_CODE_BYTES + (size_t)mpos * TILE_M * 2 + (size_t)r0 * 2;
+    }
+    *reinterpret_cast<uint4*>(dst + off) = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
 cudaError_t launch_prepack(int fmt, int d, int F, const moe_expert_src& src, uint8_t* dst,
                            cudaStream_t s) {
   const int blocks = 1024, threads = 256;
@@ -87,6 +153,11 @@ cudaError_t launch_prepack(int fmt, int d, int F, const moe_expert_src& src, uin
                                                    (const uint16_t*)src.w[1], 2, F, d, dst);
     prepack_bf16_kernel<<<blocks, threads, 0, s>>>((const uint16_t*)src.w[2], nullptr, 1, d, F,
                                                    down_dst);
+  } else if (fmt == MOE_W_FP8_G128) {
+    prepack_fp8_kernel<<<blocks, threads, 0, s>>>((const uint8_t*)src.w[0], src.scale[0],
+                                                  (const uint8_t*)src.w[1], src.scale[1], 2, F, d, dst);
+    prepack_fp8_kernel<<<blocks, threads, 0, s>>>((const uint8_t*)src.w[2], src.scale[2], nullptr,
+                                                  nullptr, 1, d, F, down_dst);
   } else {
     prepack_int4_kernel<<<blocks, threads, 0, s>>>(
         (const uint8_t*)src.w[0], src.scale[0], src.zero[0], (const uint8_t*)src.w[1],

@@ -287,6 +287,29 @@ MOE_DEV void mma2_f8_ta_elect(uint32_t d0, uint32_t d1, uint32_t a0, uint32_t a1
       "r"(d1), "r"(a0), "r"(a1), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// kind::f8f6f4 with A and B in shared memory (descriptors), issued from a
+// converged warp: two A tiles against one B into two accumulators, or one.
+MOE_DEV void mma2_f8_ss_elect(uint32_t d0, uint32_t d1, uint64_t a0, uint64_t a1, uint64_t bdesc,
+                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, %4, %5, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%1], %3, %4, %5, p;\n\t}" ::"r"(d0),
+      "r"(d1), "l"(a0), "l"(a1), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+MOE_DEV void mma_f8_ss_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives once on `bar` when every tcgen05 op this thread issued so far is done.
 MOE_DEV void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -367,6 +390,12 @@ MOE_DEV uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   return r;
 }
 // A packed e4m3 pair -> the two values as fp32 (exact), low byte first.
+// Two e4m3 bytes -> an fp16 pair (exact): the low byte becomes the low half.
+MOE_DEV uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+  return h;
+}
 MOE_DEV float2 e4m3x2_to_f32x2(uint16_t v) {
   uint32_t h;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));

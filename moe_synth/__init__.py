@@ -14,6 +14,8 @@ Workload shapes follow the five configurations the layer is measured on:
                   + 1 always-on shared expert, permuted expert->slot table
   mixtral_prefill T=2048, d=4096, F=14336, E=8,   k=2, int4, 44% of tokens
                   reuse the previous token's expert pair
+  mixtral_decode_fp8, mixtral_prefill_fp8: the two Mixtral layers with 8-bit
+                  experts (E4M3 codes, one fp16 scale per row and group of 128)
 
 Recipes (the values the layer sees; all seeded):
   * x ~ N(0,1) drawn in fp32 and rounded to bf16.
@@ -77,6 +79,11 @@ CONFIGS = {
                                  logits="zipf", zipf_s=1.1, shared=True, slot_perm=True),
     "mixtral_prefill": LayerConfig("mixtral_prefill", T=2048, d=4096, F=14336, E=8, k=2,
                                    fmt="int4", logits="reuse", reuse_p=0.44),
+    # the same two Mixtral-shaped layers with 8-bit (E4M3, group-128) experts
+    "mixtral_decode_fp8": LayerConfig("mixtral_decode_fp8", T=16, d=4096, F=14336, E=8, k=2,
+                                      fmt="fp8"),
+    "mixtral_prefill_fp8": LayerConfig("mixtral_prefill_fp8", T=2048, d=4096, F=14336, E=8, k=2,
+                                       fmt="fp8", logits="reuse", reuse_p=0.44),
 }
 
 

@@ -42,6 +42,16 @@ SMALL = {
     # the same launch writing bf16 rows, k < E
     "fused_route_bf16": ms.LayerConfig("fused_route_bf16", T=64, d=256, F=256, E=32, k=6, fmt="bf16",
                                        seed=11),
+    # 8-bit experts: decode kernel (A read from shared memory) at 16- and 32-row
+    # chunks, paired and single down tiles (d/128 odd: a pair block, then a
+    # tile alone), the shared expert and a permuted slot table
+    "fp8_tiny": ms.CONFIGS["tiny"].with_(name="fp8_tiny", fmt="fp8"),
+    "fp8_shared_perm": ms.LayerConfig("fp8_shared_perm", T=24, d=384, F=256, E=16, k=4, fmt="fp8",
+                                      logits="zipf", zipf_s=1.1, shared=True, slot_perm=True, seed=13),
+    "fp8_chunk32": ms.LayerConfig("fp8_chunk32", T=48, d=256, F=640, E=8, k=2, fmt="fp8", seed=14),
+    # ... and the prefill kernel (fp16 A dequantised into TMEM): paired and odd tile counts
+    "fp8_chunk64": ms.LayerConfig("fp8_chunk64", T=96, d=256, F=384, E=8, k=2, fmt="fp8", seed=15),
+    "fp8_wide_odd": ms.LayerConfig("fp8_wide_odd", T=96, d=384, F=512, E=4, k=2, fmt="fp8", seed=16),
 }
 
 
@@ -98,7 +108,7 @@ def test_combine_with_shared_rows():
 
 
 @pytest.mark.parametrize("name", ["mixtral_decode", "phi35_prefill", "fg125b_decode",
-                                  "mixtral_prefill"])
+                                  "mixtral_prefill", "mixtral_decode_fp8", "mixtral_prefill_fp8"])
 def test_layer_full_size_sampled(name):
     cfg = ms.CONFIGS[name]
     L = GpuLayer(cfg)
