@@ -246,6 +246,55 @@ moe_status moe_layer_forward_noalloc(const uint16_t* x, const float* logits, int
                                      const moe_pool* routed, const moe_pool* shared,
                                      uint16_t* out, moe_stream_t stream);
 
+/* ---------------------------------------------------------------- expert streaming
+ * Pools larger than HBM ([Strata] sec. 2.1: a resident hot-expert pool, cold
+ * experts in system memory loaded on demand; [CoInf] sec. 2.2: an expert cache
+ * with LRU replacement).  On a Grace-Blackwell node the cold tier is pinned host
+ * memory reached over NVLink-C2C; the hot tier is the HBM pool of a moe_pool.
+ *
+ * moe_cache_create: `routed` describes the hot tier (n_experts = E experts,
+ * n_slots slots of slot_bytes; its expert_to_slot table is rewritten by the
+ * cache); host_images = pinned host memory holding all E experts' prepacked
+ * slot images (expert e at host_images + e * slot_bytes, as moe_prepack_expert
+ * writes them).  Both are owned by the caller and must outlive the cache.  The
+ * cache starts empty; it allocates only its host-side bookkeeping.  copy_mode:
+ * MOE_CACHE_COPY_ENGINE copies each image with cudaMemcpyAsync (the DMA
+ * engines); MOE_CACHE_COPY_SM with a kernel whose threads read the host images
+ * over the C2C link and write the slot (needs host_images to be mapped into the
+ * device address space, checked with cudaHostGetDevicePointer; otherwise
+ * MOE_ERR_UNSUPPORTED); MOE_CACHE_COPY_AUTO picks the kernel when the images
+ * are mapped, else the DMA engines.
+ *
+ * moe_cache_ensure: makes the n listed experts (host int32, distinct, in
+ * [0, E), n <= n_slots) resident before the work that follows on `stream`.
+ * A listed expert already in a slot is a hit; each other one takes an empty
+ * slot, else the least recently used slot holding no listed expert (LRU), and
+ * its image is copied host -> device on `stream`.  Then the device
+ * expert_to_slot table is rewritten on `stream`: resident experts map to their
+ * slot, all others to -1, so routing a token to an expert that was not made
+ * resident flags MOE_DEVERR_SLOT_RANGE instead of reading another expert's
+ * weights.  Every copy is ordered on `stream` after the work already queued
+ * there, so a slot is never overwritten while an earlier forward on the same
+ * stream reads it.
+ *
+ * moe_cache_plan: the same decisions and bookkeeping as moe_cache_ensure
+ * without any CUDA call; writes the experts to load and their slots
+ * (load_expert / load_slot, n_slots entries each) and *n_loads.
+ *
+ * moe_cache_stats: hits, misses (= expert images copied), bytes copied. */
+typedef struct moe_expert_cache moe_expert_cache;
+enum { MOE_CACHE_COPY_AUTO = 0, MOE_CACHE_COPY_ENGINE = 1, MOE_CACHE_COPY_SM = 2 };
+typedef struct {
+  long long hits, misses, bytes_copied;
+} moe_cache_counters;
+moe_status moe_cache_create(const moe_pool* routed, const void* host_images, int copy_mode,
+                            moe_expert_cache** out);
+moe_status moe_cache_ensure(moe_expert_cache* cache, const int32_t* experts, int n, moe_stream_t stream);
+moe_status moe_cache_plan(moe_expert_cache* cache, const int32_t* experts, int n, int32_t* load_expert,
+                          int32_t* load_slot, int* n_loads);
+moe_status moe_cache_stats(const moe_expert_cache* cache, moe_cache_counters* out);
+void moe_cache_destroy(moe_expert_cache* cache);
+
 /* Kernel launches one moe_layer_forward enqueues for these arguments (0 on error). */
 int moe_layer_launch_count(int T, int k, const moe_pool* routed, const moe_pool* shared);
 

@@ -36,7 +36,9 @@ EXPORTS = ("moe_status_str", "moe_slot_bytes", "moe_prepack_expert", "moe_route_
            "moe_permute_workspace_bytes", "moe_permute", "moe_grouped_ffn_workspace_bytes",
            "moe_grouped_ffn", "moe_combine", "moe_layer_workspace_bytes", "moe_layer_forward",
            "moe_layer_forward_timed", "moe_layer_launch_count", "moe_last_device_error",
-           "moe_layer_forward_noalloc", "moe_router_logits", "moe_layer_forward_router")
+           "moe_layer_forward_noalloc", "moe_router_logits", "moe_layer_forward_router",
+           "moe_cache_create", "moe_cache_ensure", "moe_cache_plan", "moe_cache_stats",
+           "moe_cache_destroy")
 
 
 class MoeError(RuntimeError):
@@ -47,6 +49,10 @@ class MoePool(C.Structure):
     _fields_ = [("n_experts", C.c_int), ("n_slots", C.c_int), ("d_model", C.c_int),
                 ("d_ff", C.c_int), ("fmt", C.c_int), ("pool", C.c_void_p),
                 ("slot_bytes", C.c_size_t), ("expert_to_slot", C.c_void_p)]
+
+
+class CacheCounters(C.Structure):
+    _fields_ = [("hits", C.c_longlong), ("misses", C.c_longlong), ("bytes_copied", C.c_longlong)]
 
 
 class ExpertSrc(C.Structure):
@@ -74,6 +80,12 @@ def lib() -> C.CDLL:
             L.moe_router_logits.argtypes = [P, P, I, I, I, P, P]
             L.moe_layer_forward_router.argtypes = [P, P, I, I, C.POINTER(MoePool),
                                                    C.POINTER(MoePool), P, P, P, S, P]
+            L.moe_cache_create.argtypes = [C.POINTER(MoePool), P, I, C.POINTER(P)]
+            L.moe_cache_ensure.argtypes = [P, P, I, P]
+            L.moe_cache_plan.argtypes = [P, P, I, P, P, C.POINTER(I)]
+            L.moe_cache_stats.argtypes = [P, C.POINTER(CacheCounters)]
+            L.moe_cache_destroy.argtypes = [P]
+            L.moe_cache_destroy.restype = None
             L.moe_route_topk.argtypes = [P, I, I, I, P, P, P]
             L.moe_permute_workspace_bytes.restype = S
             L.moe_permute_workspace_bytes.argtypes = []
@@ -168,6 +180,69 @@ class ExpertPool:
 
     def view(self, expert_to_slot: torch.Tensor) -> PoolView:
         return PoolView(self, expert_to_slot)
+
+
+class ExpertCache:
+    """A pool larger than HBM: every expert's prepacked image in pinned host
+    memory (the cold tier, reached over NVLink-C2C on a Grace-Blackwell node) and
+    `pool`'s slots as the hot tier, filled on demand with LRU replacement
+    (moe_cache_* in moe.h).  `view` is the routed pool view the layer takes; its
+    expert -> slot table is maintained by the cache."""
+
+    COPY_AUTO, COPY_ENGINE, COPY_SM = 0, 1, 2
+
+    def __init__(self, pool: "ExpertPool", n_experts: int, copy_mode: int = 0):
+        self.pool, self.n_experts = pool, n_experts
+        self.host = torch.empty(n_experts * pool.slot_bytes, dtype=torch.uint8, pin_memory=True)
+        self.e2s = torch.full((n_experts,), -1, dtype=torch.int32, device=pool.buf.device)
+        self.view = PoolView(pool, self.e2s)
+        h = C.c_void_p()
+        _check(lib().moe_cache_create(self.view.ref, C.c_void_p(self.host.data_ptr()), copy_mode,
+                                      C.byref(h)), "moe_cache_create")
+        self._h = h
+        self._scratch = None
+
+    def load_expert(self, e: int, weights: dict):
+        """Prepack expert e (canonical device tensors) into its host image."""
+        if self._scratch is None:
+            p = self.pool
+            self._scratch = ExpertPool(1, p.d_model, p.d_ff, p.fmt, device=p.buf.device)
+        self._scratch.load_expert(0, weights)
+        sb = self.pool.slot_bytes
+        self.host[e * sb:(e + 1) * sb].copy_(self._scratch.buf)
+
+    def load_image(self, e: int, image: torch.Tensor):
+        """Expert e's host image from an already prepacked slot image (uint8,
+        slot_bytes long, e.g. a slot of another pool of the same shape)."""
+        sb = self.pool.slot_bytes
+        if image.dtype != torch.uint8 or image.numel() != sb:
+            raise MoeError("expert image must be slot_bytes uint8")
+        self.host[e * sb:(e + 1) * sb].copy_(image)
+
+    def ensure(self, experts, stream=None):
+        ex = (C.c_int32 * len(experts))(*[int(e) for e in experts])
+        _check(lib().moe_cache_ensure(self._h, C.cast(ex, C.c_void_p), len(experts), _stream(stream)),
+               "moe_cache_ensure")
+
+    def plan(self, experts):
+        """The loads ensure() would do (and its bookkeeping), without CUDA work."""
+        n = self.pool.n_slots
+        ex = (C.c_int32 * max(1, len(experts)))(*[int(e) for e in experts])
+        le, ls, nl = (C.c_int32 * n)(), (C.c_int32 * n)(), C.c_int(0)
+        _check(lib().moe_cache_plan(self._h, C.cast(ex, C.c_void_p), len(experts), C.cast(le, C.c_void_p),
+                                    C.cast(ls, C.c_void_p), C.byref(nl)), "moe_cache_plan")
+        return [(le[i], ls[i]) for i in range(nl.value)]
+
+    def stats(self) -> dict:
+        c = CacheCounters()
+        _check(lib().moe_cache_stats(self._h, C.byref(c)), "moe_cache_stats")
+        return {"hits": c.hits, "misses": c.misses, "bytes_copied": c.bytes_copied}
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and _lib is not None:
+            _lib.moe_cache_destroy(h)
+            self._h = None
 
 
 # ----------------------------------------------------------------------------- workspaces
