@@ -120,6 +120,24 @@ def test_layer_full_size_sampled(name):
     assert_close_rms(got[toks], L.oracle_forward(toks), what=name)
 
 
+@pytest.mark.parametrize("cfg", [
+    # the largest supported d_model (K = 32768 for gate/up: 256 quantisation groups)
+    ms.LayerConfig("max_d", T=5, d=32768, F=128, E=2, k=1, fmt="int4", seed=31),
+    # the largest supported d_ff (256 output tiles for gate/up, K = 32768 for down)
+    ms.LayerConfig("max_f", T=5, d=128, F=32768, E=2, k=2, fmt="fp8", seed=32),
+    # many assignments: 160000 rows through the multi-tile permutation and GEMMs
+    ms.LayerConfig("large_A", T=20000, d=128, F=128, E=64, k=8, fmt="bf16", seed=33),
+], ids=lambda c: c.name)
+def test_size_limits_sampled(cfg):
+    L = GpuLayer(cfg)
+    out, ws = L.forward()
+    assert moe.last_device_error(ws) == 0
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    toks = sorted({0, 1, cfg.T // 2, cfg.T - 1})
+    assert_close_rms(got[toks], L.oracle_forward(toks), what=cfg.name)
+
+
 def test_many_items_per_cta():
     """256 experts with d_ff = 8192 give the decode gate/up GEMM about 90 work
     items per persistent CTA, more than the per-CTA item table holds, so the
