@@ -233,3 +233,21 @@ def test_layer_graph_replay(name):
     torch.cuda.synchronize()
     assert moe.last_device_error(g.ws) == 0
     assert_close_rms(out2.float().cpu().numpy(), L.oracle_forward(), what=name + " (new inputs)")
+
+
+@pytest.mark.parametrize("fmt,E,k", [("int4", 64, 2), ("fp8", 32, 2), ("bf16", 32, 6), ("int4", 256, 4)])
+def test_one_launch_routing_matches_separate_kernels(fmt, E, k):
+    """Up to 64 tokens route, permute and gather in one launch; 65 tokens take the
+    separate kernels.
+    The same 64 tokens plus a copy of token 0 must give the first 64 output rows
+    bit for bit (same experts and row-chunk width, so the same GEMM tiling)."""
+    cfg = ms.LayerConfig("fused_vs_split", T=64, d=256, F=256, E=E, k=k, fmt=fmt, seed=41 + E)
+    L = GpuLayer(cfg)
+    out64, ws64 = L.forward()
+    x65 = torch.cat([L.x, L.x[:1]], 0).contiguous()
+    lg65 = torch.cat([L.logits, L.logits[:1]], 0).contiguous()
+    out65, ws65 = moe.layer_forward(x65, lg65, cfg.k, L.routed, L.shared)
+    torch.cuda.synchronize()
+    assert moe.last_device_error(ws64) == 0 and moe.last_device_error(ws65) == 0
+    assert torch.equal(out64.view(torch.int16), out65[:64].view(torch.int16))
+    assert_close_rms(out64.float().cpu().numpy()[:8], L.oracle_forward(range(8)), what=cfg.name)
