@@ -16,7 +16,6 @@ constexpr int MAX_E = 256;
 constexpr int MAX_K = 16;
 constexpr int MAX_A = 1 << 20;
 constexpr int MAX_DIM = 32768;
-constexpr int TARGET_ITEMS = 640;   // down-GEMM work items to aim for when picking a K split
 constexpr int MAX_KSPLIT = 8;
 constexpr int SPLIT_GRID = 152;     // persistent CTAs the decode split is balanced for (GB300 SMs)
 
@@ -96,10 +95,12 @@ moe_status check_pool(const moe_pool* p, bool single) {
 // Largest chunk of one expert's rows that one work item covers (the B tile height).
 // K split of the down GEMM.  Decode (group kernel): the split whose items
 // spread most evenly over the persistent CTAs (fewest quantisation groups on
-// the busiest CTA; its fp32 partials are small).  Otherwise: enough items to
-// fill the GPU, as few splits as that allows (partials of long batches are
-// large).
-int choose_ksplit(int A, int E, bool has_shared, int bn, int fmt, int d, int F) {
+// the busiest CTA; its fp32 partials are small).  Otherwise the same count of
+// waves times groups per item, each group priced at its MMA time or its weight
+// streaming time (whichever is longer, from nominal per-SM rates), plus the
+// fp32 partials each split writes and the combine reads back (rows x d x 8
+// bytes per split, large for long batches).
+int choose_ksplit(int A, int E, bool has_shared, int bn, int fmt, int d, int F, int rows) {
   const int active = (A < E ? A : E) + (has_shared ? 1 : 0);
   const int mean = (A + E - 1) / E;
   const int nch = mean > bn ? (mean + bn - 1) / bn : 1;
@@ -116,9 +117,22 @@ int choose_ksplit(int A, int E, bool has_shared, int bn, int fmt, int d, int F) 
     }
     return best_s;
   }
-  int s = (int)((TARGET_ITEMS + items - 1) / items);
-  if (s > smax) s = smax;
-  return s < 1 ? 1 : s;
+  const double sm_flops = 1.9e15 / SPLIT_GRID, sm_bytes = 6.8e12 / SPLIT_GRID;   // per SM per s
+  const int tiles = down_paired(fmt, d / TILE_M) ? 2 : 1;                        // output tiles per item
+  const double wbytes = fmt == MOE_W_BF16 ? 2.0 : (double)quant_mat_bytes(fmt) / (TILE_M * QGROUP);
+  const double chunk_rows = mean < bn ? mean : bn;
+  const double t_mma = 2.0 * tiles * TILE_M * chunk_rows * QGROUP / sm_flops;
+  const double t_stream = tiles * TILE_M * QGROUP * wbytes / sm_bytes;
+  const double t_group = t_mma > t_stream ? t_mma : t_stream;
+  const double t_split = (double)rows * d * 8.0 / 6.8e12;
+  int best_s = 1;
+  double best = -1.0;
+  for (int s = 1; s <= smax; ++s) {
+    const long waves = (items * s + SPLIT_GRID - 1) / SPLIT_GRID;
+    const double cost = (double)waves * ((G + s - 1) / s) * t_group + s * t_split;
+    if (best < 0 || cost < best) { best = cost; best_s = s; }
+  }
+  return best_s;
 }
 
 // The int4 decode GEMMs' e4m3 operands (see gemm_group.cu): the gathered rows
@@ -163,7 +177,7 @@ LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* s
   L.d = routed->d_model;
   L.F = routed->d_ff;
   L.bn = choose_bn(L.A, L.E, routed->fmt);
-  L.ksplit = choose_ksplit(L.A, L.E, shared != nullptr, L.bn, routed->fmt, L.d, L.F);
+  L.ksplit = choose_ksplit(L.A, L.E, shared != nullptr, L.bn, routed->fmt, L.d, L.F, L.rows);
   size_t o = 0;
   L.err = o;      o += 1024;
   L.idx = o;      o = up1k(o + (size_t)L.A * 4);
@@ -455,7 +469,7 @@ FfnLayout ffn_layout(int A, const moe_pool* pool) {
   FfnLayout L{};
   const int d = pool->d_model, F = pool->d_ff;
   L.bn = choose_bn(A, pool->n_experts, pool->fmt);
-  L.ksplit = choose_ksplit(A, pool->n_experts, false, L.bn, pool->fmt, d, F);
+  L.ksplit = choose_ksplit(A, pool->n_experts, false, L.bn, pool->fmt, d, F, A);
   const bool f16 = gemm_uses_fp16(pool->fmt);
   L.fp8 = gemm_is_group(pool->fmt, L.bn);
   size_t o = 1024;
