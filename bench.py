@@ -420,16 +420,15 @@ def run_ours(args, cfg):
         streaming[mode_name] = copied / (s0.elapsed_time(s1) / 1e3) / 1e9
         del cache, hot
 
-    # ---- end to end through the public API: pinned host in, pinned host out
-    x_h = x.cpu().pin_memory()
-    lg_h = logits.cpu().pin_memory()
-    out_h = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    # ---- end to end through the public API: pinned host in, pinned host out.
+    # The captured step includes the copies of x and the logits from pinned
+    # host buffers and of the output back to a pinned host buffer.
+    eg = moe.LayerGraph(cfg.T, cfg.k, routed, shared, device=dev, host_io=True)
+    eg.x_host.copy_(x.cpu())
+    eg.logits_host.copy_(logits.cpu())
 
     def e2e_step():
-        lg.x.copy_(x_h, non_blocking=True)
-        lg.logits.copy_(lg_h, non_blocking=True)
-        lg.replay()
-        out_h.copy_(lg.out, non_blocking=True)
+        eg.replay()
 
     for _ in range(max(args.warmup, 3)):
         e2e_step()
@@ -442,6 +441,8 @@ def run_ours(args, cfg):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    if not torch.equal(eg.out_host.view(torch.int16), lg.out.cpu().view(torch.int16)):
+        raise SystemExit("end-to-end output differs from the device-resident step")
 
     ms_step = total_ms / args.steps
     value = world * cfg.T * args.steps / (total_ms / 1e3)

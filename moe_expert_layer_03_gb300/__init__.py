@@ -390,10 +390,15 @@ class LayerGraph:
     serves every input of the same shape.  Replaying saves the host launch
     work and shortens the gaps between the layer's kernels (decode steps are
     a few hundred microseconds).
+
+    host_io=True also captures the copies from pinned host buffers
+    ``self.x_host`` / ``self.logits_host`` into the device inputs and from
+    ``self.out`` back to ``self.out_host``: one replay is then a whole step from
+    host memory to host memory (read ``out_host`` after synchronising).
     """
 
     def __init__(self, T: int, k: int, routed: PoolView, shared: PoolView | None = None,
-                 device=None):
+                 device=None, host_io: bool = False):
         dev = torch.device(device) if device is not None else routed.e2s.device
         E, d = routed.struct.n_experts, routed.struct.d_model
         self.k, self.routed, self.shared = k, routed, shared
@@ -401,6 +406,11 @@ class LayerGraph:
         self.logits = torch.zeros(T, E, dtype=torch.float32, device=dev)
         self.out = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
         self.ws = workspace(layer_workspace_bytes(T, k, routed, shared), dev)
+        self.host_io = host_io
+        if host_io:
+            self.x_host = torch.zeros(T, d, dtype=torch.bfloat16).pin_memory()
+            self.logits_host = torch.zeros(T, E, dtype=torch.float32).pin_memory()
+            self.out_host = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
         side = torch.cuda.Stream(device=dev)
         side.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(side):
@@ -412,7 +422,12 @@ class LayerGraph:
         torch.cuda.current_stream(dev).wait_stream(side)
 
     def _forward(self):
+        if self.host_io:
+            self.x.copy_(self.x_host, non_blocking=True)
+            self.logits.copy_(self.logits_host, non_blocking=True)
         layer_forward(self.x, self.logits, self.k, self.routed, self.shared, out=self.out, ws=self.ws)
+        if self.host_io:
+            self.out_host.copy_(self.out, non_blocking=True)
 
     def replay(self) -> torch.Tensor:
         self.graph.replay()

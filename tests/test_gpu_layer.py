@@ -251,3 +251,18 @@ def test_one_launch_routing_matches_separate_kernels(fmt, E, k):
     assert moe.last_device_error(ws64) == 0 and moe.last_device_error(ws65) == 0
     assert torch.equal(out64.view(torch.int16), out65[:64].view(torch.int16))
     assert_close_rms(out64.float().cpu().numpy()[:8], L.oracle_forward(range(8)), what=cfg.name)
+
+
+def test_layer_graph_host_io():
+    """The captured step with its host copies (LayerGraph(host_io=True)): inputs
+    from pinned host buffers, output back to one, bit-identical to the eager call."""
+    L = GpuLayer(SMALL["int4_shared_perm"])
+    cfg = L.cfg
+    g = moe.LayerGraph(cfg.T, cfg.k, L.routed, L.shared, host_io=True)
+    g.x_host.copy_(L.x.cpu())
+    g.logits_host.copy_(L.logits.cpu())
+    g.replay()
+    torch.cuda.synchronize()
+    out_e, _ = L.forward()
+    assert moe.last_device_error(g.ws) == 0
+    assert torch.equal(g.out_host.view(torch.int16), out_e.cpu().view(torch.int16))
