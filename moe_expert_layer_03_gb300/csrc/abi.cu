@@ -144,21 +144,24 @@ struct Fp8Rows {
   float *xs, *xe;
   uint8_t* hq;
   float* hs;
+  float* skp;   // the gate/up GEMM's stream-K partial slots [grid][2][128][bn]
 };
 struct Fp8Offsets {
-  size_t xq, xs, xe, hq, hs;
+  size_t xq, xs, xe, hq, hs, skp;
 };
 // Appends the e4m3 regions at offset o (1 KB aligned) and returns the new end.
-size_t fp8_regions(Fp8Offsets& f, size_t o, int rows, int d, int F) {
+size_t fp8_regions(Fp8Offsets& f, size_t o, int rows, int d, int F, int bn) {
   f.xq = o;  o = up1k(o + 2 * (size_t)rows * d);
   f.xs = o;  o = up1k(o + (size_t)(d / QGROUP) * rows * 4 + SUMS_PAD_BYTES);
   f.xe = o;  o = up1k(o + (size_t)rows * 4);
   f.hq = o;  o = up1k(o + 2 * (size_t)rows * F);
   f.hs = o;  o = up1k(o + (size_t)(F / QGROUP) * rows * 8 + SUMS_PAD_BYTES);
+  f.skp = o; o = up1k(o + (size_t)sm_count() * 2 * TILE_M * bn * 4);
   return o;
 }
 Fp8Rows fp8_rows(uint8_t* W, const Fp8Offsets& f) {
-  return Fp8Rows{W + f.xq, (float*)(W + f.xs), (float*)(W + f.xe), W + f.hq, (float*)(W + f.hs)};
+  return Fp8Rows{W + f.xq, (float*)(W + f.xs), (float*)(W + f.xe), W + f.hq, (float*)(W + f.hs),
+                 (float*)(W + f.skp)};
 }
 
 struct LayerLayout {
@@ -190,7 +193,7 @@ LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* s
   L.xperm = o;    o = up1k(o + (L.fp8 ? 0 : (size_t)L.rows * L.d * 2));
   L.h = o;        o = up1k(o + (L.fp8 ? 0 : (size_t)L.rows * L.F * 2));
   L.part = o;     o = up1k(o + (size_t)L.ksplit * L.rows * L.d * 4);
-  if (L.fp8) o = fp8_regions(L.f8, o, L.rows, L.d, L.F);
+  if (L.fp8) o = fp8_regions(L.f8, o, L.rows, L.d, L.F, L.bn);
   L.total = o;
   return L;
 }
@@ -255,6 +258,10 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
     g.b_scale = f8->xe;
     g.q_out = f8->hq;
     g.sum_out = f8->hs;
+    if (grid + 1 <= 256) {   // ready flags after the error word, in the workspace's 1 KB error region
+      g.sk_part = f8->skp;
+      g.sk_flags = err + 1;
+    }
   }
   if (launch_grouped_gemm(fmt, true, mx, g, plan_gemm(fmt, true, bn, n_groups, F / TILE_M), grid, s,
                           pdl) != cudaSuccess)
@@ -476,7 +483,7 @@ FfnLayout ffn_layout(int A, const moe_pool* pool) {
   L.h = o;     o = up1k(o + (L.fp8 ? 0 : (size_t)A * F * 2));
   L.part = o;  o = up1k(o + (size_t)L.ksplit * A * d * 4);
   L.x16 = o;   o = up1k(o + (f16 && !L.fp8 ? (size_t)A * d * 2 : 0));
-  if (L.fp8) o = fp8_regions(L.f8, o, A, d, F);
+  if (L.fp8) o = fp8_regions(L.f8, o, A, d, F, L.bn);
   L.total = o;
   return L;
 }

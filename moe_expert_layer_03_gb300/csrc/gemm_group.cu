@@ -78,13 +78,16 @@ enum GroupMode { G_GATEUP = 0, G_DOWN_PAIR = 1, G_DOWN = 2 };
 // block in the order {0,4,1,5,2,6,3,7}.
 __host__ __device__ constexpr int k_slot(int e) { return e < 4 ? 2 * e : 2 * (e - 4) + 1; }
 
-// A work item decoded once per CTA (the decode needs integer divisions by
-// run-time values, which every warp would otherwise repeat).
+// A work item (or, under the stream-K split, a segment of one) decoded once
+// per CTA (the decode needs integer divisions by run-time values, which every
+// warp would otherwise repeat).
 struct ItemDesc {
   const uint8_t* slot;   // nullptr: the item is skipped (bad expert slot)
-  int g0, g1;            // quantisation groups [g0, g1) of its K split
+  int g0, g1;            // quantisation groups [g0, g1) of its K split (or segment)
   int r0, n_rows;        // token rows
   int mt, ks;            // output tile (pair) and K split
+  int kind;              // 0 whole item; 1 its trailing groups, handed to the CTA before;
+                         // 2 its leading groups, finished here with the next CTA's part
 };
 constexpr int G_ITEM_TAB = 64;   // items per CTA kept in the table; later ones are decoded on the fly
 
@@ -118,6 +121,7 @@ struct GShared {
   uint64_t *acc_full, *acc_empty;  // accumulator slices: MMA (commit) -> fold, fold -> MMA
   uint64_t* epi;                   // [2] gate/up epilogue hand-offs among the fold warps
   uint64_t* fin;
+  uint64_t* sk;                    // stream-K: the fold warps' partial sums are written
   int* misc;
   WorkList W;
 };
@@ -133,7 +137,7 @@ size_t group_carve_bytes(bool f8w, int nmat, int bn, bool gateup, int n_st, int 
   size_t s = (size_t)n_st * ((size_t)bn * 256 + group_raw_stage(f8w, nmat, bn, gateup));
   s += sizeof(ItemDesc) * G_ITEM_TAB + 2 * 4 * 32 * sizeof(float);
   s = align_up(s, 16);
-  s += 8 * (size_t)(2 * n_st + 2 * G_MAX_NA + 2 * G_MAX_NBUF + 2 + 1);
+  s += 8 * (size_t)(2 * n_st + 2 * G_MAX_NA + 2 * G_MAX_NBUF + 2 + 1 + 1);
   s += 4 * (G_MISC + worklist_ints(n_groups));
   return s;
 }
@@ -147,6 +151,7 @@ __device__ __forceinline__ ItemDesc make_item_desc(int item, const GemmArgs& p, 
   d.n_rows = it.n_rows;
   d.mt = it.mt;
   d.ks = it.ks;
+  d.kind = 0;
   return d;
 }
 
@@ -215,7 +220,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   S.acc_empty = S.acc_full + G_MAX_NBUF;
   S.epi = S.acc_empty + G_MAX_NBUF;
   S.fin = S.epi + 2;
-  S.misc = reinterpret_cast<int*>(S.fin + 1);
+  S.sk = S.fin + 1;
+  S.misc = reinterpret_cast<int*>(S.sk + 1);
   S.W.prefix = S.misc + G_MISC;
   S.W.nch = S.W.prefix + (p.n_groups + 1);
   S.W.goff = S.W.nch + (p.n_groups + 1);
@@ -239,6 +245,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&S.epi[i]), G_NFOLD * 32);
     mbar_init(smem_u32(S.fin), G_NMMA);
+    mbar_init(smem_u32(S.sk), G_NFOLD * 32);
     for (int i = 1; i < G_MISC; ++i)
       if (i != 2) S.misc[i] = 0;   // [0] written by tcgen05.alloc, [2] by the first unpack warp
     fence_mbar_init();
@@ -255,9 +262,41 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   if (warp == G_UP0) {
     const int total = build_worklist(p, S.W, lane);
     __syncwarp();
-    const int n_mine = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-    for (int i = lane; i < n_mine && i < G_ITEM_TAB; i += 32)
-      S.items[i] = make_item_desc(blockIdx.x + i * gridDim.x, p, S.W);
+    // Stream-K (gate/up): the items' quantisation groups in one sequence, an
+    // equal share of it per CTA, so the last wave is never a partial one.  An
+    // item cut between CTAs c and c + 1 is finished by c (its leading groups
+    // come last in c's share) with the partial sums c + 1 hands over (its
+    // trailing groups come first in c + 1's share).  Only when every share
+    // holds at least one whole item (an item spans at most two CTAs), and only
+    // when whole items would leave the last wave well short of full: the
+    // shares scatter the CTAs over the whole pool at once, which measured a
+    // few percent slower than whole items taken in step (a last wave 89% full,
+    // 896 items on 152 CTAs, is better left alone; one 34% full, 660 items, is
+    // not).
+    const int G = p.K / QGROUP;
+    const long long units = (long long)total * G;
+    const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
+    const long long whole_waves = ((long long)total + gridDim.x - 1) / gridDim.x;
+    const bool sk = GATEUP && p.sk_part != nullptr && p.ksplit == 1 && units >= (long long)gridDim.x * G &&
+                    (u1 - u0) / G + 2 <= G_ITEM_TAB && whole_waves * gridDim.x * 100 > (long long)total * 108;
+    int n_mine;
+    if (sk) {
+      const int first = (int)(u0 / G), last = (int)((u1 - 1) / G);
+      n_mine = last - first + 1;
+      for (int i = lane; i < n_mine; i += 32) {
+        const int item = first + i;
+        ItemDesc dsc = make_item_desc(item, p, S.W);
+        const long long ib = (long long)item * G;
+        dsc.g0 = (int)((u0 > ib ? u0 : ib) - ib);
+        dsc.g1 = (int)((u1 < ib + G ? u1 : ib + G) - ib);
+        dsc.kind = dsc.g0 > 0 ? 1 : (dsc.g1 < G ? 2 : 0);
+        S.items[i] = dsc;
+      }
+    } else {
+      n_mine = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+      for (int i = lane; i < n_mine && i < G_ITEM_TAB; i += 32)
+        S.items[i] = make_item_desc(blockIdx.x + i * gridDim.x, p, S.W);
+    }
     if (lane == 0) S.misc[2] = n_mine;
   }
   tc_fence_before();
@@ -534,6 +573,46 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         rc.next();
       }
       if (!ok) break;
+
+      if constexpr (GATEUP) {
+        if (it.kind == 1) {   // trailing groups: hand the partial sums to the CTA before
+          float* part = p.sk_part + (size_t)blockIdx.x * (NMAT * TILE_M * GBN);
+#pragma unroll
+          for (int m = 0; m < NM; ++m)
+#pragma unroll
+            for (int i = 0; i < CW; ++i)
+              if (i < nc) part[((m0 + m) * TILE_M + r) * GBN + c0 + i] = acc[m][i];
+          __threadfence();
+          mbar_arrive(smem_u32(S.sk));   // at most one such segment per CTA: phase 0
+          if (warp == G_FOLD0 && lane == 0 && mbar_wait(smem_u32(S.sk), 0, abort_flag, p.err))
+            st_release_gpu(p.sk_flags + blockIdx.x, 1);
+          continue;
+        }
+        if (it.kind == 2) {   // leading groups: add the next CTA's partial sums of the item
+          const int* flag = p.sk_flags + blockIdx.x + 1;
+          if (ld_acquire_gpu(flag) == 0) {
+            const uint64_t t0 = global_timer_ns();
+            while (ok && ld_acquire_gpu(flag) == 0) {
+              if (*abort_flag) ok = false;
+              else if (global_timer_ns() - t0 > MOE_WAIT_LIMIT_NS) {
+                *abort_flag = 1;
+                atomicOr(p.err, MOE_DEVERR_TIMEOUT);
+                ok = false;
+              }
+            }
+          }
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          const float* part = p.sk_part + (size_t)(blockIdx.x + 1) * (NMAT * TILE_M * GBN);
+#pragma unroll
+          for (int m = 0; m < NM; ++m)
+#pragma unroll
+            for (int i = 0; i < CW; ++i)
+              if (i < nc) acc[m][i] += part[((m0 + m) * TILE_M + r) * GBN + c0 + i];
+        }
+      }
 
       // ---- item epilogue from the register accumulators
       if constexpr (GATEUP) {

@@ -119,6 +119,12 @@ struct GemmArgs {
   const float* b_scale;
   uint8_t* q_out;
   float* sum_out;
+  // decode gate/up, stream-K split (gemm_group.cu): per CTA one partial
+  // accumulator slot [grid][2][128][bn] and one ready flag [grid] (the flags
+  // live in the workspace's error region and are zeroed by the forward's first
+  // kernel).  null: every CTA takes whole items.
+  float* sk_part;
+  int* sk_flags;
   int n_a, n_b, n_raw;                  // pipeline depths
   uint32_t tmem_cols;                   // TMEM columns (power of two >= 32)
 };
@@ -224,6 +230,7 @@ cudaError_t launch_combine_bf16(const uint16_t* y_perm, const int32_t* row_of_as
                                 uint16_t* out, cudaStream_t s);
 cudaError_t launch_reduce_splits(const float* part, int n_split, size_t split_stride, int rows,
                                  int d, uint16_t* y, cudaStream_t s, bool pdl = false);
+// Zeroes the 256 words of a workspace's error region (error word + GEMM flags).
 cudaError_t launch_clear_word(int* p, cudaStream_t s);
 cudaError_t launch_prepack(int fmt, int d, int F, const moe_expert_src& src, uint8_t* dst,
                            cudaStream_t s);

@@ -34,8 +34,10 @@ constexpr int PERM_MAX_E = 256;
 
 // histogram, scan and stable scatter of the A = T*k expert ids, by one CTA of
 // NT threads (which all call it).  The arrays may be global or shared memory.
-// err (nullable): cleared first (first kernel of the pipeline that reports
-// device errors), then ORed with MOE_DEVERR_EXPERT_RANGE for an id outside [0, E).
+// err (nullable): the workspace's 1 KB error region, cleared first (first
+// kernel of the pipeline that reports device errors; the region also holds the
+// decode GEMM's ready flags), then the error word ORed with
+// MOE_DEVERR_EXPERT_RANGE for an id outside [0, E).
 template <int NT>
 __device__ __forceinline__ void permute_cta(const int32_t* idx, int T, int k, int E, int t_shared,
                                             int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
@@ -48,7 +50,8 @@ __device__ __forceinline__ void permute_cta(const int32_t* idx, int T, int k, in
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int A = T * k;
 
-  if (err != nullptr && tid == 0) *err = 0;
+  if (err != nullptr)   // the error word and the rest of its 1 KB region (the GEMMs' ready flags)
+    for (int i = tid; i < 256; i += NT) err[i] = 0;
   for (int e = tid; e < E; e += NT) s_cnt[e] = 0;
   __syncthreads();
   bool bad = false;
@@ -422,7 +425,7 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, i
                        T, d, x_perm);
 }
 
-__global__ void clear_word_kernel(int* p) { *p = 0; }
+__global__ void clear_word_kernel(int* p) { p[threadIdx.x] = 0; }   // 256 words
 cudaError_t launch_gather_rows_fp8(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
                                    int d, uint8_t* xq, float* xs, float* xe, int n_sm, cudaStream_t s,
                                    bool pdl) {
@@ -433,7 +436,7 @@ cudaError_t launch_gather_rows_fp8(const uint16_t* x, const int32_t* token_of_ro
 }
 
 cudaError_t launch_clear_word(int* p, cudaStream_t s) {
-  clear_word_kernel<<<1, 1, 0, s>>>(p);
+  clear_word_kernel<<<1, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

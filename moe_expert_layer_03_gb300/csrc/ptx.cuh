@@ -123,6 +123,16 @@ MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, 
   }
 }
 
+// GPU-scope acquire load / release store of a flag in global memory.
+MOE_DEV int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+MOE_DEV void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // ------------------------------------------------------------------ async copies
 // One contiguous global -> shared copy; both addresses 16-byte aligned, bytes % 16 == 0.
 MOE_DEV void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

@@ -52,6 +52,11 @@ SMALL = {
     # ... and the prefill kernel (fp16 A dequantised into TMEM): paired and odd tile counts
     "fp8_chunk64": ms.LayerConfig("fp8_chunk64", T=96, d=256, F=384, E=8, k=2, fmt="fp8", seed=15),
     "fp8_wide_odd": ms.LayerConfig("fp8_wide_odd", T=96, d=384, F=512, E=4, k=2, fmt="fp8", seed=16),
+    # decode gate/up with ~200 work items on the persistent CTAs: a short last
+    # wave, so the GEMM splits the items' groups evenly (stream-K) and CTAs hand
+    # partial sums of the items cut between them to their neighbours
+    "int4_streamk": ms.LayerConfig("int4_streamk", T=16, d=256, F=3200, E=8, k=2, fmt="int4", seed=17),
+    "fp8_streamk": ms.LayerConfig("fp8_streamk", T=16, d=384, F=3200, E=8, k=2, fmt="fp8", seed=18),
 }
 
 
