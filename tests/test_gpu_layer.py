@@ -132,6 +132,11 @@ def test_layer_full_size_sampled(name):
     ms.LayerConfig("max_f", T=5, d=128, F=32768, E=2, k=2, fmt="fp8", seed=32),
     # many assignments: 160000 rows through the multi-tile permutation and GEMMs
     ms.LayerConfig("large_A", T=20000, d=128, F=128, E=64, k=8, fmt="bf16", seed=33),
+    # prefill-size layers on the persistent full-tile kernels: about 256 down
+    # work items (one whole wave and a short last one) and 128 (fewer than CTAs)
+    ms.LayerConfig("int4_prefill_tail", T=1024, d=4096, F=1024, E=8, k=2, fmt="int4", seed=34),
+    ms.LayerConfig("int4_prefill_allsplit", T=512, d=4096, F=1024, E=8, k=2, fmt="int4", seed=36),
+    ms.LayerConfig("bf16_prefill_tail", T=512, d=4096, F=1024, E=8, k=2, fmt="bf16", seed=35),
 ], ids=lambda c: c.name)
 def test_size_limits_sampled(cfg):
     L = GpuLayer(cfg)
