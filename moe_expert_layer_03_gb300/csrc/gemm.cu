@@ -410,17 +410,18 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
           uint32_t acc1[16];
           tmem_ld_16(tl + (uint32_t)(p.bn + c * 16), acc1);
           tmem_ld_wait();
+          const int nv = it.n_rows - c * 16;   // valid token columns of the chunk (> 0)
+          const size_t o0 = (size_t)(it.r0 + c * 16) * p.out_ld + f;
+          uint16_t* hout = reinterpret_cast<uint16_t*>(p.out);
+          // Two tokens per conversion (one packed cvt instead of two scalar
+          // ones, which share the quarter-rate unit with the exponentials).
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int n = c * 16 + i;
-            if (n < it.n_rows) {
-              const float hv = silu_f(__uint_as_float(acc0[i])) * __uint_as_float(acc1[i]);
-              const size_t o = (size_t)(it.r0 + n) * p.out_ld + f;
-              if (INT4)
-                reinterpret_cast<__half*>(p.out)[o] = to_half_sat(hv);
-              else
-                reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(hv);
-            }
+          for (int i = 0; i < 16; i += 2) {
+            const float h0 = silu_f(__uint_as_float(acc0[i])) * __uint_as_float(acc1[i]);
+            const float h1 = silu_f(__uint_as_float(acc0[i + 1])) * __uint_as_float(acc1[i + 1]);
+            const uint32_t pk = INT4 ? half2_bits_sat(h0, h1) : bf162_bits(h0, h1);
+            if (i < nv) hout[o0 + (size_t)i * p.out_ld] = (uint16_t)(pk & 0xFFFFu);
+            if (i + 1 < nv) hout[o0 + (size_t)(i + 1) * p.out_ld] = (uint16_t)(pk >> 16);
           }
         } else {
           float* y = reinterpret_cast<float*>(p.out) + (size_t)it.ks * p.out_split_stride;

@@ -140,10 +140,21 @@ __device__ __forceinline__ void codes_minus_zero(uint32_t w, uint32_t nz_a, uint
   o[3] = h2_fma(lop3_and_or(hi, 0x00F000F0u, 0x64006400u), SIXTEENTH, nz_b);
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// silu(g) = g / (1 + e^-g) with the fast exponential and the approximate
+// quotient: for g below about -87, e^-g overflows and the quotient is 0 (the
+// limit); elsewhere a few ulp of fp32, far below the fp16/bf16 rounding of h.
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-__device__ __forceinline__ __half to_half_sat(float v) {
-  return __float2half_rn(fminf(fmaxf(v, -65504.f), 65504.f));
+// (a, b) -> fp16 pair (a in the low half), each saturated to the finite range
+// and rounded to nearest even.
+__device__ __forceinline__ uint32_t half2_bits_sat(float a, float b) {
+  const __half2 t = __floats2half2_rn(fminf(fmaxf(a, -65504.f), 65504.f), fminf(fmaxf(b, -65504.f), 65504.f));
+  return *reinterpret_cast<const uint32_t*>(&t);
+}
+// (a, b) -> bf16 pair (a in the low half), rounded to nearest even.
+__device__ __forceinline__ uint32_t bf162_bits(float a, float b) {
+  const __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&t);
 }
 
 }  // namespace gemm
