@@ -155,6 +155,23 @@ __device__ __forceinline__ ItemDesc make_item_desc(int item, const GemmArgs& p, 
   return d;
 }
 
+// The stream-K sequence takes the items output tile by output tile, each tile
+// over all experts' row chunks, instead of expert by expert: a share then holds
+// tiles of several experts, so the few experts with many token rows (whose
+// groups cost more to fold) do not all fall to a few neighbouring CTAs.
+// Position q -> item index (items of group g: its row chunks x tiles, chunk
+// fastest, one K split).
+__device__ __forceinline__ int tile_major_item(int q, int total, const GemmArgs& p, const WorkList& W) {
+  const int chunks = total / p.n_mt;   // row chunks over all groups
+  const int mt = q / chunks, j = q - mt * chunks;
+  int lo = 0, hi = p.n_groups - 1;   // last group whose first chunk is <= j
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (W.prefix[mid] / p.n_mt <= j) lo = mid; else hi = mid - 1;
+  }
+  return W.prefix[lo] + mt * W.nch[lo] + (j - W.prefix[lo] / p.n_mt);
+}
+
 // The CTA's i-th item (item index blockIdx.x + i * gridDim.x).
 __device__ __forceinline__ ItemDesc get_item(int i, const GemmArgs& p, const GShared& S) {
   if (i < G_ITEM_TAB) return S.items[i];
@@ -262,8 +279,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   if (warp == G_UP0) {
     const int total = build_worklist(p, S.W, lane);
     __syncwarp();
-    // Stream-K (gate/up): the items' quantisation groups in one sequence, an
-    // equal share of it per CTA, so the last wave is never a partial one.  An
+    // Stream-K (gate/up): the items' quantisation groups in one sequence
+    // (items in tile-major order), an equal share of it per CTA, so the last
+    // wave is never a partial one.  An
     // item cut between CTAs c and c + 1 is finished by c (its leading groups
     // come last in c's share) with the partial sums c + 1 hands over (its
     // trailing groups come first in c + 1's share).  Only when every share
@@ -284,9 +302,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       const int first = (int)(u0 / G), last = (int)((u1 - 1) / G);
       n_mine = last - first + 1;
       for (int i = lane; i < n_mine; i += 32) {
-        const int item = first + i;
-        ItemDesc dsc = make_item_desc(item, p, S.W);
-        const long long ib = (long long)item * G;
+        const int q = first + i;   // position in the sequence
+        ItemDesc dsc = make_item_desc(tile_major_item(q, total, p, S.W), p, S.W);
+        const long long ib = (long long)q * G;
         dsc.g0 = (int)((u0 > ib ? u0 : ib) - ib);
         dsc.g1 = (int)((u1 < ib + G ? u1 : ib + G) - ib);
         dsc.kind = dsc.g0 > 0 ? 1 : (dsc.g1 < G ? 2 : 0);
