@@ -57,6 +57,13 @@ SMALL = {
     # partial sums of the items cut between them to their neighbours
     "int4_streamk": ms.LayerConfig("int4_streamk", T=16, d=256, F=3200, E=8, k=2, fmt="int4", seed=17),
     "fp8_streamk": ms.LayerConfig("fp8_streamk", T=16, d=384, F=3200, E=8, k=2, fmt="fp8", seed=18),
+    # stream-K with skewed routing: row chunks with more than half a tile of
+    # rows next to small ones, experts with two row chunks and the shared
+    # expert in tile-major order; and 32-row chunks
+    "int4_streamk_skew": ms.LayerConfig("int4_streamk_skew", T=32, d=256, F=2560, E=8, k=2, fmt="int4",
+                                        logits="zipf", zipf_s=1.1, shared=True, slot_perm=True, seed=19),
+    "int4_streamk_g32": ms.LayerConfig("int4_streamk_g32", T=24, d=256, F=11136, E=3, k=2, fmt="int4",
+                                       seed=20),
 }
 
 
