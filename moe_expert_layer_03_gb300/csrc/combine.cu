@@ -68,14 +68,18 @@ __device__ __forceinline__ float4 y_from_partials(const float* part, int n_split
   return s;
 }
 
-template <bool OVERLAP>
+// V: 4-column vectors per thread (the CTA covers 1024 V columns); all of a
+// thread's loads for one expert row are issued before its adds.
+template <bool OVERLAP, int V>
 __global__ void __launch_bounds__(256)
     combine_partials_kernel(const float* __restrict__ part, int n_split, size_t split_stride,
                             const int32_t* __restrict__ row_of_assign,
                             const float* __restrict__ topk_w, int k, int d, int shared_row0,
                             uint16_t* __restrict__ out) {
   const int t = blockIdx.x;
-  const int c = (blockIdx.y * 256 + threadIdx.x) * 4;
+  int cv[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) cv[v] = ((blockIdx.y * V + v) * 256 + threadIdx.x) * 4;
   // The token's rows and weights come from the routing kernels, which finished
   // before the GEMM that precedes this kernel passed its own dependency wait,
   // so they are read before this kernel's wait (only the partial sums come
@@ -91,35 +95,43 @@ __global__ void __launch_bounds__(256)
     }
   griddep_wait();
   griddep_launch_dependents();
-  if (c >= d) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (cv[0] >= d) return;
+  float4 acc[V];
 #pragma unroll
-  for (int j = 0; j < PRE; ++j) {
-    if (j >= k || rj[j] < 0) continue;   // r < 0 only after an index error
-    const float4 y = y_from_partials<OVERLAP>(part, n_split, split_stride, rj[j], d, c);
-    acc.x += wj[j] * y.x;
-    acc.y += wj[j] * y.y;
-    acc.z += wj[j] * y.z;
-    acc.w += wj[j] * y.w;
-  }
-  for (int j = PRE; j < k; ++j) {
-    const int r = row_of_assign[t * k + j];
-    if (r < 0) continue;
-    const float w = topk_w[t * k + j];
-    const float4 y = y_from_partials<OVERLAP>(part, n_split, split_stride, r, d, c);
-    acc.x += w * y.x;
-    acc.y += w * y.y;
-    acc.z += w * y.z;
-    acc.w += w * y.w;
-  }
+  for (int v = 0; v < V; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto add_row = [&](int r, float w) {   // acc += w * y[r], this thread's columns
+    if (r < 0) return;                    // r < 0 only after an index error
+    float4 y[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+      if (cv[v] < d) y[v] = y_from_partials<OVERLAP>(part, n_split, split_stride, r, d, cv[v]);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      if (cv[v] >= d) continue;
+      acc[v].x += w * y[v].x;
+      acc[v].y += w * y[v].y;
+      acc[v].z += w * y[v].z;
+      acc[v].w += w * y[v].w;
+    }
+  };
+#pragma unroll
+  for (int j = 0; j < PRE; ++j)
+    if (j < k) add_row(rj[j], wj[j]);
+  for (int j = PRE; j < k; ++j) add_row(row_of_assign[t * k + j], topk_w[t * k + j]);
   if (shared_row0 >= 0) {
-    const float4 y = y_from_partials<OVERLAP>(part, n_split, split_stride, shared_row0 + t, d, c);
-    acc.x += y.x;
-    acc.y += y.y;
-    acc.z += y.z;
-    acc.w += y.w;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      if (cv[v] >= d) continue;
+      const float4 y = y_from_partials<OVERLAP>(part, n_split, split_stride, shared_row0 + t, d, cv[v]);
+      acc[v].x += y.x;
+      acc[v].y += y.y;
+      acc[v].z += y.z;
+      acc[v].w += y.w;
+    }
   }
-  store_bf16x4(out + (size_t)t * d + c, acc);
+#pragma unroll
+  for (int v = 0; v < V; ++v)
+    if (cv[v] < d) store_bf16x4(out + (size_t)t * d + cv[v], acc[v]);
 }
 
 __global__ void __launch_bounds__(256)
@@ -169,10 +181,11 @@ cudaError_t launch_combine_partials(const float* part, int n_split, size_t split
                                     bool pdl) {
   if (T <= 0) return cudaSuccess;
   if (T <= 256)
-    return launch_kernel(combine_partials_kernel<true>, grid_rows(T, d), dim3(256), 0, s, pdl, part,
+    return launch_kernel(combine_partials_kernel<true, 1>, grid_rows(T, d), dim3(256), 0, s, pdl, part,
                          n_split, split_stride, row_of_assign, topk_w, k, d, shared_row0, out);
-  return launch_kernel(combine_partials_kernel<false>, grid_rows(T, d), dim3(256), 0, s, pdl, part,
-                       n_split, split_stride, row_of_assign, topk_w, k, d, shared_row0, out);
+  return launch_kernel(combine_partials_kernel<false, 2>, dim3((unsigned)T, (unsigned)((d + 2047) / 2048)),
+                       dim3(256), 0, s, pdl, part, n_split, split_stride, row_of_assign, topk_w, k, d,
+                       shared_row0, out);
 }
 
 cudaError_t launch_combine_bf16(const uint16_t* y_perm, const int32_t* row_of_assign,

@@ -29,7 +29,7 @@
 namespace moe {
 
 constexpr int PERM_THREADS = 1024;
-constexpr int PERM_WARPS = PERM_THREADS / 32;
+constexpr int GATHER_UNROLL = 4;   // 16-byte row vectors a lane loads before storing any
 constexpr int PERM_MAX_E = 256;
 
 // histogram, scan and stable scatter of the A = T*k expert ids, by one CTA of
@@ -159,7 +159,15 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
       continue;
     }
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-    for (int i = lane; i < nvec; i += 32) dst[i] = __ldg(src + i);
+    for (int i0 = lane; i0 < nvec; i0 += 32 * GATHER_UNROLL) {   // loads first: 4 vectors in flight
+      uint4 v[GATHER_UNROLL];
+#pragma unroll
+      for (int u = 0; u < GATHER_UNROLL; ++u)
+        if (i0 + 32 * u < nvec) v[u] = __ldg(src + i0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < GATHER_UNROLL; ++u)
+        if (i0 + 32 * u < nvec) dst[i0 + 32 * u] = v[u];
+    }
   }
 }
 
@@ -186,16 +194,25 @@ __global__ void __launch_bounds__(256)
     const bool valid = (t >= 0 && t < T);
     uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * d);
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(valid ? t : 0) * d);
-    for (int i = lane; i < nvec; i += 32) {
-      uint4 o = make_uint4(0, 0, 0, 0);
-      if (valid) {
-        const uint4 v = __ldg(src + i);
-        o.x = bf16x2_to_f16x2(v.x);
-        o.y = bf16x2_to_f16x2(v.y);
-        o.z = bf16x2_to_f16x2(v.z);
-        o.w = bf16x2_to_f16x2(v.w);
+    for (int i0 = lane; i0 < nvec; i0 += 32 * GATHER_UNROLL) {   // loads first: 4 vectors in flight
+      uint4 v[GATHER_UNROLL];
+#pragma unroll
+      for (int u = 0; u < GATHER_UNROLL; ++u) {
+        v[u] = make_uint4(0, 0, 0, 0);
+        if (valid && i0 + 32 * u < nvec) v[u] = __ldg(src + i0 + 32 * u);
       }
-      dst[i] = o;
+#pragma unroll
+      for (int u = 0; u < GATHER_UNROLL; ++u) {
+        if (i0 + 32 * u >= nvec) continue;
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (valid) {
+          o.x = bf16x2_to_f16x2(v[u].x);
+          o.y = bf16x2_to_f16x2(v[u].y);
+          o.z = bf16x2_to_f16x2(v[u].z);
+          o.w = bf16x2_to_f16x2(v[u].w);
+        }
+        dst[i0 + 32 * u] = o;
+      }
     }
   }
 }
