@@ -432,3 +432,77 @@ class LayerGraph:
     def replay(self) -> torch.Tensor:
         self.graph.replay()
         return self.out
+
+
+class LayerPipeline:
+    """Host-to-host layer steps with the copies overlapped with compute.
+
+    Two slots of device inputs/outputs and pinned host buffers
+    (``x_host[s]``, ``logits_host[s]``, ``out_host[s]``).  Step i computes
+    slot i % 2 while a second stream copies step i - 1's output back to the
+    host and step i + 1's inputs in (both in the other slot), so on a stream
+    the copies run under the compute instead of around it.  One CUDA graph per
+    slot holds both branches; replays on one stream order the steps.
+
+        pipe.x_host[0][...] = ...; pipe.logits_host[0][...] = ...   # step 0
+        pipe.start()                      # copies step 0's inputs in
+        for i in range(n):
+            # before step i: the inputs of step i + 1 in the host slot (i + 1) % 2
+            pipe.step(i)
+        pipe.finish(n - 1)                # copies the last output out
+        torch.cuda.current_stream().synchronize()
+        # step i's output: out_host[i % 2], valid once step i + 1 (or finish) has run
+
+    The host slots of step i + 1's inputs must be filled before ``step(i)`` is
+    called, and ``out_host[i % 2]`` read before ``step(i + 2)`` overwrites it.
+    """
+
+    def __init__(self, T: int, k: int, routed: PoolView, shared: PoolView | None = None, device=None):
+        dev = torch.device(device) if device is not None else routed.e2s.device
+        E, d = routed.struct.n_experts, routed.struct.d_model
+        self.k, self.routed, self.shared = k, routed, shared
+        self.x = [torch.zeros(T, d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.logits = [torch.zeros(T, E, dtype=torch.float32, device=dev) for _ in range(2)]
+        self.out = [torch.zeros(T, d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.x_host = [torch.zeros(T, d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        self.logits_host = [torch.zeros(T, E, dtype=torch.float32).pin_memory() for _ in range(2)]
+        self.out_host = [torch.zeros(T, d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        self.ws = workspace(layer_workspace_bytes(T, k, routed, shared), dev)
+        self.copy_stream = torch.cuda.Stream(device=dev)
+        main = torch.cuda.Stream(device=dev)
+        main.wait_stream(torch.cuda.current_stream(dev))
+        self.graphs = []
+        with torch.cuda.stream(main):
+            self._forward(0)   # first call: one-time library set-up happens outside the capture
+            main.synchronize()
+            for s in range(2):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=main):
+                    self._step_body(s, main)
+                self.graphs.append(g)
+        torch.cuda.current_stream(dev).wait_stream(main)
+
+    def _forward(self, s: int):
+        layer_forward(self.x[s], self.logits[s], self.k, self.routed, self.shared, out=self.out[s], ws=self.ws)
+
+    def _step_body(self, s: int, main):
+        o = 1 - s
+        self.copy_stream.wait_stream(main)
+        with torch.cuda.stream(self.copy_stream):   # the other slot: last output out, next inputs in
+            self.out_host[o].copy_(self.out[o], non_blocking=True)
+            self.x[o].copy_(self.x_host[o], non_blocking=True)
+            self.logits[o].copy_(self.logits_host[o], non_blocking=True)
+        self._forward(s)
+        main.wait_stream(self.copy_stream)
+
+    def start(self):
+        """Copies step 0's inputs (host slot 0) to the device, on the current stream."""
+        self.x[0].copy_(self.x_host[0], non_blocking=True)
+        self.logits[0].copy_(self.logits_host[0], non_blocking=True)
+
+    def step(self, i: int):
+        self.graphs[i % 2].replay()
+
+    def finish(self, last: int):
+        """Copies the last step's output to ``out_host[last % 2]``, on the current stream."""
+        self.out_host[last % 2].copy_(self.out[last % 2], non_blocking=True)

@@ -283,3 +283,42 @@ def test_layer_graph_host_io():
     out_e, _ = L.forward()
     assert moe.last_device_error(g.ws) == 0
     assert torch.equal(g.out_host.view(torch.int16), out_e.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["int4_shared_perm", "int4_streamk_skew"])
+def test_layer_pipeline_steps(name):
+    """LayerPipeline: five host-to-host steps with different inputs (token rows
+    of x and the logits rolled by the step index), the copies of neighbouring
+    steps overlapped with compute; every step's output is bit-identical to the
+    eager call on that step's inputs."""
+    L = GpuLayer(SMALL[name])
+    cfg = L.cfg
+    pipe = moe.LayerPipeline(cfg.T, cfg.k, L.routed, L.shared)
+    xs = [torch.roll(L.x, i, dims=0).contiguous() for i in range(5)]
+    lgs = [torch.roll(L.logits, i, dims=0).contiguous() for i in range(5)]
+    want = []
+    for i in range(5):
+        out_e, ws = moe.layer_forward(xs[i], lgs[i], cfg.k, L.routed, L.shared)
+        torch.cuda.synchronize()
+        assert moe.last_device_error(ws) == 0
+        want.append(out_e.cpu())
+    got = [None] * 5
+    stream = torch.cuda.current_stream()
+    pipe.x_host[0].copy_(xs[0].cpu())
+    pipe.logits_host[0].copy_(lgs[0].cpu())
+    pipe.start()
+    for i in range(5):
+        if i + 1 < 5:   # step i + 1's inputs into the other host slot before step i runs
+            stream.synchronize()   # step i - 1 (which read that slot) is done
+            pipe.x_host[(i + 1) % 2].copy_(xs[i + 1].cpu())
+            pipe.logits_host[(i + 1) % 2].copy_(lgs[i + 1].cpu())
+        pipe.step(i)
+        if i >= 1:   # step i copied step i - 1's output out
+            stream.synchronize()
+            got[i - 1] = pipe.out_host[(i - 1) % 2].clone()
+    pipe.finish(4)
+    stream.synchronize()
+    got[4] = pipe.out_host[0].clone()
+    assert moe.last_device_error(pipe.ws) == 0
+    for i in range(5):
+        assert torch.equal(got[i].view(torch.int16), want[i].view(torch.int16)), f"step {i}"
