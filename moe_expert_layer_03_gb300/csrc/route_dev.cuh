@@ -5,7 +5,11 @@
 //
 // One warp routes one token: lane l holds logits l, l+32, ...; k rounds of a
 // warp arg-max on the key (value desc, expert index asc) pick the experts in
-// descending order; the weights are the softmax over the k selected logits.
+// descending order (E <= 32: a shuffle butterfly on the (value, index) pair
+// per round; E > 32: a warp max of an order-preserving integer key of the
+// value, then a warp min of the expert indices that hold it -- fewer dependent
+// steps, measured faster there and slower at E <= 32); the weights are the
+// softmax over the k selected logits.
 #pragma once
 #include <math.h>
 
@@ -13,9 +17,21 @@
 
 namespace moe {
 
-template <int VPL>   // logits per lane = ceil(E / 32)
-__device__ __forceinline__ void route_one_token(const float* __restrict__ logits, int tok, int E, int k,
-                                                int32_t* __restrict__ idx, float* __restrict__ w, int lane) {
+// Order-preserving 32-bit key of a float (larger float -> larger key; -0.0
+// is folded into +0.0 first so that equal values give equal keys) and back.
+__device__ __forceinline__ uint32_t route_key(float x) {
+  const uint32_t u = __float_as_uint(x == 0.f ? 0.f : x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float route_key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// E <= 32 (one logit per lane): a shuffle butterfly on (value, index).
+template <int VPL>
+__device__ __forceinline__ void route_one_token_small(const float* __restrict__ logits, int tok, int E,
+                                                      int k, int32_t* __restrict__ idx, float* __restrict__ w,
+                                                      int lane) {
   const float* row = logits + (size_t)tok * E;
   float v[VPL];
 #pragma unroll
@@ -62,6 +78,64 @@ __device__ __forceinline__ void route_one_token(const float* __restrict__ logits
 #pragma unroll
   for (int j = 0; j < 16; ++j)
     if (j < k && lane == j) w[(size_t)tok * k + j] = expf(sel[j] - m) / den;
+}
+
+// E > 32: per round two warp reductions on an order-preserving integer key.
+template <int VPL>
+__device__ __forceinline__ void route_one_token_large(const float* __restrict__ logits, int tok, int E,
+                                                      int k, int32_t* __restrict__ idx, float* __restrict__ w,
+                                                      int lane) {
+  const float* row = logits + (size_t)tok * E;
+  uint32_t key[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    float x = e < E ? __ldg(row + e) : -INFINITY;
+    key[i] = route_key((x != x) ? -INFINITY : x);   // NaN never outranks a number
+  }
+  uint32_t taken = 0;
+  float sel[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j < k) {
+      // my best untaken logit (ties: my lower index, i.e. the first one seen);
+      // experts past E have no candidate (key 0 and index INT_MAX never win)
+      uint32_t bk = 0;
+      int bi = 0x7FFFFFFF;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (bi == 0x7FFFFFFF || key[i] > bk)) {
+          bk = key[i];
+          bi = e;
+        }
+      }
+      // the warp's largest key, then the lowest expert index holding it
+      const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+      const int mi = __reduce_min_sync(0xffffffffu, (bi != 0x7FFFFFFF && bk == mk) ? bi : 0x7FFFFFFF);
+      if ((mi & 31) == lane) taken |= 1u << (mi >> 5);
+      sel[j] = route_key_value(mk);
+      if (lane == 0) idx[(size_t)tok * k + j] = mi;
+    }
+  }
+  // softmax over the selected logits, max-subtracted, summed in selection order
+  const float m = sel[0];
+  float den = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (j < k) den += expf(sel[j] - m);
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (j < k && lane == j) w[(size_t)tok * k + j] = expf(sel[j] - m) / den;
+}
+
+template <int VPL>   // logits per lane = ceil(E / 32)
+__device__ __forceinline__ void route_one_token(const float* __restrict__ logits, int tok, int E, int k,
+                                                int32_t* __restrict__ idx, float* __restrict__ w, int lane) {
+  if constexpr (VPL == 1)
+    route_one_token_small<VPL>(logits, tok, E, k, idx, w, lane);
+  else
+    route_one_token_large<VPL>(logits, tok, E, k, idx, w, lane);
 }
 
 }  // namespace moe
