@@ -89,6 +89,7 @@ struct ItemDesc {
   int kind;              // 0 whole item; 1 its trailing groups, handed to the CTA before;
                          // 2 its leading groups, finished here with the next CTA's part
 };
+constexpr int G_PREFETCH_STAGES = 8;   // weight stages a CTA prefetches into L2 before its dependency wait
 constexpr int G_ITEM_TAB = 64;   // items per CTA kept in the table; later ones are decoded on the fly
 
 // Per stage the producer also copies the item rows' entries of the token
@@ -271,6 +272,37 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   if (warp == 1) {
     tmem_alloc(smem_u32(&S.misc[0]), p.tmem_cols);
     tmem_relinquish();
+  }
+  // fp8 weights (a pure weight stream): before the dependency wait, prefetch
+  // into L2 the first weight stages of the item this CTA gets if every group
+  // is active with one row chunk (likely when the batch holds at least two
+  // rows per routed expert), so the stream starts while the previous kernel
+  // finishes (the 8-bit Mixtral-shaped decode step: 232 -> 224 us).  Only the
+  // expert-to-slot table is read (an input, not an earlier kernel's output); a
+  // wrong guess costs the prefetched bytes.  The int4 kernel, bound by its
+  // unpack, measured no gain and keeps no such code.
+  if constexpr (F8W && MODE != G_DOWN) {
+    if (warp == 0 && lane == 0 && p.rows_total >= 2 * p.n_routed) {
+      const int per_g = p.n_mt * p.ksplit;
+      const int g = (int)blockIdx.x / per_g;
+      if (g < p.n_groups) {
+        const int t2 = (int)blockIdx.x - g * per_g, ks = t2 % p.ksplit, mt = t2 / p.ksplit;
+        int g0, g1;
+        kgroups(p, ks, g0, g1);
+        const uint8_t* slot = nullptr;
+        if (g < p.n_routed) {
+          const int sl = p.e2s_r[g];
+          if (sl >= 0 && sl < p.n_slots_r) slot = p.pool_r + (size_t)sl * p.slot_bytes_r;
+        } else if (p.pool_s != nullptr) {
+          const int sl = p.e2s_s[0];
+          if (sl >= 0 && sl < p.n_slots_s) slot = p.pool_s + (size_t)sl * p.slot_bytes_s;
+        }
+        if (slot != nullptr)
+          for (int kg = g0; kg < g1 && kg < g0 + G_PREFETCH_STAGES; ++kg) {
+            prefetch_l2_bulk(slot + p.sec_off + ((size_t)mt * (p.K / QGROUP) + kg) * W_BYTES, W_BYTES);
+          }
+      }
+    }
   }
   // everything above overlaps the previous kernel's tail (dependent launch);
   // below, the offsets, token rows and outputs of earlier kernels are read

@@ -166,6 +166,10 @@ MOE_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, u
       "l"(map), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+// Bulk prefetch of global memory into L2; address 16-byte aligned, bytes % 16 == 0.
+MOE_DEV void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 MOE_DEV void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
