@@ -6,8 +6,10 @@
 // K-split partial sums of each expert output and uses them unrounded; the bf16
 // variant reads the bf16 y_perm of the standalone grouped-FFN entry point.
 //
-// One CTA per (token, 1024-column slab); each thread owns 4 consecutive columns
-// (16-byte fp32 / 8-byte bf16 vectors).
+// One CTA per (token, column slab); each thread owns 4 consecutive columns
+// (16-byte fp32 / 8-byte bf16 vectors) per vector: one vector (1024-column
+// slabs) for batches up to 256 tokens, two (2048-column slabs, twice the loads
+// in flight per thread) above.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
