@@ -166,8 +166,9 @@ Fp8Rows fp8_rows(uint8_t* W, const Fp8Offsets& f) {
 
 struct LayerLayout {
   int A, Tsh, rows, E, d, F, bn, ksplit;
-  bool fp8;   // int4 decode path: e4m3 operands instead of x_perm / h
-  size_t err, idx, w, counts, offsets, roa, tor, xperm, h, part, total;
+  bool fp8;   // quantised decode path: e4m3 operands instead of x_perm / h
+  bool f16;   // quantised prefill path: fp16 x_perm and h, scaled per row (xe: 2^-ex per row)
+  size_t err, idx, w, counts, offsets, roa, tor, xperm, xe, h, part, total;
   Fp8Offsets f8;
 };
 
@@ -190,7 +191,9 @@ LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* s
   L.roa = o;      o = up1k(o + (size_t)L.A * 4);
   L.tor = o;      o = up1k(o + (size_t)L.rows * 4);
   L.fp8 = gemm_is_group(routed->fmt, L.bn);
+  L.f16 = !L.fp8 && gemm_uses_fp16(routed->fmt);
   L.xperm = o;    o = up1k(o + (L.fp8 ? 0 : (size_t)L.rows * L.d * 2));
+  L.xe = o;       o = up1k(o + (L.f16 ? (size_t)L.rows * 4 : 0));
   L.h = o;        o = up1k(o + (L.fp8 ? 0 : (size_t)L.rows * L.F * 2));
   L.part = o;     o = up1k(o + (size_t)L.ksplit * L.rows * L.d * 4);
   if (L.fp8) o = fp8_regions(L.f8, o, L.rows, L.d, L.F, L.bn);
@@ -221,11 +224,12 @@ GemmArgs base_args(const moe_pool* routed, const moe_pool* shared, int* err) {
 }
 
 // gate/up (SwiGLU) then down over the row groups described by `offsets`.
-// x_rows and h are fp16 for int4 pools, bf16 otherwise; with f8 (the int4
-// decode path) the GEMMs read and write the e4m3 forms instead.  pdl: both
+// x_rows and h are fp16 for quantised pools (x_rows scaled per row, x_unscale =
+// 2^-ex per row), bf16 otherwise; with f8 (the quantised decode path) the GEMMs
+// read and write the e4m3 forms instead.  pdl: both
 // launches follow a kernel of the same call (dependent launch).
-moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups, int rows,
-                   const moe_pool* routed, const moe_pool* shared, int bn, int ksplit, uint16_t* h,
+moe_status run_ffn(const uint16_t* x_rows, const float* x_unscale, const int32_t* offsets, int n_groups,
+                   int rows, const moe_pool* routed, const moe_pool* shared, int bn, int ksplit, uint16_t* h,
                    float* part, const Fp8Rows* f8, int* err, cudaStream_t s, bool pdl,
                    cudaEvent_t ev_mid, cudaEvent_t ev_down) {
   const int d = routed->d_model, F = routed->d_ff, fmt = routed->fmt;
@@ -243,6 +247,8 @@ moe_status run_ffn(const uint16_t* x_rows, const int32_t* offsets, int n_groups,
   a.n_groups = n_groups;
   a.bn = bn;
   a.rows_total = rows;
+  a.trailer_off = slot_payload_bytes(fmt, d, F);
+  a.b_scale = x_unscale;   // the prefill GEMMs' per-row x unscale (decode gate/up: set below)
 
   GemmArgs g = a;   // gate/up + SwiGLU
   g.sec_off = 0;
@@ -325,9 +331,9 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
   int32_t* roa = (int32_t*)(W + L.roa);
   int32_t* tor = (int32_t*)(W + L.tor);
   uint16_t* xperm = (uint16_t*)(W + L.xperm);
+  float* xe = L.f16 ? (float*)(W + L.xe) : nullptr;
   uint16_t* h = (uint16_t*)(W + L.h);
   float* part = (float*)(W + L.part);
-  const bool f16 = gemm_uses_fp16(routed->fmt);
   const Fp8Rows f8 = L.fp8 ? fp8_rows(W, L.f8) : Fp8Rows{};
   auto rec = [&](int i) -> bool {
     return !ev || !ev[i] || cudaEventRecord((cudaEvent_t)ev[i], s) == cudaSuccess;
@@ -338,8 +344,8 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
 
   if (!rec(MOE_STAGE_ROUTE)) return MOE_ERR_CUDA;
   if (T <= FUSED_ROUTE_MAX_T) {   // one launch; its time is reported as the routing stage
-    const GatherDst dst{xperm, f8.xq, f8.xs, f8.xe};
-    const int out_kind = L.fp8 ? GATHER_FP8 : f16 ? GATHER_F16 : GATHER_BF16;
+    const GatherDst dst{xperm, f8.xq, f8.xs, L.fp8 ? f8.xe : xe};
+    const int out_kind = L.fp8 ? GATHER_FP8 : L.f16 ? GATHER_F16 : GATHER_BF16;
     if (launch_route_gather(logits, T, k, E, L.Tsh, x, L.d, idx, w, counts, offsets, roa, tor, err,
                             out_kind, dst, sm_count(), s, route_pdl && pdl) != cudaSuccess)
       return MOE_ERR_CUDA;
@@ -355,12 +361,15 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
       if (launch_gather_rows_fp8(x, tor, L.rows, T, L.d, f8.xq, f8.xs, f8.xe, sm_count(), s, pdl) !=
           cudaSuccess)
         return MOE_ERR_CUDA;
-    } else if (launch_gather_rows(x, tor, L.rows, T, L.d, xperm, f16, sm_count(), s, pdl) != cudaSuccess) {
+    } else if (L.f16) {
+      if (launch_gather_rows_f16(x, tor, L.rows, T, L.d, xperm, xe, sm_count(), s, pdl) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    } else if (launch_gather_rows(x, tor, L.rows, T, L.d, xperm, sm_count(), s, pdl) != cudaSuccess) {
       return MOE_ERR_CUDA;
     }
   }
   if (!rec(MOE_STAGE_GATE_UP)) return MOE_ERR_CUDA;
-  st = run_ffn(xperm, offsets, E + (shared ? 1 : 0), L.rows, routed, shared, L.bn, L.ksplit, h, part,
+  st = run_ffn(xperm, xe, offsets, E + (shared ? 1 : 0), L.rows, routed, shared, L.bn, L.ksplit, h, part,
                L.fp8 ? &f8 : nullptr, err, s, pdl, ev ? (cudaEvent_t)ev[MOE_STAGE_DOWN] : nullptr,
                ev ? (cudaEvent_t)ev[MOE_STAGE_COMBINE] : nullptr);
   if (st != MOE_OK) return st;
@@ -392,7 +401,7 @@ size_t moe_slot_bytes(int fmt, int d_model, int d_ff) {
   if ((fmt != MOE_W_BF16 && !fmt_quantised(fmt)) || d_model < 128 || d_ff < 128 ||
       d_model % 128 || d_ff % 128)
     return 0;
-  return gateup_section_bytes(fmt, d_model, d_ff) + down_section_bytes(fmt, d_model, d_ff);
+  return slot_payload_bytes(fmt, d_model, d_ff) + SLOT_TRAILER_BYTES;
 }
 
 moe_status moe_prepack_expert(int fmt, int d_model, int d_ff, const moe_expert_src* src,
@@ -457,18 +466,19 @@ moe_status moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int k,
   if (launch_permute_index(topk_idx, T, k, E, 0, counts, offsets, row_of_assign, token_of_row, err,
                            s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (launch_gather_rows(x, token_of_row, T * k, T, d, x_perm, false, sm_count(), s, true) !=
+  if (launch_gather_rows(x, token_of_row, T * k, T, d, x_perm, sm_count(), s, true) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
-// Workspace of the standalone grouped FFN: error word, h, down partials and, for
-// int4 pools, an fp16 copy of x_perm, or (decode path) the e4m3 operands.
+// Workspace of the standalone grouped FFN: error word, h, down partials and,
+// for quantised pools, the scaled fp16 copy of x_perm with its per-row unscale
+// factors (prefill path) or the e4m3 operands (decode path).
 struct FfnLayout {
   int bn, ksplit;
   bool fp8;
-  size_t h, part, x16, total;
+  size_t h, part, x16, xe, total;
   Fp8Offsets f8;
 };
 
@@ -483,6 +493,7 @@ FfnLayout ffn_layout(int A, const moe_pool* pool) {
   L.h = o;     o = up1k(o + (L.fp8 ? 0 : (size_t)A * F * 2));
   L.part = o;  o = up1k(o + (size_t)L.ksplit * A * d * 4);
   L.x16 = o;   o = up1k(o + (f16 && !L.fp8 ? (size_t)A * d * 2 : 0));
+  L.xe = o;    o = up1k(o + (f16 && !L.fp8 ? (size_t)A * 4 : 0));
   if (L.fp8) o = fp8_regions(L.f8, o, A, d, F, L.bn);
   L.total = o;
   return L;
@@ -510,20 +521,22 @@ moe_status moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int A
   cudaStream_t s = (cudaStream_t)stream;
   const bool f16 = gemm_uses_fp16(pool->fmt);
   const uint16_t* rows_in = x_perm;
+  float* xe = nullptr;
   const Fp8Rows f8 = L.fp8 ? fp8_rows(W, L.f8) : Fp8Rows{};
   if (launch_clear_word(err, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (L.fp8) {   // the int4 decode GEMMs read e4m3 rows
+  if (L.fp8) {   // the quantised decode GEMMs read e4m3 rows
     if (launch_gather_rows_fp8(x_perm, nullptr, A, A, pool->d_model, f8.xq, f8.xs, f8.xe, sm_count(), s,
                                true) != cudaSuccess)
       return MOE_ERR_CUDA;
-  } else if (f16) {   // the other int4 GEMMs read fp16 rows
+  } else if (f16) {   // the quantised prefill GEMMs read scaled fp16 rows
     uint16_t* x16 = (uint16_t*)(W + L.x16);
-    if (launch_gather_rows(x_perm, nullptr, A, A, pool->d_model, x16, true, sm_count(), s, true) !=
+    xe = (float*)(W + L.xe);
+    if (launch_gather_rows_f16(x_perm, nullptr, A, A, pool->d_model, x16, xe, sm_count(), s, true) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     rows_in = x16;
   }
-  st = run_ffn(rows_in, offsets, pool->n_experts, A, pool, nullptr, L.bn, L.ksplit, h, part,
+  st = run_ffn(rows_in, xe, offsets, pool->n_experts, A, pool, nullptr, L.bn, L.ksplit, h, part,
                L.fp8 ? &f8 : nullptr, err, s, true, nullptr, nullptr);
   if (st != MOE_OK) return st;
   return launch_reduce_splits(part, L.ksplit, (size_t)A * pool->d_model, A, pool->d_model, y_perm,

@@ -6,7 +6,11 @@
 // two-layer MLP; the tokens of each expert form one contiguous batch and the
 // active experts run as one grouped GEMM instead of many small ones; sec. 3.1 --
 // per-expert int4 weights with their own scale and zero-point, dequantised to
-// fp16 for the tensor cores on the way in rather than in a separate pass.
+// fp16 for the tensor cores on the way in rather than in a separate pass.  The
+// fp16 token rows and h are scaled per row by powers of two so that neither
+// can leave fp16's range: x by its row maximum (the gather), h by a bound from
+// x's row maximum and the expert's largest gate / up row L1 norms (the slot
+// trailer, h_row_scale); the scales are undone in fp32.
 //
 // One persistent CTA per SM walks a list of work items
 //   (expert group g, 128-row weight tile mt, K split ks, row chunk nc)
@@ -113,6 +117,19 @@ __device__ __forceinline__ void dequant_fp8(const uint8_t* codes, int r, int c0,
       }
     }
   }
+}
+
+// h's fp16 scale for one token row of a quantised prefill GEMM: x entered as
+// fp16 x * 2^ex with max|x| * 2^ex < 2^14 (ux = 2^-ex), and every gate / up
+// output of the row is at most max|x| * 2^Bg / * 2^Bu (bsum = Bg + Bu, the slot
+// trailer's bound exponents), so |h| = |silu(g) u| <= |g| |u| <
+// 2^(28 - 2 ex + bsum).  Returns 2^eh with eh = 2 ex - 13 - bsum, which keeps
+// |h| 2^eh below 2^15 (fp16's largest finite value is 65504); *inv = 2^-eh.
+__device__ __forceinline__ float h_row_scale(float ux, int bsum, float* inv) {
+  const int ex = 127 - (int)(__float_as_uint(ux) >> 23);
+  const int eh = max(-126, min(126, 2 * ex - 13 - bsum));
+  *inv = __int_as_float((127 - eh) << 23);
+  return __int_as_float((127 + eh) << 23);
 }
 
 }  // namespace
@@ -402,23 +419,41 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
       tc_fence_after();
       const int half = wr >> 2;
       const int n_chunks = (it.n_rows + 15) >> 4;
+      // quantised weights: token row n entered the MMA as fp16 x * 2^ex_n
+      // (b_scale[n] = 2^-ex_n) and h is stored as fp16 h * 2^eh_n, eh_n from ex_n
+      // and the expert's bound exponents in the slot trailer (h_row_scale)
+      int bsum = 0;
+      if constexpr (INT4) {
+        const int2 bb = *reinterpret_cast<const int2*>(it.slot + p.trailer_off + 8);
+        bsum = bb.x + bb.y;
+      }
       for (int c = half; c < n_chunks; c += NHALF) {
         uint32_t acc0[16];
         tmem_ld_16(tl + (uint32_t)(c * 16), acc0);
+        const int nv = it.n_rows - c * 16;   // valid token columns of the chunk (> 0)
+        const float* ux_c = p.b_scale + it.r0 + c * 16;
         if (GATEUP) {
           const int f = it.mt * TILE_M + r;   // output feature of this thread
           uint32_t acc1[16];
           tmem_ld_16(tl + (uint32_t)(p.bn + c * 16), acc1);
           tmem_ld_wait();
-          const int nv = it.n_rows - c * 16;   // valid token columns of the chunk (> 0)
           const size_t o0 = (size_t)(it.r0 + c * 16) * p.out_ld + f;
           uint16_t* hout = reinterpret_cast<uint16_t*>(p.out);
           // Two tokens per conversion (one packed cvt instead of two scalar
           // ones, which share the quarter-rate unit with the exponentials).
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {
-            const float h0 = silu_f(__uint_as_float(acc0[i])) * __uint_as_float(acc1[i]);
-            const float h1 = silu_f(__uint_as_float(acc0[i + 1])) * __uint_as_float(acc1[i + 1]);
+            float g0 = __uint_as_float(acc0[i]), u0 = __uint_as_float(acc1[i]);
+            float g1 = __uint_as_float(acc0[i + 1]), u1 = __uint_as_float(acc1[i + 1]);
+            if constexpr (INT4) {   // undo x's row scale (exact), apply h's (u * 2^-ex * 2^eh)
+              float inv;
+              const float x0 = i < nv ? __ldg(ux_c + i) : 1.f, x1 = i + 1 < nv ? __ldg(ux_c + i + 1) : 1.f;
+              g0 *= x0;
+              u0 *= x0 * h_row_scale(x0, bsum, &inv);
+              g1 *= x1;
+              u1 *= x1 * h_row_scale(x1, bsum, &inv);
+            }
+            const float h0 = silu_f(g0) * u0, h1 = silu_f(g1) * u1;
             const uint32_t pk = INT4 ? half2_bits_sat(h0, h1) : bf162_bits(h0, h1);
             if (i < nv) hout[o0 + (size_t)i * p.out_ld] = (uint16_t)(pk & 0xFFFFu);
             if (i + 1 < nv) hout[o0 + (size_t)(i + 1) * p.out_ld] = (uint16_t)(pk >> 16);
@@ -427,15 +462,22 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
           float* y = reinterpret_cast<float*>(p.out) + (size_t)it.ks * p.out_split_stride;
           uint32_t acc1[16];
           if (PAIR) tmem_ld_16(tl + (uint32_t)(p.bn + c * 16), acc1);
+          float hu[16];   // quantised: 2^-eh of each token row (h's scale undone), else 1
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            hu[i] = 1.f;
+            if constexpr (INT4) {
+              if (i < nv) h_row_scale(__ldg(ux_c + i), bsum, &hu[i]);
+            }
+          }
           tmem_ld_wait();
 #pragma unroll
           for (int m = 0; m < NMAT; ++m) {
             const int f = (PAIR ? 2 * it.mt + m : it.mt) * TILE_M + r;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const int n = c * 16 + i;
-              if (n < it.n_rows)
-                y[(size_t)(it.r0 + n) * p.out_ld + f] = __uint_as_float(m == 0 ? acc0[i] : acc1[i]);
+              if (i < nv)
+                y[(size_t)(it.r0 + c * 16 + i) * p.out_ld + f] = __uint_as_float(m == 0 ? acc0[i] : acc1[i]) * hu[i];
             }
           }
         }

@@ -13,12 +13,15 @@
 //     e4m3 number q * 2^-9, so one AND (and one shift per 8 codes) makes the
 //     operand; it lives in tensor memory (tcgen05.st), one TMEM lane per
 //     weight row;
-//   * the B operand is the token rows in e4m3 too, each row scaled by a power
-//     of two and split into hi + lo parts that hold a bf16 value exactly (the
-//     gather kernel and this kernel's gate/up epilogue write them); the hi
-//     tile and the lo tile below it form one B operand of 2 x bn rows, so
-//     one MMA per K step and matrix covers both, and the fold adds the hi and
-//     lo columns of the accumulator;
+//   * the B operand is the token rows in e4m3 too, each row (h: each row's
+//     128-feature block) scaled by a power of two that puts its largest
+//     magnitude m in [128, 256), then split into hi = e4m3(v) and
+//     lo = e4m3(v - hi) (the gather kernel and this kernel's gate/up epilogue
+//     write them): hi + lo is the bf16 value exactly for every element of at
+//     least m / 512, and within 2^-17 m for the smaller ones; the hi tile and
+//     the lo tile below it form one B operand of 2 x bn rows, so one MMA per K
+//     step and matrix covers both, and the fold adds the hi and lo columns of
+//     the accumulator;
 //   * the MMA is tcgen05.mma kind::f8f6f4 (K = 32), A from TMEM;
 //   * each quantisation group (K = 128) accumulates into its own TMEM slice,
 //     folded into fp32 registers with the group's scale s and zero z:
@@ -702,7 +705,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             const float am = fmaxf(fmaxf(S.red[t], S.red[32 + t]), fmaxf(S.red[64 + t], S.red[96 + t]));
             int ex = 0;
             if (am > 0.f) frexpf(am, &ex);
-            const int e = max(-126, min(127, am > 0.f ? 8 - ex : 0));
+            const int e = max(-126, min(126, am > 0.f ? 8 - ex : 0));   // 2^e, 2^-e normal
             const float x = hv[i] * __int_as_float((127 + e) << 23);
             const uint16_t hb = f32x2_to_e4m3x2(x, 0.f);
             const float hf = e4m3x2_to_f32x2(hb).x;

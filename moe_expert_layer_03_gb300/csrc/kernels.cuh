@@ -83,6 +83,18 @@ __host__ __device__ inline size_t down_section_bytes(int fmt, int d, int F) {
   return fmt_quantised(fmt) ? (size_t)(d / TILE_M) * (F / QGROUP) * quant_mat_bytes(fmt)
                             : (size_t)(d / TILE_M) * (F / KSTEP) * BF16_TILE_BYTES;
 }
+// Every slot ends in a 256-byte trailer after its two sections (both sections
+// are multiples of 256 bytes, so the trailer keeps the slot 256-byte aligned):
+//   float  L[2]   largest row L1 norm of the dequantised gate ([0]) and up ([1])
+//                 weights, sum_k |w[n][k]| (accumulated by the prepack)
+//   int32  B[2]   ceil(log2(L[m] * (1 + 2^-7))): powers of two that bound every
+//                 gate / up output of a token row x by max|x| * 2^B[m]
+// The quantised prefill GEMM sizes the fp16 scale of h from B (gemm.cu); the
+// bf16 formats leave the trailer zero.
+constexpr int SLOT_TRAILER_BYTES = 256;
+__host__ __device__ inline size_t slot_payload_bytes(int fmt, int d, int F) {
+  return gateup_section_bytes(fmt, d, F) + down_section_bytes(fmt, d, F);
+}
 
 // ------------------------------------------------------------------ grouped GEMM
 // Row group g (an expert, or the shared expert appended as the last group) owns
@@ -125,6 +137,10 @@ struct GemmArgs {
   // kernel).  null: every CTA takes whole items.
   float* sk_part;
   int* sk_flags;
+  // quantised prefill GEMMs (gemm.cu): the token rows are fp16 copies of x
+  // scaled per row by 2^ex (b_scale holds 2^-ex per row), h is fp16 scaled per
+  // row by 2^eh, eh from ex and the slot trailer's bounds (at trailer_off)
+  unsigned long long trailer_off;
   int n_a, n_b, n_raw;                  // pipeline depths
   uint32_t tmem_cols;                   // TMEM columns (power of two >= 32)
 };
@@ -139,7 +155,8 @@ struct GemmPlan {
 };
 
 // Quantised layers run their prefill-size GEMMs on fp16 operands (x_perm and h
-// are fp16); bf16 layers on bf16 operands.
+// are fp16, each row scaled by a power of two, see gemm.cu); bf16 layers on
+// bf16 operands.
 inline bool gemm_uses_fp16(int fmt) { return fmt_quantised(fmt); }
 
 // Uses the group-scaled decode kernel (int4 or fp8, row chunks of <= 32)?
@@ -197,9 +214,10 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_
                                  int32_t* token_of_row, int* err, cudaStream_t s, bool pdl = false);
 // Routing, permutation and row gather in one launch, for batches of up to
 // FUSED_ROUTE_MAX_T tokens: the outputs of launch_route_topk,
-// launch_permute_index and the row gather (out: GATHER_BF16 / GATHER_F16 into
-// dst.x16 [rows][d], or GATHER_FP8 into dst.xq/xs/xe, the int4 decode GEMM's
-// e4m3 form), rows = T*k (+ t_shared).
+// launch_permute_index and the row gather (out: GATHER_BF16 into dst.x16
+// [rows][d]; GATHER_F16 into dst.x16 and dst.xe, the scaled fp16 rows of
+// launch_gather_rows_f16; GATHER_FP8 into dst.xq/xs/xe, the quantised decode
+// GEMMs' e4m3 form), rows = T*k (+ t_shared).
 constexpr int FUSED_ROUTE_MAX_T = 64;
 enum { GATHER_BF16 = 0, GATHER_F16 = 1, GATHER_FP8 = 2 };
 struct GatherDst {
@@ -211,11 +229,16 @@ cudaError_t launch_route_gather(const float* logits, int T, int k, int E, int t_
                                 int d, int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
                                 int32_t* row_of_assign, int32_t* token_of_row, int* err, int out,
                                 const GatherDst& dst, int n_sm, cudaStream_t s, bool pdl = false);
-// x_perm[r] = x[token_of_row[r]].  to_fp16: write fp16 (saturating) instead of
-// bf16.  token_of_row == nullptr: x_perm[r] = x[r].
+// x_perm[r] = x[token_of_row[r]] (bf16).  token_of_row == nullptr: x_perm[r] = x[r].
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
-                               int d, uint16_t* x_perm, bool to_fp16, int n_sm, cudaStream_t s,
-                               bool pdl = false);
+                               int d, uint16_t* x_perm, int n_sm, cudaStream_t s, bool pdl = false);
+// The quantised prefill GEMMs' fp16 rows: x16[r] = fp16(x[token_of_row[r]] *
+// 2^ex_r) with ex_r putting the row's largest magnitude in [2^13, 2^14) (exact
+// for bf16 inputs down to 2^-27 of that magnitude), xe[r] = 2^-ex_r.
+// token_of_row == nullptr: rows of x in order.
+cudaError_t launch_gather_rows_f16(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
+                                   int d, uint16_t* x16, float* xe, int n_sm, cudaStream_t s,
+                                   bool pdl = false);
 // The int4 decode GEMM's e4m3 form of the gathered rows (see permute.cu):
 // xq [2*rows][d] bytes (hi rows, then lo rows), xs [d/128][rows], xe [rows].
 cudaError_t launch_gather_rows_fp8(const uint16_t* x, const int32_t* token_of_row, int rows, int T,

@@ -171,19 +171,31 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
   }
 }
 
-// bf16 -> fp16 (saturating) pair
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
-  const float a = fminf(fmaxf(__uint_as_float(u << 16), -65504.f), 65504.f);
-  const float b = fminf(fmaxf(__uint_as_float(u & 0xFFFF0000u), -65504.f), 65504.f);
-  const __half2 h = __floats2half2_rn(a, b);
+// The quantised prefill GEMMs read fp16 rows scaled by a power of two: the
+// row's largest magnitude m goes to [2^13, 2^14), so no element overflows fp16
+// and every bf16 element of at least 2^-27 m (fp16's normal range) converts
+// exactly (8 significant bits fit fp16's 11).  Returns 2^ex; *inv = 2^-ex.
+__device__ __forceinline__ float f16_row_scale(float m, float* inv) {
+  int ex = 0;
+  if (m > 0.f) frexpf(m, &ex);               // m = f * 2^ex, f in [0.5, 1)
+  int sc = m > 0.f ? 14 - ex : 0;            // m * 2^sc in [2^13, 2^14)
+  sc = max(-126, min(126, sc));              // 2^sc and 2^-sc both normal fp32
+  *inv = __int_as_float((127 - sc) << 23);
+  return __int_as_float((127 + sc) << 23);
+}
+// bf16 pair * mul -> fp16 pair (mul a power of two, no overflow by the choice of mul)
+__device__ __forceinline__ uint32_t bf16x2_scaled_f16x2(uint32_t u, float mul) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(u << 16) * mul, __uint_as_float(u & 0xFFFF0000u) * mul);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
+__device__ __forceinline__ float bf16x2_absmax(uint32_t u) {
+  return fmaxf(fabsf(__uint_as_float(u << 16)), fabsf(__uint_as_float(u & 0xFFFF0000u)));
+}
 
-// Same gather, converting to fp16 (token_of_row == nullptr: row r of x, a plain
-// conversion).
+// One warp per row: the row's largest magnitude, then the scaled fp16 copy.
 __global__ void __launch_bounds__(256)
     gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ token_of_row,
-                           int rows, int T, int d, uint16_t* __restrict__ x_perm) {
+                           int rows, int T, int d, uint16_t* __restrict__ x16, float* __restrict__ xe) {
   griddep_launch_dependents();
   griddep_wait();
   const int lane = threadIdx.x & 31;
@@ -192,8 +204,19 @@ __global__ void __launch_bounds__(256)
        r += (int)((gridDim.x * blockDim.x) >> 5)) {
     const int t = token_of_row != nullptr ? token_of_row[r] : r;   // nullptr: rows in order
     const bool valid = (t >= 0 && t < T);
-    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * d);
+    uint4* dst = reinterpret_cast<uint4*>(x16 + (size_t)r * d);
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(valid ? t : 0) * d);
+    float m = 0.f;
+    if (valid)
+      for (int i = lane; i < nvec; i += 32) {
+        const uint4 v = __ldg(src + i);
+        m = fmaxf(m, fmaxf(fmaxf(bf16x2_absmax(v.x), bf16x2_absmax(v.y)),
+                           fmaxf(bf16x2_absmax(v.z), bf16x2_absmax(v.w))));
+      }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float inv;
+    const float mul = f16_row_scale(m, &inv);
     for (int i0 = lane; i0 < nvec; i0 += 32 * GATHER_UNROLL) {   // loads first: 4 vectors in flight
       uint4 v[GATHER_UNROLL];
 #pragma unroll
@@ -204,26 +227,26 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
       for (int u = 0; u < GATHER_UNROLL; ++u) {
         if (i0 + 32 * u >= nvec) continue;
-        uint4 o = make_uint4(0, 0, 0, 0);
-        if (valid) {
-          o.x = bf16x2_to_f16x2(v[u].x);
-          o.y = bf16x2_to_f16x2(v[u].y);
-          o.z = bf16x2_to_f16x2(v[u].z);
-          o.w = bf16x2_to_f16x2(v[u].w);
-        }
-        dst[i0 + 32 * u] = o;
+        dst[i0 + 32 * u] = make_uint4(bf16x2_scaled_f16x2(v[u].x, mul), bf16x2_scaled_f16x2(v[u].y, mul),
+                                      bf16x2_scaled_f16x2(v[u].z, mul), bf16x2_scaled_f16x2(v[u].w, mul));
       }
     }
+    if (lane == 0) xe[r] = inv;
   }
 }
 
-// The int4 decode GEMM's B operand is e4m3: each gathered row r is scaled by
-// a power of two 2^e_r (its largest magnitude lands in [128, 256)) and split
-// into hi = e4m3(x 2^e) and lo = e4m3(x 2^e - hi), which together hold a bf16
-// value exactly.  Within every 8-element block the elements are stored in the
-// order {0,4,1,5,2,6,3,7}, the K order in which the GEMM unpacks the weight
-// nibbles.  Writes xq [2*rows][d] (hi rows, then lo rows), xs [d/128][rows]
-// (per-group sums of hi + lo) and xe [rows] (2^-e).
+// The quantised decode GEMMs' B operand is e4m3: each gathered row r is
+// scaled by a power of two 2^e_r (its largest magnitude m lands in [128, 256))
+// and split into hi = e4m3(x 2^e) and lo = e4m3(x 2^e - hi).  For a bf16 x with
+// |x 2^e| >= 2^-2 (every element of at least m / 512) the residual x 2^e - hi
+// is a multiple of x's bf16 ulp no larger than half an ulp of hi, so it has at
+// most 4 significant bits on e4m3's grid and hi + lo == x 2^e exactly; a
+// smaller element keeps an absolute error of at most 2^-10 (half the e4m3
+// subnormal step), i.e. below 2^-17 m before scaling.  Within every 8-element
+// block the elements are stored in the order {0,4,1,5,2,6,3,7}, the K order in
+// which the GEMM unpacks the weight nibbles.  Writes xq [2*rows][d] (hi rows,
+// then lo rows), xs [d/128][rows] (per-group sums of hi + lo) and xe [rows]
+// (2^-e).
 // fp8_row: one row by the NT threads of a CTA (src == nullptr: a zero row);
 // a half-warp covers one 128-element group.  red: NT/32 floats of shared memory.
 template <int NT>
@@ -256,7 +279,7 @@ __device__ __forceinline__ void fp8_row(const uint16_t* __restrict__ src, int r,
   int ex = 0;
   if (m > 0.f) frexpf(m, &ex);               // m = f * 2^ex, f in [0.5, 1)
   int sc = m > 0.f ? 8 - ex : 0;             // m * 2^sc in [128, 256)
-  sc = max(-126, min(127, sc));
+  sc = max(-126, min(126, sc));              // 2^sc and 2^-sc both normal fp32
   const float mul = __int_as_float((127 + sc) << 23);
   const float inv = __int_as_float((127 - sc) << 23);
   uint8_t* hi_row = xq + (size_t)r * d;
@@ -315,25 +338,50 @@ __global__ void __launch_bounds__(FP8_GATHER_THREADS)
   }
 }
 
-// x_perm row = x row (bf16 copy, or saturating fp16 conversion), by the NT
-// threads of a CTA; src == nullptr: a zero row.
-template <int NT, bool F16>
+// x_perm row = x row (bf16 copy), by the NT threads of a CTA; src == nullptr: a
+// zero row.
+template <int NT>
 __device__ __forceinline__ void copy_row(const uint16_t* __restrict__ src, int d, uint16_t* __restrict__ dst) {
   const uint4* vs = reinterpret_cast<const uint4*>(src);
   uint4* vd = reinterpret_cast<uint4*>(dst);
+  for (int i = threadIdx.x; i < d / 8; i += NT) vd[i] = src != nullptr ? __ldg(vs + i) : make_uint4(0, 0, 0, 0);
+}
+
+// The scaled fp16 row of gather_rows_f16_kernel, by the NT threads of a CTA
+// (src == nullptr: a zero row); red: NT/32 floats of shared memory.
+template <int NT>
+__device__ __forceinline__ void f16_row(const uint16_t* __restrict__ src, int d, uint16_t* __restrict__ dst,
+                                        float* __restrict__ xe_r, float* red) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint4* vs = reinterpret_cast<const uint4*>(src);
+  uint4* vd = reinterpret_cast<uint4*>(dst);
+  float m = 0.f;
+  if (src != nullptr)
+    for (int i = threadIdx.x; i < d / 8; i += NT) {
+      const uint4 v = __ldg(vs + i);
+      m = fmaxf(m, fmaxf(fmaxf(bf16x2_absmax(v.x), bf16x2_absmax(v.y)), fmaxf(bf16x2_absmax(v.z), bf16x2_absmax(v.w))));
+    }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  m = red[0];
+#pragma unroll
+  for (int i = 1; i < NW; ++i) m = fmaxf(m, red[i]);
+  __syncthreads();   // red is rewritten for the next row
+  float inv;
+  const float mul = f16_row_scale(m, &inv);
   for (int i = threadIdx.x; i < d / 8; i += NT) {
     uint4 o = make_uint4(0, 0, 0, 0);
     if (src != nullptr) {
-      o = __ldg(vs + i);
-      if (F16) {
-        o.x = bf16x2_to_f16x2(o.x);
-        o.y = bf16x2_to_f16x2(o.y);
-        o.z = bf16x2_to_f16x2(o.z);
-        o.w = bf16x2_to_f16x2(o.w);
-      }
+      const uint4 v = __ldg(vs + i);
+      o = make_uint4(bf16x2_scaled_f16x2(v.x, mul), bf16x2_scaled_f16x2(v.y, mul), bf16x2_scaled_f16x2(v.z, mul),
+                     bf16x2_scaled_f16x2(v.w, mul));
     }
     vd[i] = o;
   }
+  if (threadIdx.x == 0) *xe_r = inv;
 }
 
 // ------------------------------------------------------------------ fused
@@ -381,8 +429,10 @@ __global__ void __launch_bounds__(RG_THREADS, 1)
     const uint16_t* src = (t >= 0 && t < T) ? x + (size_t)t * d : nullptr;
     if (OUT == GATHER_FP8)
       fp8_row<RG_THREADS>(src, r, rows, d, dst.xq, dst.xs, dst.xe, s_red);
+    else if (OUT == GATHER_F16)
+      f16_row<RG_THREADS>(src, d, dst.x16 + (size_t)r * d, dst.xe + r, s_red);
     else
-      copy_row<RG_THREADS, OUT == GATHER_F16>(src, d, dst.x16 + (size_t)r * d);
+      copy_row<RG_THREADS>(src, d, dst.x16 + (size_t)r * d);
   }
 }
 
@@ -430,16 +480,21 @@ cudaError_t launch_route_gather(const float* logits, int T, int k, int E, int t_
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
-                               int d, uint16_t* x_perm, bool to_fp16, int n_sm, cudaStream_t s,
-                               bool pdl) {
+                               int d, uint16_t* x_perm, int n_sm, cudaStream_t s, bool pdl) {
   if (rows <= 0) return cudaSuccess;
   int blocks = (rows + 7) / 8;   // 8 warps (rows) per block
   if (blocks > 4 * n_sm) blocks = 4 * n_sm;
-  if (to_fp16)
-    return launch_kernel(gather_rows_f16_kernel, dim3(blocks), dim3(256), 0, s, pdl, x, token_of_row,
-                         rows, T, d, x_perm);
   return launch_kernel(gather_rows_kernel, dim3(blocks), dim3(256), 0, s, pdl, x, token_of_row, rows,
                        T, d, x_perm);
+}
+
+cudaError_t launch_gather_rows_f16(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
+                                   int d, uint16_t* x16, float* xe, int n_sm, cudaStream_t s, bool pdl) {
+  if (rows <= 0) return cudaSuccess;
+  int blocks = (rows + 7) / 8;   // 8 warps (rows) per block
+  if (blocks > 4 * n_sm) blocks = 4 * n_sm;
+  return launch_kernel(gather_rows_f16_kernel, dim3(blocks), dim3(256), 0, s, pdl, x, token_of_row, rows,
+                       T, d, x16, xe);
 }
 
 __global__ void clear_word_kernel(int* p) { p[threadIdx.x] = 0; }   // 256 words

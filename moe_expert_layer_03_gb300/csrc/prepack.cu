@@ -144,6 +144,53 @@ __global__ void prepack_fp8_kernel(const uint8_t* __restrict__ q0, const uint16_
   }
 }
 
+// Slot trailer (kernels.cuh): largest row L1 norm of a quantised matrix [rows][K]
+// in its canonical form, one warp per row, sum_k |w| in fp32 with w the
+// dequantised value ((q - z) * s for int4, e4m3(q) * s for fp8); the row maxima
+// meet in trailer float m by an integer atomicMax (non-negative floats order
+// like their bit patterns).
+__global__ void row_l1_max_kernel(int fmt, const uint8_t* __restrict__ q, const uint16_t* __restrict__ sc,
+                                  const uint16_t* __restrict__ zr, int rows, int K, float* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int G = K / QGROUP;
+  for (int row = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); row < rows;
+       row += (int)((gridDim.x * blockDim.x) >> 5)) {
+    float acc = 0.f;
+    for (int k = lane; k < K; k += 32) {
+      const int g = k / QGROUP;
+      const float s = __half2float(__ushort_as_half(sc[(size_t)row * G + g]));
+      float w;
+      if (fmt == MOE_W_INT4_G128) {
+        const uint8_t b = q[(size_t)row * (K / 2) + (k >> 1)];
+        const int code = (k & 1) ? (b >> 4) : (b & 15);
+        w = ((float)code - __half2float(__ushort_as_half(zr[(size_t)row * G + g]))) * s;
+      } else {
+        const uint16_t pair = q[(size_t)row * K + k];
+        w = e4m3x2_to_f32x2(pair).x * s;
+      }
+      acc += fabsf(w);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) atomicMax(reinterpret_cast<int*>(out), __float_as_int(acc));
+  }
+}
+
+// trailer B[m] = ceil(log2(L[m] * (1 + 2^-7))) (the margin covers the fp16
+// rounding of the GEMM's weights and the fp32 sums), clamped to [-126, 127].
+__global__ void trailer_bounds_kernel(uint8_t* trailer) {
+  const int m = threadIdx.x;
+  if (m >= 2) return;
+  const float L = reinterpret_cast<const float*>(trailer)[m] * (1.0f + 0.0078125f);
+  int b = -126;
+  if (L > 0.f) {
+    int e;
+    const float f = frexpf(L, &e);   // L = f * 2^e, f in [0.5, 1)
+    b = f == 0.5f ? e - 1 : e;       // smallest b with L <= 2^b
+  }
+  reinterpret_cast<int*>(trailer + 8)[m] = max(-126, min(127, b));
+}
+
 cudaError_t launch_prepack(int fmt, int d, int F, const moe_expert_src& src, uint8_t* dst,
                            cudaStream_t s) {
   const int blocks = 1024, threads = 256;
@@ -165,6 +212,17 @@ cudaError_t launch_prepack(int fmt, int d, int F, const moe_expert_src& src, uin
     prepack_int4_kernel<<<blocks, threads, 0, s>>>((const uint8_t*)src.w[2], src.scale[2],
                                                    src.zero[2], nullptr, nullptr, nullptr, 1, d, F,
                                                    down_dst);
+  }
+  uint8_t* trailer = dst + slot_payload_bytes(fmt, d, F);
+  cudaError_t e = cudaMemsetAsync(trailer, 0, SLOT_TRAILER_BYTES, s);
+  if (e != cudaSuccess) return e;
+  if (fmt_quantised(fmt)) {
+    const int l1_blocks = (F + 7) / 8 < 1024 ? (F + 7) / 8 : 1024;   // 8 warps (rows) per block
+    for (int m = 0; m < 2; ++m)
+      row_l1_max_kernel<<<l1_blocks, 256, 0, s>>>(fmt, (const uint8_t*)src.w[m], src.scale[m],
+                                                  fmt == MOE_W_INT4_G128 ? src.zero[m] : nullptr, F, d,
+                                                  reinterpret_cast<float*>(trailer) + m);
+    trailer_bounds_kernel<<<1, 32, 0, s>>>(trailer);
   }
   return cudaGetLastError();
 }

@@ -18,7 +18,17 @@ Workload shapes follow the five configurations the layer is measured on:
                   experts (E4M3 codes, one fp16 scale per row and group of 128)
 
 Recipes (the values the layer sees; all seeded):
-  * x ~ N(0,1) drawn in fp32 and rounded to bf16.
+  * x ~ N(0,1) drawn in fp32 and rounded to bf16 ("normal").  Activation
+    stress variants (x_dist) for the precision tests:
+      - "outlier": N(0,1) rows with 4 seeded outlier columns, the same in every
+                   token, multiplied by x_outlier (100, 1000: the few very large
+                   feature channels of real LLM hidden states);
+      - "wide":    magnitudes 2^u, u ~ Uniform(-20, 10), random signs, so each
+                   row spans 2^-20 .. 2^10;
+      - "tiny":    N(0,1) * 1e-6;
+      - "scaled":  N(0,1) * x_outlier (every element large);
+      - "onehot":  one nonzero element per row (a seeded column, N(0,1) value
+                   pushed away from 0 by 1).
   * expert weights ~ N(0, 0.02) drawn in fp32 and rounded to bf16 ("source"),
     one independent torch Generator stream per (expert, matrix) so any single
     expert can be regenerated alone on any device.
@@ -61,6 +71,8 @@ class LayerConfig:
     shared: bool = False      # one always-on shared expert (weight 1.0)
     slot_perm: bool = False   # expert->slot table is a seeded random permutation
     seed: int = 0
+    x_dist: str = "normal"    # "normal" | "outlier" | "wide" | "tiny" | "scaled" | "onehot"
+    x_outlier: float = 1000.0
 
     @property
     def A(self) -> int:
@@ -93,9 +105,27 @@ def _rng(seed: int, *stream: int) -> np.random.Generator:
 
 # ----------------------------------------------------------------------------- activations
 def make_x(cfg: LayerConfig) -> torch.Tensor:
-    """Token activations, bf16 [T, d] on the CPU."""
-    v = _rng(cfg.seed, 1).standard_normal((cfg.T, cfg.d), dtype=np.float32)
-    return torch.from_numpy(v).to(torch.bfloat16)
+    """Token activations, bf16 [T, d] on the CPU (distribution: cfg.x_dist)."""
+    rng = _rng(cfg.seed, 1)
+    v = rng.standard_normal((cfg.T, cfg.d), dtype=np.float32)
+    if cfg.x_dist == "outlier":
+        cols = _rng(cfg.seed, 6).choice(cfg.d, size=min(4, cfg.d), replace=False)
+        v[:, cols] *= np.float32(cfg.x_outlier)
+    elif cfg.x_dist == "wide":
+        u = rng.uniform(-20.0, 10.0, size=(cfg.T, cfg.d))
+        v = (np.sign(v) * np.exp2(u)).astype(np.float32)
+    elif cfg.x_dist == "tiny":
+        v = v * np.float32(1e-6)
+    elif cfg.x_dist == "scaled":
+        v = v * np.float32(cfg.x_outlier)
+    elif cfg.x_dist == "onehot":
+        col = rng.integers(0, cfg.d, size=cfg.T)
+        val = v[np.arange(cfg.T), col]
+        v = np.zeros_like(v)
+        v[np.arange(cfg.T), col] = val + np.sign(val)
+    elif cfg.x_dist != "normal":
+        raise ValueError(f"unknown x_dist {cfg.x_dist!r}")
+    return torch.from_numpy(np.ascontiguousarray(v)).to(torch.bfloat16)
 
 
 # ----------------------------------------------------------------------------- router weight

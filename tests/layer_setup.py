@@ -2,6 +2,9 @@
 matching CPU-oracle description of the same seeded inputs."""
 from __future__ import annotations
 
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import torch
 
@@ -14,6 +17,46 @@ import oracle
 # exact value by at most one ulp: a bf16 output cannot be closer than half an ulp,
 # and the fp32 sum before its rounding may fall on either side of the midpoint.
 TOL = 2e-2
+HOST_THREADS = max(1, os.cpu_count() or 1)
+
+
+def row_chunk_width(cfg: ms.LayerConfig) -> int:
+    """The GEMMs' row-chunk width for a layer (a host-side planning rule of the
+    library, restated here only to choose which token rows to compare): a power
+    of two of at least twice the mean rows per routed expert, 16..256, and 192
+    instead of 256 for quantised weights."""
+    mean = -(-cfg.A // cfg.E)
+    bn = 16
+    while bn < 2 * mean and bn < 256:
+        bn <<= 1
+    if cfg.fmt != "bf16" and bn > 128:
+        bn = 192
+    return bn
+
+
+def chunk_edge_tokens(cfg: ms.LayerConfig, logits_np: np.ndarray) -> list[int]:
+    """Tokens whose rows are the first and the last row of every row chunk of
+    every expert group (and of the shared expert's group), from the oracle's own
+    routing and permutation: every chunk, the short last one included, is then
+    compared."""
+    idx, _ = oracle.route_topk(logits_np, cfg.k)
+    counts, offsets, _, tor = oracle.permute(idx, cfg.E)
+    bn = row_chunk_width(cfg)
+    groups = [(int(offsets[e]), int(counts[e]), tor) for e in range(cfg.E)]
+    if cfg.shared:
+        groups.append((0, cfg.T, np.arange(cfg.T, dtype=np.int32)))
+    toks = set()
+    for start, cnt, rows_to_tok in groups:
+        if cnt == 0:
+            continue
+        nch = -(-cnt // bn)
+        rpc = (-(-cnt // nch) + 15) // 16 * 16
+        for c in range(nch):
+            lo, hi = c * rpc, min(cnt, (c + 1) * rpc)
+            if lo < hi:
+                toks.add(int(rows_to_tok[start + lo]))
+                toks.add(int(rows_to_tok[start + hi - 1]))
+    return sorted(toks)
 
 
 class GpuLayer:
@@ -51,8 +94,9 @@ class GpuLayer:
         torch.cuda.synchronize()
         return out, ws
 
-    def oracle_forward(self, tokens=None):
-        """Oracle output rows (exact, float64) for the listed tokens (all if None)."""
+    def oracle_forward(self, tokens=None, threads: int = 1):
+        """Oracle output rows (exact, float64) for the listed tokens (all if None),
+        the tokens split over `threads` host threads (the C oracle releases the GIL)."""
         cfg = self.cfg
         toks = list(range(cfg.T)) if tokens is None else list(tokens)
         idx, _ = oracle.route_topk(self.logits_np[toks], cfg.k)
@@ -61,8 +105,21 @@ class GpuLayer:
         for e in used:
             refs[e] = self.ref(e)
         sh = self.ref("shared") if cfg.shared else None
-        out, _, _ = oracle.layer_forward(self.x.cpu(), self.logits_np, cfg.k, refs, sh, cfg.d,
-                                         cfg.F, tokens=toks)
+        x = self.x.cpu()
+        n = max(1, min(threads, len(toks)))
+        parts = [toks[i::n] for i in range(n)]
+
+        def run(part):
+            return oracle.layer_forward(x, self.logits_np, cfg.k, refs, sh, cfg.d, cfg.F,
+                                        tokens=part)[0]
+
+        if n == 1:
+            return run(toks)
+        with cf.ThreadPoolExecutor(max_workers=n) as pool:
+            outs = list(pool.map(run, parts))
+        out = np.zeros((len(toks), cfg.d), np.float64)
+        for i, o in enumerate(outs):
+            out[i::n] = o
         return out
 
 

@@ -36,9 +36,12 @@ def test_every_declared_symbol_is_exported(L):
 def test_status_strings_and_slot_bytes(L):
     assert L.moe_status_str(0) == b"ok"
     assert L.moe_status_str(3) == b"workspace too small"
-    assert L.moe_slot_bytes(moe.W_INT4, 4096, 14336) == 93_585_408
-    assert L.moe_slot_bytes(moe.W_BF16, 4096, 6400) == 6 * 4096 * 6400
-    assert L.moe_slot_bytes(moe.W_INT4, 5120, 1536) == 12_533_760
+    # the prepacked weights (int4: 1.59375 B per weight; bf16: 2) plus a
+    # 256-byte trailer of bound exponents
+    assert L.moe_slot_bytes(moe.W_INT4, 4096, 14336) == 93_585_408 + 256
+    assert L.moe_slot_bytes(moe.W_BF16, 4096, 6400) == 6 * 4096 * 6400 + 256
+    assert L.moe_slot_bytes(moe.W_INT4, 5120, 1536) == 12_533_760 + 256
+    assert L.moe_slot_bytes(moe.W_FP8, 4096, 14336) == 178_913_280 + 256   # 3.046875 B per weight
     assert L.moe_slot_bytes(moe.W_INT4, 4096, 100) == 0          # d_ff not a multiple of 128
     assert L.moe_slot_bytes(7, 4096, 4096) == 0
 

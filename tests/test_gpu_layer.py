@@ -1,8 +1,9 @@
 """GPU parity: the grouped SwiGLU FFN, the combine and the whole layer against the
 oracle, within max|err| <= 2e-2 * RMS(out) (bf16 activations, fp32 accumulation).
 
-Small cases run the oracle on every token; the five workload shapes run at full
-size in the bench's launch configuration and compare a sample of tokens."""
+Small cases run the oracle on every token; the workload shapes run at full size
+in the bench's launch configuration: every token at decode, and at prefill the
+tokens at both ends of every expert's every row chunk."""
 import numpy as np
 import pytest
 import torch
@@ -10,7 +11,7 @@ import torch
 import moe_expert_layer_03_gb300 as moe
 import moe_synth as ms
 import oracle
-from layer_setup import GpuLayer, assert_close_rms
+from layer_setup import HOST_THREADS, GpuLayer, assert_close_rms, chunk_edge_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -75,6 +76,38 @@ def test_layer_small_all_tokens(name):
     assert_close_rms(out.float().cpu().numpy(), L.oracle_forward(), what=name)
 
 
+# Activation stress: each weight format on each GEMM path (decode kernel: row
+# chunks of <= 32; prefill kernel: wider chunks) with token rows far from N(0,1).
+STRESS_PATHS = {
+    "int4_decode": ms.LayerConfig("int4_decode", T=16, d=512, F=768, E=8, k=2, fmt="int4", seed=51),
+    "int4_prefill": ms.LayerConfig("int4_prefill", T=163, d=512, F=768, E=8, k=2, fmt="int4", seed=52),
+    "fp8_decode": ms.LayerConfig("fp8_decode", T=16, d=512, F=768, E=8, k=2, fmt="fp8", seed=53),
+    "fp8_prefill": ms.LayerConfig("fp8_prefill", T=163, d=512, F=768, E=8, k=2, fmt="fp8", seed=54),
+    "bf16": ms.LayerConfig("bf16", T=40, d=512, F=768, E=8, k=2, fmt="bf16", seed=55),
+    "int4_decode_shared": ms.LayerConfig("int4_decode_shared", T=12, d=384, F=512, E=16, k=4, fmt="int4",
+                                         logits="zipf", zipf_s=1.1, shared=True, slot_perm=True, seed=56),
+}
+STRESS_X = {"outlier100": dict(x_dist="outlier", x_outlier=100.0),
+            "outlier1000": dict(x_dist="outlier", x_outlier=1000.0),
+            "wide": dict(x_dist="wide"), "tiny": dict(x_dist="tiny"), "onehot": dict(x_dist="onehot"),
+            # every element about 200: gate and up near 250, |h| above fp16's 65504
+            "scaled200": dict(x_dist="scaled", x_outlier=200.0)}
+
+
+@pytest.mark.parametrize("dist", list(STRESS_X))
+@pytest.mark.parametrize("path", list(STRESS_PATHS))
+def test_activation_stress(path, dist):
+    """Rows with outlier channels (x100, x1000), rows spanning 2^-20 .. 2^10,
+    all-tiny rows (1e-6), rows of large values (200 N(0,1), whose h exceeds
+    fp16's range unless scaled) and rows with one nonzero element: every token
+    against the oracle within the layer's bound, on every GEMM path."""
+    cfg = STRESS_PATHS[path].with_(name=f"{path}_{dist}", **STRESS_X[dist])
+    L = GpuLayer(cfg)
+    out, ws = L.forward()
+    assert moe.last_device_error(ws) == 0
+    assert_close_rms(out.float().cpu().numpy(), L.oracle_forward(), what=cfg.name)
+
+
 @pytest.mark.parametrize("name", ["tiny", "tiny_int4", "int4_ragged", "bf16_multichunk"])
 def test_grouped_ffn_and_combine_entry_points(name):
     """route -> permute -> grouped_ffn -> combine through the separate ABI calls:
@@ -105,6 +138,38 @@ def test_grouped_ffn_and_combine_entry_points(name):
         assert_close_rms(oc[t], want, what=f"{name} combine token {t}")
 
 
+@pytest.mark.parametrize("fmt", ["int4", "fp8", "bf16"])
+def test_slot_trailer_bounds(fmt):
+    """The prepack's slot trailer: the largest row L1 norm of the dequantised
+    gate and up weights (numpy float64 from the canonical weights, to fp32
+    rounding) and its bound exponent ceil(log2(L (1 + 2^-7))); zero for bf16."""
+    cfg = ms.LayerConfig("trailer", T=1, d=384, F=640, E=1, k=1, fmt=fmt, seed=61)
+    w = ms.expert_weights(cfg, 0, "cuda")
+    pool = moe.ExpertPool(1, cfg.d, cfg.F, cfg.fmt)
+    pool.load_expert(0, w)
+    torch.cuda.synchronize()
+    tr = pool.buf[pool.slot_bytes - 256:pool.slot_bytes].cpu().numpy()
+    L = tr[:8].view(np.float32)
+    B = tr[8:16].view(np.int32)
+    if fmt == "bf16":
+        assert not tr.any()
+        return
+    for m, name in enumerate(("gate", "up")):
+        q = w[name]["q"].cpu().numpy()
+        s = np.repeat(w[name]["scale"].cpu().float().numpy().astype(np.float64), 128, axis=1)
+        if fmt == "int4":
+            codes = np.empty((q.shape[0], q.shape[1] * 2), np.float64)
+            codes[:, 0::2] = q & 15
+            codes[:, 1::2] = q >> 4
+            z = np.repeat(w[name]["zero"].cpu().float().numpy().astype(np.float64), 128, axis=1)
+            deq = (codes - z) * s
+        else:
+            deq = torch.from_numpy(q).view(torch.float8_e4m3fn).float().numpy().astype(np.float64) * s
+        want = np.abs(deq).sum(axis=1).max()
+        assert abs(float(L[m]) - want) <= 1e-5 * want
+        assert int(B[m]) == int(np.ceil(np.log2(float(L[m]) * (1 + 2.0 ** -7))))
+
+
 def test_combine_with_shared_rows():
     T, k, d = 5, 3, 256
     y = torch.randn(T * k, d, device="cuda").to(torch.bfloat16)
@@ -119,17 +184,33 @@ def test_combine_with_shared_rows():
         assert_close_rms(out[t], want, what=f"token {t}")
 
 
-@pytest.mark.parametrize("name", ["mixtral_decode", "phi35_prefill", "fg125b_decode",
-                                  "mixtral_prefill", "mixtral_decode_fp8", "mixtral_prefill_fp8"])
-def test_layer_full_size_sampled(name):
+@pytest.mark.parametrize("name", ["mixtral_decode", "fg125b_decode", "mixtral_decode_fp8"])
+def test_layer_full_size_decode_every_token(name):
+    """The decode workloads at full size, in the bench's launch configuration:
+    every token against the oracle (run on all host cores)."""
     cfg = ms.CONFIGS[name]
     L = GpuLayer(cfg)
     out, ws = L.forward()
     assert moe.last_device_error(ws) == 0
     got = out.float().cpu().numpy()
     assert np.all(np.isfinite(got))
-    toks = sorted({0, cfg.T - 1, cfg.T // 2})[: 2 if cfg.d * cfg.F > 30e6 else 3]
-    assert_close_rms(got[toks], L.oracle_forward(toks), what=name)
+    assert_close_rms(got, L.oracle_forward(threads=HOST_THREADS), what=name)
+
+
+@pytest.mark.parametrize("name", ["phi35_prefill", "mixtral_prefill", "mixtral_prefill_fp8"])
+def test_layer_full_size_prefill_every_row_chunk(name):
+    """The prefill workloads at full size: the tokens holding the first and the
+    last row of every row chunk of every expert (so each expert's first, middle
+    and short last chunk is compared), against the oracle."""
+    cfg = ms.CONFIGS[name]
+    L = GpuLayer(cfg)
+    out, ws = L.forward()
+    assert moe.last_device_error(ws) == 0
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    toks = chunk_edge_tokens(cfg, L.logits_np)
+    assert len(toks) >= cfg.E
+    assert_close_rms(got[toks], L.oracle_forward(toks, threads=HOST_THREADS), what=name)
 
 
 @pytest.mark.parametrize("cfg", [
