@@ -47,20 +47,34 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="mixtral_decode", choices=list(ms.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=4)
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time only --config, not the other workloads as well")
     return ap.parse_args()
 
 
-def describe(cfg: ms.LayerConfig) -> dict:
+L2_BYTES = 129 * 2 ** 20   # GB300 L2
+
+
+def describe(cfg: ms.LayerConfig, n_gpus: int = 1) -> dict:
+    """The workload's config dict, identical for both arms."""
     w = {"bf16": "bf16", "int4": "int4 asymmetric group-128 (fp16 scale + zero)",
          "fp8": "fp8 E4M3 group-128 (fp16 scale)"}[cfg.fmt]
     route = {"normal": "i.i.d. N(0,1) logits", "zipf": f"Zipf(s={cfg.zipf_s}) routing",
              "reuse": f"{int(cfg.reuse_p * 100)}% of tokens reuse the previous token's experts"}[cfg.logits]
+    lg = ms.make_logits(cfg)
+    n_active = len(needed_experts(cfg, lg, list(range(cfg.T)))) + (1 if cfg.shared else 0)
+    wbytes = n_active * ms.active_expert_bytes(cfg)
+    l2 = (f"inputs larger than L2: every step streams the {n_active} active experts' weights "
+          f"({wbytes / 1e6:.0f} MB) from HBM, above the 129 MB L2" if wbytes > L2_BYTES else
+          f"weights ({wbytes / 1e6:.1f} MB) fit in L2 and stay resident across steps (no flush): "
+          f"a launch-bound workload")
     return {"workload": f"{cfg.name}: MoE FFN layer forward, T={cfg.T}, d_model={cfg.d}, "
                         f"d_ff={cfg.F}, E={cfg.E}, top-{cfg.k}, SwiGLU, {w} weights, {route}"
                         + (", + 1 shared expert" if cfg.shared else ""),
             "T": cfg.T, "d_model": cfg.d, "d_ff": cfg.F, "experts": cfg.E, "top_k": cfg.k,
-            "weights": cfg.fmt, "shared_expert": cfg.shared}
+            "weights": cfg.fmt, "shared_expert": cfg.shared, "active_experts": n_active,
+            "parallelism": "single GPU" if n_gpus == 1 else f"{n_gpus} independent replicas, one per GPU",
+            "l2": l2}
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -204,7 +218,7 @@ def run_reference(args, cfg):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": describe(cfg),
+        "config": describe(cfg, args.gpus),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(threads, n_tok),
                          "kind": "oracle",
                          "sample": f"{n_tok} of {cfg.T} tokens per step, all their experts, "
@@ -294,68 +308,78 @@ def dominant_roofline(cfg, n_active, rows, gu_bytes, gu_ms, hbm, tflops, peak_ki
     return ent
 
 
-def run_ours(args, cfg):
-    import moe_expert_layer_03_gb300 as moe
-    rank, world, local = dist_init(args.gpus)
-    moe.build()
-    dev = f"cuda:{local}"
-    torch.cuda.set_device(local)
+class Layer:
+    """One workload's layer, resident on the device: seeded inputs, the expert
+    pool (prepacked through the library) and its routed / shared views."""
 
-    # ---- the layer, resident in HBM
-    x = ms.make_x(cfg).to(dev)
-    logits_np = ms.make_logits(cfg)
-    logits = torch.from_numpy(logits_np).to(dev)
-    e2s = ms.make_slot_table(cfg)
-    pool = moe.ExpertPool(cfg.E + (1 if cfg.shared else 0), cfg.d, cfg.F, cfg.fmt, device=dev)
-    toks_cpu = list(range(min(cfg.T, args.cpu_sample_tokens)))
-    need_cpu = set(needed_experts(cfg, logits_np, toks_cpu)) if rank == 0 and world == 1 else set()
-    weights_cpu = {}
-    for e in range(cfg.E):
-        w = ms.expert_weights(cfg, e, dev)
-        pool.load_expert(int(e2s[e]), w)
-        if e in need_cpu:
-            weights_cpu[e] = {m: {k: v.cpu() for k, v in w[m].items()} for m in w}
-        del w
-    routed = pool.view(torch.from_numpy(e2s).to(dev))
-    shared = None
-    if cfg.shared:
-        w = ms.expert_weights(cfg, "shared", dev)
-        pool.load_expert(cfg.E, w)
-        if need_cpu:
-            weights_cpu["shared"] = {m: {k: v.cpu() for k, v in w[m].items()} for m in w}
-        shared = pool.view(torch.tensor([cfg.E], dtype=torch.int32, device=dev))
-        del w
-    torch.cuda.synchronize()
-    n_active = len(set(needed_experts(cfg, logits_np, list(range(cfg.T))))) + (1 if cfg.shared else 0)
+    def __init__(self, moe, cfg, dev, keep_cpu: bool):
+        self.cfg = cfg
+        self.x = ms.make_x(cfg).to(dev)
+        self.logits_np = ms.make_logits(cfg)
+        self.logits = torch.from_numpy(self.logits_np).to(dev)
+        e2s = ms.make_slot_table(cfg)
+        self.e2s = e2s
+        self.pool = moe.ExpertPool(cfg.E + (1 if cfg.shared else 0), cfg.d, cfg.F, cfg.fmt, device=dev)
+        used = set(needed_experts(cfg, self.logits_np, list(range(cfg.T))))
+        self.weights_cpu = {}
+        for e in range(cfg.E):
+            w = ms.expert_weights(cfg, e, dev)
+            self.pool.load_expert(int(e2s[e]), w)
+            if keep_cpu and e in used:
+                self.weights_cpu[e] = {m: {k: v.cpu() for k, v in w[m].items()} for m in w}
+            del w
+        self.routed = self.pool.view(torch.from_numpy(e2s).to(dev))
+        self.shared = None
+        if cfg.shared:
+            w = ms.expert_weights(cfg, "shared", dev)
+            self.pool.load_expert(cfg.E, w)
+            if keep_cpu:
+                self.weights_cpu["shared"] = {m: {k: v.cpu() for k, v in w[m].items()} for m in w}
+            self.shared = self.pool.view(torch.tensor([cfg.E], dtype=torch.int32, device=dev))
+            del w
+        torch.cuda.synchronize()
+        self.n_active = len(used) + (1 if cfg.shared else 0)
+        self.rows = cfg.A + (cfg.T if cfg.shared else 0)
 
-    ws = moe.workspace(moe.layer_workspace_bytes(cfg.T, cfg.k, routed, shared), dev)
-    out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
-    launches = moe.layer_launch_count(cfg.T, cfg.k, routed, shared)
+
+def time_layer(moe, L: Layer, args, world: int, local: int, dev) -> dict:
+    """K graph replays of the layer timed with CUDA events (inputs resident),
+    clocks sampled meanwhile, then the per-stage split of an eager run."""
+    cfg = L.cfg
     stream = torch.cuda.current_stream()
+    ws = moe.workspace(moe.layer_workspace_bytes(cfg.T, cfg.k, L.routed, L.shared), dev)
+    out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
     # the step as a user runs it: the layer captured once as a CUDA graph over
     # fixed input/output buffers, replayed per step
-    lg = moe.LayerGraph(cfg.T, cfg.k, routed, shared, device=dev)
-    lg.x.copy_(x)
-    lg.logits.copy_(logits)
-
-    # ---- warm-up and correctness guard (device error word)
-    for _ in range(max(args.warmup, 3)):
+    lg = moe.LayerGraph(cfg.T, cfg.k, L.routed, L.shared, device=dev)
+    lg.x.copy_(L.x)
+    lg.logits.copy_(L.logits)
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(max(args.warmup, 3)):
+        if i == 1:
+            w0.record(stream)
         lg.replay()
-        moe.layer_forward(x, logits, cfg.k, routed, shared, out=out, ws=ws)
+    w1.record(stream)
+    moe.layer_forward(L.x, L.logits, cfg.k, L.routed, L.shared, out=out, ws=ws)
     torch.cuda.synchronize()
     code = moe.last_device_error(lg.ws) or moe.last_device_error(ws)
     if code:
-        raise SystemExit(f"device error code {code} during warm-up")
+        raise SystemExit(f"{cfg.name}: device error code {code} during warm-up")
+    per_replay_s = max(w0.elapsed_time(w1) / 1e3 / max(max(args.warmup, 3) - 1, 1), 1e-6)
 
-    # ---- timed region: K steps (graph replays), inputs resident in HBM
+    # ---- timed region: K steps (graph replays).  The clock sampler runs from
+    # before an untimed ~0.25 s stretch of replays (the GPU under load when the
+    # samples are taken) until after the timed steps.
     clk = ClockSampler(local)
     clk.start()
-    time.sleep(0.3)
+    time.sleep(0.2)
+    for _ in range(int(min(0.25 / per_replay_s, 20000))):
+        lg.replay()
     barrier(world)
     torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for i in range(args.steps):
+    for _ in range(args.steps):
         lg.replay()
     stop.record(stream)
     torch.cuda.synchronize()
@@ -363,18 +387,70 @@ def run_ours(args, cfg):
     clocks = clk.stop()
     total_ms = max_over_ranks(start.elapsed_time(stop), world)
     if moe.last_device_error(lg.ws):
-        raise SystemExit("device error during the timed region")
+        raise SystemExit(f"{cfg.name}: device error during the timed region")
 
     # ---- per-stage breakdown: the same step run eagerly with CUDA events
-    # between the kernels (the events themselves add gaps, so this run only
-    # apportions time; it is not the headline)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
-          for _ in range(args.steps)]
-    for i in range(args.steps):
-        moe.layer_forward(x, logits, cfg.k, routed, shared, out=out, ws=ws, events=ev[i])
+    # between the kernels (the events add gaps and turn off the dependent
+    # launches, so this run only apportions time; it is not the headline)
+    n_ev = min(args.steps, 50)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(n_ev)]
+    for i in range(n_ev):
+        moe.layer_forward(L.x, L.logits, cfg.k, L.routed, L.shared, out=out, ws=ws, events=ev[i])
     torch.cuda.synchronize()
-    stage_ms = {s: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)]))
-                for j, s in enumerate(STAGES)}
+    stage_ms = {s_: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(n_ev)]))
+                for j, s_ in enumerate(STAGES)}
+    return {"total_ms": total_ms, "stage_ms": stage_ms, "clocks": clocks, "graph": lg,
+            "launches": moe.layer_launch_count(cfg.T, cfg.k, L.routed, L.shared)}
+
+
+def summarize(L: Layer, t: dict, args, world: int, hbm, tflops, peak_kind) -> dict:
+    cfg = L.cfg
+    ms_step = t["total_ms"] / args.steps
+    gu_bytes = gateup_bytes(cfg, L.n_active, L.rows)
+    lb = layer_bytes(cfg, L.n_active)
+    return {
+        "value": world * cfg.T * args.steps / (t["total_ms"] / 1e3), "unit": "tokens/s",
+        "ms_per_step": ms_step, "steps": args.steps, "warmup": args.warmup,
+        "dtype": dtype_of(cfg), "config": describe(cfg, world),
+        "roofline": dominant_roofline(cfg, L.n_active, L.rows, gu_bytes, t["stage_ms"]["gate_up"], hbm,
+                                      tflops, peak_kind),
+        "layer_roofline": layer_roofline(cfg, L.rows, lb, ms_step, hbm, tflops),
+        "stage_ms": t["stage_ms"], "gpu_launches": t["launches"] * args.steps, "clocks": t["clocks"],
+    }
+
+
+def dtype_of(cfg) -> str:
+    """The arithmetic the layer's GEMMs run in for this workload."""
+    bn = 16
+    mean = -(-cfg.A // cfg.E)
+    while bn < 2 * mean and bn < 256:
+        bn <<= 1
+    if cfg.fmt == "bf16":
+        return "bf16 (tensor cores bf16 x bf16 -> fp32)"
+    w = "int4 codes" if cfg.fmt == "int4" else "fp8 E4M3 codes"
+    if bn <= 32:   # the decode kernel
+        return (f"{w} x bf16 activations carried as two e4m3 terms (hi + lo, per-row power-of-two "
+                f"scale), tensor cores e4m3 x e4m3 -> fp32, scales applied in fp32")
+    return (f"{w} dequantised to fp16 x fp16 activations (per-row power-of-two scale), tensor cores "
+            f"fp16 x fp16 -> fp32")
+
+
+def run_ours(args, cfg):
+    import moe_expert_layer_03_gb300 as moe
+    rank, world, local = dist_init(args.gpus)
+    moe.build()
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    hbm, tflops, peak_kind = load_peaks()
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+
+    # ---- the headline workload
+    L = Layer(moe, cfg, dev, keep_cpu=want_cpu)
+    t = time_layer(moe, L, args, world, local, dev)
+    head = summarize(L, t, args, world, hbm, tflops, peak_kind)
+    lgraph = t["graph"]
+    stream = torch.cuda.current_stream()
+    x, logits, routed, shared = L.x, L.logits, L.routed, L.shared
 
     # ---- the optional router GEMM (logits = x . w_router) that can stand in front
     # of the gating; not part of the step (the step takes logits as input).
@@ -397,17 +473,19 @@ def run_ours(args, cfg):
         rgraph.replay()
     r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     r0.record(stream)
-    for _ in range(max(args.steps // 10, 3)):
+    n_rg = max(args.steps // 10, 3)
+    for _ in range(n_rg):
         rgraph.replay()
     r1.record(stream)
     torch.cuda.synchronize()
-    router_us = r0.elapsed_time(r1) / (max(args.steps // 10, 3) * RG) * 1e3
+    router_us = r0.elapsed_time(r1) / (n_rg * RG) * 1e3
     router_bytes = x.numel() * 2 + wr.numel() * 2 + rl.numel() * 4
 
     # ---- expert streaming (pools larger than HBM): expert images in pinned host
     # memory copied on demand into 2 HBM slots by the LRU cache; timed as
     # alternating pairs of cold experts, 2 copies per ensure(), once with the
     # DMA engines and once with the SM copy kernel (when the images are mapped)
+    pool, e2s = L.pool, L.e2s
     sb = pool.slot_bytes
     streaming = {}
     for mode_name, mode in (("dma", moe.ExpertCache.COPY_ENGINE), ("sm", moe.ExpertCache.COPY_SM)):
@@ -459,53 +537,64 @@ def run_ours(args, cfg):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    if not torch.equal(eg.out_host[(args.steps - 1) % 2].view(torch.int16), lg.out.cpu().view(torch.int16)):
+    if not torch.equal(eg.out_host[(args.steps - 1) % 2].view(torch.int16), lgraph.out.cpu().view(torch.int16)):
         raise SystemExit("end-to-end output differs from the device-resident step")
 
-    ms_step = total_ms / args.steps
-    value = world * cfg.T * args.steps / (total_ms / 1e3)
-    hbm, tflops, peak_kind = load_peaks()
-    rows = cfg.A + (cfg.T if cfg.shared else 0)
-    gu_bytes = gateup_bytes(cfg, n_active, rows)
-    lb = layer_bytes(cfg, n_active)
+    ms_step = head["ms_per_step"]
     line = {
-        "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "metric": "moe_layer_tokens_per_s", "value": head["value"], "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
         "data": "synthetic (seeded), random-init weights of the configured shape",
-        "config": dict(describe(cfg), parallelism=f"replicas x{world}" if world > 1 else "single GPU",
-                       l2="inputs larger than L2: the active experts' weights streamed per step "
-                          f"({lb / 1e6:.0f} MB) exceed the 129 MB L2",
-                       active_experts=n_active),
-        "roofline": dominant_roofline(cfg, n_active, rows, gu_bytes, stage_ms["gate_up"], hbm,
-                                      tflops, peak_kind),
-        "layer_roofline": layer_roofline(cfg, rows, lb, ms_step, hbm, tflops),
-        "stage_ms": stage_ms,
+        "config": head["config"],
+        "roofline": head["roofline"], "layer_roofline": head["layer_roofline"],
+        "stage_ms": head["stage_ms"],
         "e2e": {"value": world * cfg.T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
-                "d2h_bytes_per_step": out.numel() * 2},
-        "gpu_launches": launches * args.steps,
+                "d2h_bytes_per_step": cfg.T * cfg.d * 2},
+        "gpu_launches": head["gpu_launches"],
         "router_gemm": {"us_per_launch": router_us, "algorithmic_bytes": router_bytes,
                         "achieved_gbs": router_bytes / (router_us / 1e6) / 1e9,
                         "note": "back-to-back launches in one CUDA graph; x and the router weight stay in L2"},
         "expert_streaming": {"h2d_gbs_dma": streaming["dma"], "h2d_gbs_sm": streaming["sm"],
                              "expert_image_bytes": sb,
-                             "cold_step_ms": n_active * sb / (max(v for v in streaming.values() if v) * 1e9)
+                             "cold_step_ms": L.n_active * sb / (max(v for v in streaming.values() if v) * 1e9)
                                              * 1e3 + ms_step,
                              "note": "LRU expert cache, pinned host images -> 2 HBM slots, 12 images "
                                      "copied per mode; cold_step_ms = every active expert copied in at "
                                      "the faster mode's rate, then the step"},
-        "clocks": clocks,
+        "clocks": head["clocks"],
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if want_cpu:
         import oracle
         oracle.build()
-        refs = oracle_refs(cfg, weights_cpu)
-        n = len(toks_cpu)
-        t = time_oracle(cfg, x.cpu(), logits_np, refs, toks_cpu, n)
-        line["cpu_baseline"] = {"value": n / t, "unit": "tokens/s", "cores": n, "kind": "oracle",
-                                "sample": f"{n} of {cfg.T} tokens (their {cfg.k} experts each, full "
-                                          f"d_model x d_ff), one host thread per token"}
+        refs = oracle_refs(cfg, L.weights_cpu)
+        cores = os.cpu_count() or 1
+        toks = list(range(cfg.T))
+        n_all = min(cfg.T, cores)
+        t_all = time_oracle(cfg, x.cpu(), L.logits_np, refs, toks[:n_all], n_all)
+        t_one = time_oracle(cfg, x.cpu(), L.logits_np, refs, toks[:1], 1)
+        line["cpu_baseline"] = {
+            "value": n_all / t_all, "unit": "tokens/s", "cores": n_all, "nproc": cores, "kind": "oracle",
+            "sample": f"{n_all} of {cfg.T} tokens (their {cfg.k} experts each, full d_model x d_ff), "
+                      f"one host thread per token on {n_all} of {cores} cores",
+            "single_thread": {"value": 1.0 / t_one, "unit": "tokens/s", "cores": 1,
+                              "sample": "token 0 on one host thread"}}
+    del lgraph, eg, t, L
+    torch.cuda.empty_cache()
+
+    # ---- every other workload, same steps and warm-up, each under its own clocks
+    workloads = {}
+    if not args.no_workloads:
+        for name, c in ms.CONFIGS.items():
+            if name == cfg.name:
+                continue
+            Lw = Layer(moe, c, dev, keep_cpu=False)
+            tw = time_layer(moe, Lw, args, world, local, dev)
+            workloads[name] = summarize(Lw, tw, args, world, hbm, tflops, peak_kind)
+            del Lw, tw
+            torch.cuda.empty_cache()
+        line["workloads"] = workloads
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

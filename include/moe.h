@@ -235,9 +235,12 @@ moe_status moe_layer_forward_timed(const uint16_t* x, const float* logits, int T
  * moe_layer_workspace_bytes(T, k, routed, shared) exceeds that size returns
  * MOE_ERR_WORKSPACE and launches nothing (decode-sized batches fit; large
  * prefill chunks do not).  No cudaMalloc, cudaFree or allocating library call
- * is made.  The first call on a device looks up that device's address of the
- * array (cudaGetSymbolAddress, with the device current); make that first call
- * before any stream capture.  All calls share the one array and it keeps the
+ * is made.  The first call in a CUDA context (normally: on a device) looks up
+ * that device's address of the array (cudaGetSymbolAddress, with the device
+ * current); make that first call before any stream capture.  A new context
+ * (after cudaDeviceReset, or another context made current) is detected by its
+ * unique id and gets a fresh lookup on its first call.  Device-side errors of
+ * these calls are read with moe_noalloc_last_device_error.  All calls share the one array and it keeps the
  * last call's contents (its error word is cleared at the start of each call):
  * calls that overlap on the GPU -- on different streams, or from different
  * host threads -- race on it and must be serialised by the caller. */
@@ -245,6 +248,16 @@ moe_status moe_layer_forward_timed(const uint16_t* x, const float* logits, int T
 moe_status moe_layer_forward_noalloc(const uint16_t* x, const float* logits, int T, int k,
                                      const moe_pool* routed, const moe_pool* shared,
                                      uint16_t* out, moe_stream_t stream);
+
+/* Device-side error word of the allocation-free scratch on the current device
+ * (the caller of moe_layer_forward_noalloc has no workspace pointer to pass to
+ * moe_last_device_error).  Synchronises `stream`, then copies the word: *code
+ * = the OR of the MOE_DEVERR_* bits raised by the most recent
+ * moe_layer_forward_noalloc call on this device (each call clears it first);
+ * returns MOE_OK if it is 0, MOE_ERR_DEVICE otherwise, MOE_ERR_CUDA on a
+ * failed synchronisation or copy.  The pages have no counterpart to this entry
+ * point.  Allocates nothing. */
+moe_status moe_noalloc_last_device_error(int* code, moe_stream_t stream);
 
 /* ---------------------------------------------------------------- expert streaming
  * Pools larger than HBM ([Strata] sec. 2.1: a resident hot-expert pool, cold

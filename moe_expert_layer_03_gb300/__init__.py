@@ -36,7 +36,7 @@ EXPORTS = ("moe_status_str", "moe_slot_bytes", "moe_prepack_expert", "moe_route_
            "moe_permute_workspace_bytes", "moe_permute", "moe_grouped_ffn_workspace_bytes",
            "moe_grouped_ffn", "moe_combine", "moe_layer_workspace_bytes", "moe_layer_forward",
            "moe_layer_forward_timed", "moe_layer_launch_count", "moe_last_device_error",
-           "moe_layer_forward_noalloc", "moe_router_logits", "moe_layer_forward_router",
+           "moe_layer_forward_noalloc", "moe_noalloc_last_device_error", "moe_router_logits", "moe_layer_forward_router",
            "moe_cache_create", "moe_cache_ensure", "moe_cache_plan", "moe_cache_stats",
            "moe_cache_destroy")
 

@@ -264,7 +264,9 @@ moe_status run_ffn(const uint16_t* x_rows, const float* x_unscale, const int32_t
     g.b_scale = f8->xe;
     g.q_out = f8->hq;
     g.sum_out = f8->hs;
-    if (grid + 1 <= 256) {   // ready flags after the error word, in the workspace's 1 KB error region
+    // ready flags err[1 .. grid] after the error word, in the workspace's 1 KB
+    // (256-word) error region; a finishing CTA b reads the flag of CTA b + 1
+    if (grid + 2 <= 256) {
       g.sk_part = f8->skp;
       g.sk_flags = err + 1;
     }
@@ -618,27 +620,67 @@ moe_status moe_last_device_error(const void* ws, int* code, moe_stream_t stream)
 // ===================================================================== allocation-free variant
 // Scratch for moe_layer_forward_noalloc: one file-scope device array per GPU
 // that loads the library.  In host code `g_noalloc_scratch` names a host-side
-// stand-in, never a device address: the device address is looked up once per
-// device with cudaGetSymbolAddress and passed to the kernels as their workspace.
+// stand-in, never a device address: the device address is looked up with
+// cudaGetSymbolAddress, with the device current, at the first call in each
+// CUDA context and passed to the kernels as their workspace.  The cache is
+// keyed by the context's unique id (cuCtxGetId, never reused within a process),
+// so a context created anew -- after cudaDeviceReset, or another context made
+// current -- gets its own lookup instead of a stale address.
 namespace {
 __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
-constexpr int NOALLOC_MAX_DEVICES = 64;
+constexpr int NOALLOC_CACHE = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {nullptr};
+struct NoallocEntry {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+NoallocEntry g_noalloc_cache[NOALLOC_CACHE] = {};
+int g_noalloc_next = 0;
 
-moe_status noalloc_scratch_for_current_device(void** ptr) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES)
-    return MOE_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return MOE_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+// Unique id of the calling thread's current CUDA context (the runtime's
+// primary context once the runtime is initialised on the current device).
+bool current_context_id(unsigned long long* id) {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  if (!g_ctx_current || !g_ctx_id) return false;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return false;
+  if (ctx == nullptr) {   // no context bound to this thread yet: the runtime's primary one
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return false;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
   }
-  *ptr = g_noalloc_ptr[dev];
+  return g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
+
+moe_status noalloc_scratch_for_current_context(void** ptr) {
+  unsigned long long id = 0;
+  if (!current_context_id(&id)) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  for (int i = 0; i < NOALLOC_CACHE; ++i)
+    if (g_noalloc_cache[i].ptr != nullptr && g_noalloc_cache[i].ctx_id == id) {
+      *ptr = g_noalloc_cache[i].ptr;
+      return MOE_OK;
+    }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+  g_noalloc_cache[g_noalloc_next] = NoallocEntry{id, p};
+  g_noalloc_next = (g_noalloc_next + 1) % NOALLOC_CACHE;
+  *ptr = p;
   return MOE_OK;
 }
 }  // namespace
@@ -651,8 +693,16 @@ extern "C" moe_status moe_layer_forward_noalloc(const uint16_t* x, const float* 
   if (need == 0) return MOE_ERR_INVALID_ARG;
   if (need > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
   void* ws = nullptr;
-  const moe_status st = noalloc_scratch_for_current_device(&ws);
+  const moe_status st = noalloc_scratch_for_current_context(&ws);
   if (st != MOE_OK) return st;
   return layer_forward_impl(x, logits, T, k, routed, shared, out, ws, MOE_NOALLOC_SCRATCH_BYTES,
                             (cudaStream_t)stream, nullptr);
+}
+
+extern "C" moe_status moe_noalloc_last_device_error(int* code, moe_stream_t stream) {
+  if (!code) return MOE_ERR_INVALID_ARG;
+  void* ws = nullptr;
+  const moe_status st = noalloc_scratch_for_current_context(&ws);
+  if (st != MOE_OK) return st;
+  return moe_last_device_error(ws, code, stream);
 }

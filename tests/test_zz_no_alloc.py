@@ -6,8 +6,9 @@ real-time loops that forbid allocation latency.  For them the library keeps a
 fixed scratch array on every device and needs only the inputs and outputs.
 This file checks, through the C ABI, that the variant gives the same output as
 moe_layer_forward (which takes a caller-provided workspace) on two calls in a
-row, and that a call too large for the fixed scratch is refused before any
-launch.  It is collected last on purpose and also passes alone in a fresh
+row -- bit for bit, since both run the same kernels on the same layout -- that
+its device-side error word can be read back without a workspace pointer, and
+that a call too large for the fixed scratch is refused before any launch.  It is collected last on purpose and also passes alone in a fresh
 process (the per-device set-up happens on the first call).
 """
 import ctypes as C
@@ -46,6 +47,15 @@ CASES = {
 }
 
 
+def _last_error() -> tuple[int, int]:
+    f = moe.lib().moe_noalloc_last_device_error
+    f.argtypes = [C.POINTER(C.c_int), P]
+    f.restype = C.c_int
+    code = C.c_int(-1)
+    st = f(C.byref(code), P(torch.cuda.current_stream().cuda_stream))
+    return st, code.value
+
+
 @pytest.mark.parametrize("name", list(CASES))
 def test_noalloc_matches_layer_forward_on_two_calls(name):
     L = GpuLayer(CASES[name])
@@ -56,7 +66,27 @@ def test_noalloc_matches_layer_forward_on_two_calls(name):
         out = torch.full_like(ref, float("nan"))
         assert _call(L, out) == 0
         torch.cuda.synchronize()
+        assert _last_error() == (0, 0)
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
         assert_close_rms(out.float().cpu().numpy(), want, what=f"{name} noalloc")
+
+
+def test_noalloc_device_error_is_readable():
+    """A token routed to an expert whose slot is out of range raises the
+    slot-range bit (4) in the scratch's error word; the next clean call clears it."""
+    L = GpuLayer(CASES["int4_shared"])
+    cfg = L.cfg
+    table = torch.from_numpy(L.e2s_np.astype(np.int32)).to("cuda")
+    table[int(L.logits_np[0].argmax())] = 999            # token 0's first expert
+    bad = L.pool.view(table)
+    out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device="cuda")
+    st = _noalloc_fn()(P(L.x.data_ptr()), P(L.logits.data_ptr()), cfg.T, cfg.k, bad.ref, L.shared.ref,
+                       P(out.data_ptr()), P(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    st, code = _last_error()
+    assert st == 5 and code & 4                          # MOE_ERR_DEVICE, slot out of range
+    assert _call(L, out) == 0
+    assert _last_error() == (0, 0)
 
 
 def test_noalloc_rejects_a_call_beyond_its_scratch():
