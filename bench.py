@@ -481,6 +481,67 @@ def run_ours(args, cfg):
     router_us = r0.elapsed_time(r1) / (n_rg * RG) * 1e3
     router_bytes = x.numel() * 2 + wr.numel() * 2 + rl.numel() * 4
 
+    # ---- the step from the token rows alone (router GEMM + layer, one call;
+    # for T <= 64 the router runs inside the routing launch): captured and
+    # replayed like the headline step
+    router_step = {}
+    try:
+        rg_graph = moe.LayerGraph(cfg.T, cfg.k, routed, shared, device=dev, router_weight=wr)
+        rg_graph.x.copy_(x)
+        for _ in range(max(args.warmup, 3)):
+            rg_graph.replay()
+        q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        q0.record(stream)
+        for _ in range(args.steps):
+            rg_graph.replay()
+        q1.record(stream)
+        torch.cuda.synchronize()
+        if moe.last_device_error(rg_graph.ws):
+            raise SystemExit("device error in the router step")
+        same = torch.equal(rg_graph.logits, moe.router_logits(x, wr)) and torch.equal(
+            rg_graph.out.view(torch.int16),
+            moe.layer_forward(x, rg_graph.logits, cfg.k, routed, shared)[0].view(torch.int16))
+        # the same work as two calls (router GEMM, then the layer on its logits),
+        # captured and replayed the same way
+        two_lg = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=dev)
+        two_out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
+        two_ws = moe.workspace(moe.layer_workspace_bytes(cfg.T, cfg.k, routed, shared), dev)
+        side2 = torch.cuda.Stream(device=dev)
+        side2.wait_stream(stream)
+        with torch.cuda.stream(side2):
+            moe.router_logits(x, wr, logits=two_lg)
+            moe.layer_forward(x, two_lg, cfg.k, routed, shared, out=two_out, ws=two_ws)
+            side2.synchronize()
+            two_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(two_graph, stream=side2):
+                moe.router_logits(x, wr, logits=two_lg)
+                moe.layer_forward(x, two_lg, cfg.k, routed, shared, out=two_out, ws=two_ws)
+        stream.wait_stream(side2)
+        for _ in range(max(args.warmup, 3)):
+            two_graph.replay()
+        q2, q3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        q2.record(stream)
+        for _ in range(args.steps):
+            two_graph.replay()
+        q3.record(stream)
+        torch.cuda.synchronize()
+        lg_np = rg_graph.logits.cpu().numpy()
+        router_step = {"us_per_step": q0.elapsed_time(q1) / args.steps * 1e3,
+                       "us_per_step_two_calls": q2.elapsed_time(q3) / args.steps * 1e3,
+                       "gpu_launches_per_step": moe.layer_launch_count(cfg.T, cfg.k, routed, shared)
+                                                + (0 if cfg.T <= 64 else 1),
+                       "gpu_launches_per_step_two_calls": moe.layer_launch_count(cfg.T, cfg.k, routed, shared) + 1,
+                       "router_fused_into_routing_launch": cfg.T <= 64,
+                       "active_experts": len(needed_experts(cfg, lg_np, list(range(cfg.T))))
+                                         + (1 if cfg.shared else 0),
+                       "matches_router_then_layer": bool(same),
+                       "note": "graph replays of moe_layer_forward_router against moe_router_logits + "
+                               "moe_layer_forward on the same router logits (random router weight: "
+                               "the routing, and so the active experts, differ from the headline step's)"}
+        del rg_graph, two_graph
+    except (RuntimeError, moe.MoeError) as e:
+        router_step = {"error": str(e)[:200]}
+
     # ---- expert streaming (pools larger than HBM): expert images in pinned host
     # memory copied on demand into 2 HBM slots by the LRU cache; timed as
     # alternating pairs of cold experts, 2 copies per ensure(), once with the
@@ -556,6 +617,7 @@ def run_ours(args, cfg):
         "router_gemm": {"us_per_launch": router_us, "algorithmic_bytes": router_bytes,
                         "achieved_gbs": router_bytes / (router_us / 1e6) / 1e9,
                         "note": "back-to-back launches in one CUDA graph; x and the router weight stay in L2"},
+        "router_step": router_step,
         "expert_streaming": {"h2d_gbs_dma": streaming["dma"], "h2d_gbs_sm": streaming["sm"],
                              "expert_image_bytes": sb,
                              "cold_step_ms": L.n_active * sb / (max(v for v in streaming.values() if v) * 1e9)

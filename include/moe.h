@@ -193,10 +193,16 @@ moe_status moe_layer_forward(const uint16_t* x, const float* logits, int T, int 
                              const moe_pool* routed, const moe_pool* shared, uint16_t* out,
                              void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* The whole layer from the token rows and the router weight: moe_router_logits
- * into `logits` (caller-owned fp32 [T][E], written; E = routed->n_experts),
- * then moe_layer_forward on those logits.  w_router bf16 [E][d_model].  Same
- * workspace, checks and results as moe_layer_forward; one launch more. */
+/* The whole layer from the token rows and the router weight: the logits of
+ * moe_router_logits (the same bits) into `logits` (caller-owned fp32 [T][E],
+ * written; E = routed->n_experts), then moe_layer_forward on those logits.
+ * w_router bf16 [E][d_model].  Same workspace, checks and results as
+ * moe_layer_forward.  For T <= 64 the router GEMM runs inside the routing
+ * launch ("CPU-GPU co-inference for MoE models", sec. 2.1: the router in front
+ * of the gating on the GPU): a cooperative launch of at most one CTA per SM,
+ * so the call launches as many kernels as moe_layer_forward; it fails with
+ * MOE_ERR_CUDA where a cooperative launch is refused (fewer resident CTAs than
+ * its grid).  Larger batches run the router GEMM as its own launch first. */
 moe_status moe_layer_forward_router(const uint16_t* x, const uint16_t* w_router, int T, int k,
                                     const moe_pool* routed, const moe_pool* shared,
                                     float* logits, uint16_t* out, void* ws, size_t ws_bytes,

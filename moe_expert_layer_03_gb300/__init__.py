@@ -395,13 +395,18 @@ class LayerGraph:
     ``self.x_host`` / ``self.logits_host`` into the device inputs and from
     ``self.out`` back to ``self.out_host``: one replay is then a whole step from
     host memory to host memory (read ``out_host`` after synchronising).
+
+    router_weight (bf16 [E, d] on the device): the step starts from the token
+    rows alone (moe_layer_forward_router); ``self.logits`` is then written by
+    each replay instead of read.
     """
 
     def __init__(self, T: int, k: int, routed: PoolView, shared: PoolView | None = None,
-                 device=None, host_io: bool = False):
+                 device=None, host_io: bool = False, router_weight: torch.Tensor | None = None):
         dev = torch.device(device) if device is not None else routed.e2s.device
         E, d = routed.struct.n_experts, routed.struct.d_model
         self.k, self.routed, self.shared = k, routed, shared
+        self.router_weight = router_weight
         self.x = torch.zeros(T, d, dtype=torch.bfloat16, device=dev)
         self.logits = torch.zeros(T, E, dtype=torch.float32, device=dev)
         self.out = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
@@ -425,7 +430,11 @@ class LayerGraph:
         if self.host_io:
             self.x.copy_(self.x_host, non_blocking=True)
             self.logits.copy_(self.logits_host, non_blocking=True)
-        layer_forward(self.x, self.logits, self.k, self.routed, self.shared, out=self.out, ws=self.ws)
+        if self.router_weight is not None:
+            layer_forward_router(self.x, self.router_weight, self.k, self.routed, self.shared,
+                                 logits=self.logits, out=self.out, ws=self.ws)
+        else:
+            layer_forward(self.x, self.logits, self.k, self.routed, self.shared, out=self.out, ws=self.ws)
         if self.host_io:
             self.out_host.copy_(self.out, non_blocking=True)
 

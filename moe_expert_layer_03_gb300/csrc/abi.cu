@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "kernels.cuh"
+#include "router_dev.cuh"
 
 using namespace moe;
 
@@ -166,6 +167,7 @@ Fp8Rows fp8_rows(uint8_t* W, const Fp8Offsets& f) {
 
 struct LayerLayout {
   int A, Tsh, rows, E, d, F, bn, ksplit;
+  size_t sync;   // the fused router's grid-barrier counter
   bool fp8;   // quantised decode path: e4m3 operands instead of x_perm / h
   bool f16;   // quantised prefill path: fp16 x_perm and h, scaled per row (xe: 2^-ex per row)
   size_t err, idx, w, counts, offsets, roa, tor, xperm, xe, h, part, total;
@@ -184,6 +186,7 @@ LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* s
   L.ksplit = choose_ksplit(L.A, L.E, shared != nullptr, L.bn, routed->fmt, L.d, L.F, L.rows);
   size_t o = 0;
   L.err = o;      o += 1024;
+  L.sync = o;     o += 1024;
   L.idx = o;      o = up1k(o + (size_t)L.A * 4);
   L.w = o;        o = up1k(o + (size_t)L.A * 4);
   L.counts = o;   o = up1k(o + (size_t)(L.E + 1) * 4);
@@ -303,12 +306,14 @@ moe_status check_route_args(const float* logits, int T, int E, int k, const void
   return MOE_OK;
 }
 
-// route_pdl: the routing kernel follows a kernel of the same call (the router
-// GEMM) and may start early.
+// w_router (nullable): the router GEMM comes first and writes `logits` (then
+// an output of the call): fused into the routing launch for batches of up to
+// FUSED_ROUTE_MAX_T tokens, its own launch before the routing kernel (which may
+// then start early) otherwise.
 moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int k,
                               const moe_pool* routed, const moe_pool* shared, uint16_t* out,
                               void* ws, size_t ws_bytes, cudaStream_t s, void* const* ev,
-                              bool route_pdl = false) {
+                              const uint16_t* w_router = nullptr) {
   moe_status st = check_pool(routed, false);
   if (st != MOE_OK) return st;
   if (shared) {
@@ -348,12 +353,20 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
   if (T <= FUSED_ROUTE_MAX_T) {   // one launch; its time is reported as the routing stage
     const GatherDst dst{xperm, f8.xq, f8.xs, L.fp8 ? f8.xe : xe};
     const int out_kind = L.fp8 ? GATHER_FP8 : L.f16 ? GATHER_F16 : GATHER_BF16;
+    const RouterSrc rs{w_router, router_token_tile(T, E, sm_count()), (int*)(W + L.sync)};
+    // the router's barrier counter and the error region (which the routing
+    // kernel then leaves as it is), zero before the cooperative launch
+    if (w_router && cudaMemsetAsync(W + L.err, 0, L.sync + sizeof(int) - L.err, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
     if (launch_route_gather(logits, T, k, E, L.Tsh, x, L.d, idx, w, counts, offsets, roa, tor, err,
-                            out_kind, dst, sm_count(), s, route_pdl && pdl) != cudaSuccess)
+                            out_kind, dst, sm_count(), s, false, w_router ? &rs : nullptr) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (!rec(MOE_STAGE_PERMUTE) || !rec(MOE_STAGE_GATHER)) return MOE_ERR_CUDA;
   } else {
-    if (launch_route_topk(logits, T, E, k, idx, w, nullptr, s, route_pdl && pdl) != cudaSuccess)
+    if (w_router && launch_router_logits(x, w_router, T, L.d, E, const_cast<float*>(logits), sm_count(), s) !=
+                        cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (launch_route_topk(logits, T, E, k, idx, w, nullptr, s, w_router != nullptr && pdl) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (!rec(MOE_STAGE_PERMUTE)) return MOE_ERR_CUDA;
     if (launch_permute_index(idx, T, k, E, L.Tsh, counts, offsets, roa, tor, err, s, pdl) != cudaSuccess)
@@ -585,11 +598,8 @@ moe_status moe_layer_forward_router(const uint16_t* x, const uint16_t* w_router,
   if (!out || !ws || k < 1 || k > routed->n_experts) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < moe_layer_workspace_bytes(T, k, routed, shared)) return MOE_ERR_WORKSPACE;
   if (moe_layer_workspace_bytes(T, k, routed, shared) == 0) return MOE_ERR_INVALID_ARG;
-  cudaStream_t s = (cudaStream_t)stream;
-  if (launch_router_logits(x, w_router, T, routed->d_model, routed->n_experts, logits, sm_count(), s) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
-  return layer_forward_impl(x, logits, T, k, routed, shared, out, ws, ws_bytes, s, nullptr, true);
+  return layer_forward_impl(x, logits, T, k, routed, shared, out, ws, ws_bytes, (cudaStream_t)stream, nullptr,
+                            w_router);
 }
 
 moe_status moe_layer_forward_timed(const uint16_t* x, const float* logits, int T, int k,

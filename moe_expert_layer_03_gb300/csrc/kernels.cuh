@@ -225,10 +225,18 @@ struct GatherDst {
   uint8_t* xq;
   float *xs, *xe;
 };
+// router (nullable): compute the logits first, in the same launch, from x and
+// the router weight (written to `logits`, then routed; see permute.cu).
+struct RouterSrc {
+  const uint16_t* w_router;   // bf16 [E][d]
+  int tt;                     // token tile of the router GEMM (router_token_tile)
+  int* sync;                  // grid-barrier counter, zero at launch
+};
 cudaError_t launch_route_gather(const float* logits, int T, int k, int E, int t_shared, const uint16_t* x,
                                 int d, int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
                                 int32_t* row_of_assign, int32_t* token_of_row, int* err, int out,
-                                const GatherDst& dst, int n_sm, cudaStream_t s, bool pdl = false);
+                                const GatherDst& dst, int n_sm, cudaStream_t s, bool pdl = false,
+                                const RouterSrc* router = nullptr);
 // x_perm[r] = x[token_of_row[r]] (bf16).  token_of_row == nullptr: x_perm[r] = x[r].
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,
                                int d, uint16_t* x_perm, int n_sm, cudaStream_t s, bool pdl = false);

@@ -25,6 +25,7 @@
 #include "kernels.cuh"
 #include "ptx.cuh"
 #include "route_dev.cuh"
+#include "router_dev.cuh"
 
 namespace moe {
 
@@ -34,14 +35,14 @@ constexpr int PERM_MAX_E = 256;
 
 // histogram, scan and stable scatter of the A = T*k expert ids, by one CTA of
 // NT threads (which all call it).  The arrays may be global or shared memory.
-// err (nullable): the workspace's 1 KB error region, cleared first (first
-// kernel of the pipeline that reports device errors; the region also holds the
-// decode GEMM's ready flags), then the error word ORed with
+// err (nullable): the workspace's 1 KB error region, cleared first if `clear`
+// (first kernel of the pipeline that reports device errors; the region also
+// holds the decode GEMM's ready flags), then the error word ORed with
 // MOE_DEVERR_EXPERT_RANGE for an id outside [0, E).
 template <int NT>
 __device__ __forceinline__ void permute_cta(const int32_t* idx, int T, int k, int E, int t_shared,
                                             int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
-                                            int32_t* token_of_row, int* err) {
+                                            int32_t* token_of_row, int* err, bool clear = true) {
   constexpr int NW = NT / 32;
   __shared__ int s_cnt[PERM_MAX_E];
   __shared__ int s_base[PERM_MAX_E];
@@ -50,7 +51,7 @@ __device__ __forceinline__ void permute_cta(const int32_t* idx, int T, int k, in
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int A = T * k;
 
-  if (err != nullptr)   // the error word and the rest of its 1 KB region (the GEMMs' ready flags)
+  if (err != nullptr && clear)   // the error word and the rest of its 1 KB region (the GEMMs' ready flags)
     for (int i = tid; i < 256; i += NT) err[i] = 0;
   for (int e = tid; e < E; e += NT) s_cnt[e] = 0;
   __syncthreads();
@@ -389,14 +390,49 @@ constexpr int RG_THREADS = 512;
 constexpr int RG_MAX_A = FUSED_ROUTE_MAX_T * 16;            // T * k, k <= 16
 constexpr int RG_MAX_ROWS = RG_MAX_A + FUSED_ROUTE_MAX_T;   // + the shared expert's rows
 
-template <int VPL, int OUT>
+// Grid-wide barrier of a cooperative launch (every CTA resident): thread 0 of
+// each CTA adds one to *ctr (zeroed before the launch, with the error word)
+// and waits until all gridDim.x have arrived.  The wait is bounded: past MOE_WAIT_LIMIT_NS it sets
+// MOE_DEVERR_TIMEOUT and lets the CTA go on (its results are then invalid, and
+// the error word says so).
+__device__ __forceinline__ void grid_barrier(int* ctr, int* err) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();   // this CTA's writes before its arrival
+    atomicAdd(ctr, 1);
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire_gpu(ctr) < (int)gridDim.x) {
+      if (global_timer_ns() - t0 > MOE_WAIT_LIMIT_NS) {
+        atomicOr(err, MOE_DEVERR_TIMEOUT);
+        break;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// ROUTER: the router GEMM runs first, in the same launch (a cooperative
+// launch: every CTA is resident).  The CTAs' two 256-thread teams compute the
+// logit tiles (router_tile, the tiling of the standalone router kernel, so
+// the logits are the same bits), write them to `logits`, and after a grid-wide
+// barrier every CTA routes from them with L2-coherent loads.
+template <int VPL, int OUT, bool ROUTER>
 __global__ void __launch_bounds__(RG_THREADS, 1)
-    route_gather_kernel(const float* __restrict__ logits, int T, int k, int E, int t_shared,
+    route_gather_kernel(const float* logits, int T, int k, int E, int t_shared,
                         const uint16_t* __restrict__ x, int d, int32_t* __restrict__ idx,
                         float* __restrict__ w, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                         int32_t* __restrict__ row_of_assign, int32_t* __restrict__ token_of_row,
-                        int* __restrict__ err, GatherDst dst) {
+                        int* __restrict__ err, GatherDst dst, RouterSrc rsrc) {
   griddep_wait();
+  if constexpr (ROUTER) {
+    __shared__ float s_rred[2][RT_WARPS][32];
+    const int team = threadIdx.x / RT_THREADS, tid = threadIdx.x % RT_THREADS;
+    const int ntt = (T + rsrc.tt - 1) / rsrc.tt, eb = (E + RT_EB - 1) / RT_EB;
+    for (int gt = (int)blockIdx.x * 2 + team; gt < ntt * eb; gt += (int)gridDim.x * 2)
+      router_tile(x, rsrc.w_router, T, d, E, (gt % ntt) * rsrc.tt, rsrc.tt, (gt / ntt) * RT_EB,
+                  const_cast<float*>(logits), tid, s_rred[team], 1 + team);
+    grid_barrier(rsrc.sync, err);   // every logit written and visible
+  }
   griddep_launch_dependents();
   __shared__ int32_t s_idx[RG_MAX_A];
   __shared__ float s_w[RG_MAX_A];
@@ -409,10 +445,12 @@ __global__ void __launch_bounds__(RG_THREADS, 1)
   const bool lead = blockIdx.x == 0;
   for (int i = threadIdx.x; i < rows; i += RG_THREADS) s_tor[i] = -1;   // rows of bad ids stay -1
   for (int tok = threadIdx.x >> 5; tok < T; tok += RG_THREADS / 32)
-    route_one_token<VPL>(logits, tok, E, k, s_idx, s_w, threadIdx.x & 31);
+    route_one_token<VPL, ROUTER>(logits, tok, E, k, s_idx, s_w, threadIdx.x & 31);
   __syncthreads();
+  // with the router, the error region was zeroed before the launch (the barrier
+  // may already have reported into it)
   permute_cta<RG_THREADS>(s_idx, T, k, E, t_shared, s_counts, s_offsets, s_roa, s_tor,
-                          lead ? err : nullptr);
+                          lead ? err : nullptr, !ROUTER);
   __syncthreads();
   if (lead) {
     for (int i = threadIdx.x; i < A; i += RG_THREADS) {
@@ -443,40 +481,66 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int k, int E, int t_
                        t_shared, counts, offsets, row_of_assign, token_of_row, err);
 }
 
+template <int VPL, int OUT>
+static cudaError_t launch_route_gather_out(dim3 g, cudaStream_t s, bool pdl, const float* logits, int T, int k,
+                                           int E, int t_shared, const uint16_t* x, int d, int32_t* idx, float* w,
+                                           int32_t* counts, int32_t* offsets, int32_t* roa, int32_t* tor, int* err,
+                                           const GatherDst& dst, const RouterSrc* router) {
+  const dim3 b(RG_THREADS);
+  if (router == nullptr)
+    return launch_kernel(route_gather_kernel<VPL, OUT, false>, g, b, 0, s, pdl, logits, T, k, E, t_shared, x, d,
+                         idx, w, counts, offsets, roa, tor, err, dst, RouterSrc{});
+  // cooperative: the grid-wide barrier needs every CTA resident (grid <= SMs,
+  // one 512-thread CTA per SM); the first kernel of its call, so no dependent
+  // launch attribute
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = g;
+  cfg.blockDim = b;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_gather_kernel<VPL, OUT, true>, logits, T, k, E, t_shared, x, d, idx, w,
+                            counts, offsets, roa, tor, err, dst, *router);
+}
+
 template <int VPL>
 static cudaError_t launch_route_gather_vpl(int out, dim3 g, cudaStream_t s, bool pdl, const float* logits,
                                            int T, int k, int E, int t_shared, const uint16_t* x, int d,
                                            int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
-                                           int32_t* roa, int32_t* tor, int* err, const GatherDst& dst) {
-  const dim3 b(RG_THREADS);
+                                           int32_t* roa, int32_t* tor, int* err, const GatherDst& dst,
+                                           const RouterSrc* router) {
   if (out == GATHER_FP8)
-    return launch_kernel(route_gather_kernel<VPL, GATHER_FP8>, g, b, 0, s, pdl, logits, T, k, E, t_shared,
-                         x, d, idx, w, counts, offsets, roa, tor, err, dst);
+    return launch_route_gather_out<VPL, GATHER_FP8>(g, s, pdl, logits, T, k, E, t_shared, x, d, idx, w, counts,
+                                                    offsets, roa, tor, err, dst, router);
   if (out == GATHER_F16)
-    return launch_kernel(route_gather_kernel<VPL, GATHER_F16>, g, b, 0, s, pdl, logits, T, k, E, t_shared,
-                         x, d, idx, w, counts, offsets, roa, tor, err, dst);
-  return launch_kernel(route_gather_kernel<VPL, GATHER_BF16>, g, b, 0, s, pdl, logits, T, k, E, t_shared,
-                       x, d, idx, w, counts, offsets, roa, tor, err, dst);
+    return launch_route_gather_out<VPL, GATHER_F16>(g, s, pdl, logits, T, k, E, t_shared, x, d, idx, w, counts,
+                                                    offsets, roa, tor, err, dst, router);
+  return launch_route_gather_out<VPL, GATHER_BF16>(g, s, pdl, logits, T, k, E, t_shared, x, d, idx, w, counts,
+                                                   offsets, roa, tor, err, dst, router);
 }
 
 cudaError_t launch_route_gather(const float* logits, int T, int k, int E, int t_shared, const uint16_t* x,
                                 int d, int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
                                 int32_t* row_of_assign, int32_t* token_of_row, int* err, int out,
-                                const GatherDst& dst, int n_sm, cudaStream_t s, bool pdl) {
+                                const GatherDst& dst, int n_sm, cudaStream_t s, bool pdl, const RouterSrc* router) {
   if (T < 1 || T > FUSED_ROUTE_MAX_T || k < 1 || k > 16 || E < 1 || E > PERM_MAX_E) return cudaErrorInvalidValue;
   const int rows = T * k + t_shared;
   const dim3 g((unsigned)(rows < n_sm ? rows : n_sm));
   if (E <= 32)
     return launch_route_gather_vpl<1>(out, g, s, pdl, logits, T, k, E, t_shared, x, d, idx, w, counts,
-                                      offsets, row_of_assign, token_of_row, err, dst);
+                                      offsets, row_of_assign, token_of_row, err, dst, router);
   if (E <= 64)
     return launch_route_gather_vpl<2>(out, g, s, pdl, logits, T, k, E, t_shared, x, d, idx, w, counts,
-                                      offsets, row_of_assign, token_of_row, err, dst);
+                                      offsets, row_of_assign, token_of_row, err, dst, router);
   if (E <= 128)
     return launch_route_gather_vpl<4>(out, g, s, pdl, logits, T, k, E, t_shared, x, d, idx, w, counts,
-                                      offsets, row_of_assign, token_of_row, err, dst);
+                                      offsets, row_of_assign, token_of_row, err, dst, router);
   return launch_route_gather_vpl<8>(out, g, s, pdl, logits, T, k, E, t_shared, x, d, idx, w, counts,
-                                    offsets, row_of_assign, token_of_row, err, dst);
+                                    offsets, row_of_assign, token_of_row, err, dst, router);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* token_of_row, int rows, int T,

@@ -27,8 +27,18 @@ __device__ __forceinline__ float route_key_value(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
+// Logit loads: through the read-only cache, or (COHERENT) from L2, for logits
+// written earlier by the same kernel (the fused router, permute.cu).
+template <bool COHERENT>
+__device__ __forceinline__ float load_logit(const float* p) {
+  if constexpr (COHERENT)
+    return __ldcg(p);
+  else
+    return __ldg(p);
+}
+
 // E <= 32 (one logit per lane): a shuffle butterfly on (value, index).
-template <int VPL>
+template <int VPL, bool COHERENT>
 __device__ __forceinline__ void route_one_token_small(const float* __restrict__ logits, int tok, int E,
                                                       int k, int32_t* __restrict__ idx, float* __restrict__ w,
                                                       int lane) {
@@ -37,7 +47,7 @@ __device__ __forceinline__ void route_one_token_small(const float* __restrict__ 
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int e = lane + 32 * i;
-    float x = e < E ? __ldg(row + e) : -INFINITY;
+    float x = e < E ? load_logit<COHERENT>(row + e) : -INFINITY;
     v[i] = (x != x) ? -INFINITY : x;   // NaN never outranks a number
   }
   uint32_t taken = 0;
@@ -81,7 +91,7 @@ __device__ __forceinline__ void route_one_token_small(const float* __restrict__ 
 }
 
 // E > 32: per round two warp reductions on an order-preserving integer key.
-template <int VPL>
+template <int VPL, bool COHERENT>
 __device__ __forceinline__ void route_one_token_large(const float* __restrict__ logits, int tok, int E,
                                                       int k, int32_t* __restrict__ idx, float* __restrict__ w,
                                                       int lane) {
@@ -90,7 +100,7 @@ __device__ __forceinline__ void route_one_token_large(const float* __restrict__ 
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int e = lane + 32 * i;
-    float x = e < E ? __ldg(row + e) : -INFINITY;
+    float x = e < E ? load_logit<COHERENT>(row + e) : -INFINITY;
     key[i] = route_key((x != x) ? -INFINITY : x);   // NaN never outranks a number
   }
   uint32_t taken = 0;
@@ -129,13 +139,13 @@ __device__ __forceinline__ void route_one_token_large(const float* __restrict__ 
     if (j < k && lane == j) w[(size_t)tok * k + j] = expf(sel[j] - m) / den;
 }
 
-template <int VPL>   // logits per lane = ceil(E / 32)
+template <int VPL, bool COHERENT = false>   // logits per lane = ceil(E / 32)
 __device__ __forceinline__ void route_one_token(const float* __restrict__ logits, int tok, int E, int k,
                                                 int32_t* __restrict__ idx, float* __restrict__ w, int lane) {
   if constexpr (VPL == 1)
-    route_one_token_small<VPL>(logits, tok, E, k, idx, w, lane);
+    route_one_token_small<VPL, COHERENT>(logits, tok, E, k, idx, w, lane);
   else
-    route_one_token_large<VPL>(logits, tok, E, k, idx, w, lane);
+    route_one_token_large<VPL, COHERENT>(logits, tok, E, k, idx, w, lane);
 }
 
 }  // namespace moe

@@ -81,19 +81,33 @@ def test_router_logits_reproducible_and_row_independent():
     assert torch.equal(a[17:18], one)
 
 
-@pytest.mark.parametrize("name", ["tiny_int4", "int4_shared_perm", "int4_ragged"])
+@pytest.mark.parametrize("name", ["tiny_int4", "int4_shared_perm", "int4_ragged", "fused_route_max",
+                                  "fused_route_bf16", "large_E_decode", "prefill_chunk"])
 def test_layer_forward_router(name):
     """The layer from x and the router weight: logits within the bound above,
     then every token whose top-k choice is unambiguous under that bound routed as
     the oracle routes its own logits, and its output within 2e-2 RMS."""
     from test_gpu_layer import SMALL
-    cfg = SMALL[name]
+    extra = {
+        # E > 32 and the shared expert on the fused path
+        "large_E_decode": ms.LayerConfig("large_E_decode", T=16, d=512, F=256, E=128, k=8, fmt="int4",
+                                         logits="zipf", zipf_s=1.1, shared=True, slot_perm=True, seed=71),
+        # more than 64 tokens: the router GEMM as its own launch
+        "prefill_chunk": ms.LayerConfig("prefill_chunk", T=200, d=384, F=256, E=8, k=2, fmt="int4", seed=72),
+    }
+    cfg = SMALL[name] if name in SMALL else extra[name]
     L = GpuLayer(cfg)
     wr = ms.make_router_weight(cfg)
     out, logits, ws = moe.layer_forward_router(L.x, wr.to(L.dev), cfg.k, L.routed, L.shared)
     torch.cuda.synchronize()
     assert moe.last_device_error(ws) == 0
     want_lg, bound = _check_logits(logits, L.x, wr, name)
+    # the same bits as the standalone router GEMM (same tiling, same sum order)
+    assert torch.equal(logits, moe.router_logits(L.x, wr.to(L.dev)))
+    # and the same layer output as moe_layer_forward on those logits
+    out2, _ = moe.layer_forward(L.x, logits, cfg.k, L.routed, L.shared)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
 
     # tokens whose k + 1 largest exact logits are pairwise further apart than two
     # bounds (the chosen set and its order cannot depend on the rounding)
