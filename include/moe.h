@@ -300,6 +300,26 @@ moe_status moe_noalloc_last_device_error(int* code, moe_stream_t stream);
  * without any CUDA call; writes the experts to load and their slots
  * (load_expert / load_slot, n_slots entries each) and *n_loads.
  *
+ * Overlapped streaming ([Strata] sec. 2.2: the next layer's experts are
+ * prefetched into a double buffer while the current one computes; [CoInf]
+ * sec. 3.1: transfers on their own stream, overlapped with compute):
+ * moe_cache_prefetch makes the n listed experts resident on `copy_stream`
+ * without touching the table: each missing one takes an empty slot, else the
+ * least recently used slot that holds neither a listed expert nor one of the
+ * committed set; before overwriting a slot the copy stream waits for that
+ * slot's release event (below).  MOE_ERR_UNSUPPORTED if listed + committed
+ * experts exceed the slots.  moe_cache_commit makes the n listed experts (all
+ * resident, e.g. prefetched) the committed set on `compute_stream`: the stream
+ * waits for their copies, each slot whose expert leaves the committed set gets
+ * a release event recorded on `compute_stream` (complete once the work queued
+ * there before the commit -- the forwards that may read it -- has finished),
+ * and the table is rewritten on `compute_stream`: committed experts -> their
+ * slot, all others -> -1.  Forwards queued after the commit read the new set.
+ * A decode loop per step i: prefetch(A[i+1], copy); forward(i); commit(A[i+1],
+ * compute).  No host synchronisation; use either ensure or prefetch/commit
+ * with one cache.  The events are created by the cache on first use and
+ * destroyed with it.
+ *
  * moe_cache_stats: hits, misses (= expert images copied), bytes copied. */
 typedef struct moe_expert_cache moe_expert_cache;
 enum { MOE_CACHE_COPY_AUTO = 0, MOE_CACHE_COPY_ENGINE = 1, MOE_CACHE_COPY_SM = 2 };
@@ -311,6 +331,8 @@ moe_status moe_cache_create(const moe_pool* routed, const void* host_images, int
 moe_status moe_cache_ensure(moe_expert_cache* cache, const int32_t* experts, int n, moe_stream_t stream);
 moe_status moe_cache_plan(moe_expert_cache* cache, const int32_t* experts, int n, int32_t* load_expert,
                           int32_t* load_slot, int* n_loads);
+moe_status moe_cache_prefetch(moe_expert_cache* cache, const int32_t* experts, int n, moe_stream_t copy_stream);
+moe_status moe_cache_commit(moe_expert_cache* cache, const int32_t* experts, int n, moe_stream_t compute_stream);
 moe_status moe_cache_stats(const moe_expert_cache* cache, moe_cache_counters* out);
 void moe_cache_destroy(moe_expert_cache* cache);
 

@@ -37,8 +37,8 @@ EXPORTS = ("moe_status_str", "moe_slot_bytes", "moe_prepack_expert", "moe_route_
            "moe_grouped_ffn", "moe_combine", "moe_layer_workspace_bytes", "moe_layer_forward",
            "moe_layer_forward_timed", "moe_layer_launch_count", "moe_last_device_error",
            "moe_layer_forward_noalloc", "moe_noalloc_last_device_error", "moe_router_logits", "moe_layer_forward_router",
-           "moe_cache_create", "moe_cache_ensure", "moe_cache_plan", "moe_cache_stats",
-           "moe_cache_destroy")
+           "moe_cache_create", "moe_cache_ensure", "moe_cache_plan", "moe_cache_prefetch",
+           "moe_cache_commit", "moe_cache_stats", "moe_cache_destroy")
 
 
 class MoeError(RuntimeError):
@@ -82,6 +82,8 @@ def lib() -> C.CDLL:
                                                    C.POINTER(MoePool), P, P, P, S, P]
             L.moe_cache_create.argtypes = [C.POINTER(MoePool), P, I, C.POINTER(P)]
             L.moe_cache_ensure.argtypes = [P, P, I, P]
+            L.moe_cache_prefetch.argtypes = [P, P, I, P]
+            L.moe_cache_commit.argtypes = [P, P, I, P]
             L.moe_cache_plan.argtypes = [P, P, I, P, P, C.POINTER(I)]
             L.moe_cache_stats.argtypes = [P, C.POINTER(CacheCounters)]
             L.moe_cache_destroy.argtypes = [P]
@@ -223,6 +225,20 @@ class ExpertCache:
         ex = (C.c_int32 * len(experts))(*[int(e) for e in experts])
         _check(lib().moe_cache_ensure(self._h, C.cast(ex, C.c_void_p), len(experts), _stream(stream)),
                "moe_cache_ensure")
+
+    def prefetch(self, experts, stream):
+        """Copies the listed experts in on `stream` (a copy stream) without touching
+        the table; never evicts a committed expert (moe_cache_prefetch)."""
+        ex = (C.c_int32 * max(1, len(experts)))(*[int(e) for e in experts])
+        _check(lib().moe_cache_prefetch(self._h, C.cast(ex, C.c_void_p), len(experts), _stream(stream)),
+               "moe_cache_prefetch")
+
+    def commit(self, experts, stream=None):
+        """Makes the listed (resident) experts the ones the layer reads, on `stream`
+        (the compute stream), after their copies (moe_cache_commit)."""
+        ex = (C.c_int32 * max(1, len(experts)))(*[int(e) for e in experts])
+        _check(lib().moe_cache_commit(self._h, C.cast(ex, C.c_void_p), len(experts), _stream(stream)),
+               "moe_cache_commit")
 
     def plan(self, experts):
         """The loads ensure() would do (and its bookkeeping), without CUDA work."""

@@ -11,6 +11,19 @@
 // cudaMemcpyAsync (DMA engines) or a kernel whose threads stream the image
 // across the C2C link with 16-byte loads and write it to HBM (all SMs pull at
 // once; the images must be mapped into the device address space).
+//
+// Overlapped streaming ("125B MoE on an RTX 3090", sec. 2.2: the next experts
+// are prefetched into a double buffer while the current layer computes;
+// "CPU-GPU co-inference", sec. 3.1: transfers on their own stream, overlapped
+// with compute): prefetch() copies on a copy stream into slots that hold
+// neither a listed expert nor one of the committed set (the experts the
+// forwards already queued may read); each overwrite first waits on the slot's
+// release event.  commit() makes the listed experts the committed set on the
+// compute stream: the stream waits for their copies, the slots that leave the
+// set get a release event recorded there (complete once every forward queued
+// before the commit has finished), and the table is rewritten on the compute
+// stream (committed experts -> their slot, all others -> -1).  No host
+// synchronisation anywhere.
 #include <algorithm>
 #include <new>
 #include <vector>
@@ -29,6 +42,17 @@ struct moe_expert_cache {
   std::vector<unsigned long long> last_use;   // per slot: tick of the last ensure listing it
   unsigned long long tick = 0;
   moe_cache_counters counters{};
+  // overlapped streaming (prefetch / commit)
+  std::vector<char> committed;        // per expert: in the committed set
+  std::vector<cudaEvent_t> copied;    // per slot: its last prefetch copy has landed
+  std::vector<cudaEvent_t> released;  // per slot: the forwards that may read its previous expert are done
+  std::vector<char> has_copied, has_released;
+  ~moe_expert_cache() {
+    for (cudaEvent_t e : copied)
+      if (e) cudaEventDestroy(e);
+    for (cudaEvent_t e : released)
+      if (e) cudaEventDestroy(e);
+  }
 };
 
 namespace moe {
@@ -59,9 +83,11 @@ __global__ void __launch_bounds__(CP_THREADS)
   for (; i < n16; i += stride) dst[i] = src[i];
 }
 
-// The decisions of one ensure(): updates the bookkeeping and lists the loads.
+// The decisions of one ensure() (or, with keep_committed, one prefetch(),
+// which never evicts a committed expert): updates the bookkeeping and lists the
+// loads.
 moe_status plan_loads(moe_expert_cache* c, const int32_t* experts, int n, int32_t* load_expert,
-                      int32_t* load_slot, int* n_loads) {
+                      int32_t* load_slot, int* n_loads, bool keep_committed = false) {
   if (!c || (!experts && n > 0) || n < 0) return MOE_ERR_INVALID_ARG;
   if (n > c->n_slots) return MOE_ERR_UNSUPPORTED;
   std::vector<char> listed(c->n_experts, 0);
@@ -69,6 +95,15 @@ moe_status plan_loads(moe_expert_cache* c, const int32_t* experts, int n, int32_
     const int e = experts[i];
     if (e < 0 || e >= c->n_experts || listed[e]) return MOE_ERR_INVALID_ARG;
     listed[e] = 1;
+  }
+  {   // enough slots to take every missing listed expert? (checked before any change)
+    int missing = 0, free_slots = 0;
+    for (int i = 0; i < n; ++i) missing += c->expert_slot[experts[i]] < 0;
+    for (int s = 0; s < c->n_slots; ++s) {
+      const int e = c->slot_expert[s];
+      free_slots += e < 0 || (!listed[e] && !(keep_committed && c->committed[e]));
+    }
+    if (missing > free_slots) return MOE_ERR_UNSUPPORTED;
   }
   ++c->tick;
   int nl = 0;
@@ -88,9 +123,10 @@ moe_status plan_loads(moe_expert_cache* c, const int32_t* experts, int n, int32_
     if (victim < 0)
       for (int s = 0; s < c->n_slots; ++s) {   // least recently used, not listed now
         if (listed[c->slot_expert[s]]) continue;
+        if (keep_committed && c->committed[c->slot_expert[s]]) continue;
         if (victim < 0 || c->last_use[s] < c->last_use[victim]) victim = s;
       }
-    if (victim < 0) return MOE_ERR_UNSUPPORTED;   // unreachable: n <= n_slots
+    if (victim < 0) return MOE_ERR_UNSUPPORTED;   // unreachable: checked above
     if (c->slot_expert[victim] >= 0) c->expert_slot[c->slot_expert[victim]] = -1;
     c->slot_expert[victim] = e;
     c->expert_slot[e] = victim;
@@ -144,6 +180,11 @@ moe_status moe_cache_create(const moe_pool* routed, const void* host_images, int
   c->slot_expert.assign(c->n_slots, -1);
   c->expert_slot.assign(c->n_experts, -1);
   c->last_use.assign(c->n_slots, 0);
+  c->committed.assign(c->n_experts, 0);
+  c->copied.assign(c->n_slots, nullptr);
+  c->released.assign(c->n_slots, nullptr);
+  c->has_copied.assign(c->n_slots, 0);
+  c->has_released.assign(c->n_slots, 0);
   *out = c;
   return MOE_OK;
 }
@@ -154,6 +195,25 @@ moe_status moe_cache_plan(moe_expert_cache* c, const int32_t* experts, int n, in
   return plan_loads(c, experts, n, load_expert, load_slot, n_loads);
 }
 
+// One expert image host -> slot on stream s (DMA engines, or the SM copy kernel).
+static moe_status copy_image(moe_expert_cache* c, int e, int slot, cudaStream_t s) {
+  uint8_t* dst = c->dev + (size_t)slot * c->slot_bytes;
+  if (c->host_dev) {
+    int n_sm = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    image_copy_kernel<<<4 * n_sm, CP_THREADS, 0, s>>>(
+        reinterpret_cast<const uint4*>(c->host_dev + (size_t)e * c->slot_bytes), reinterpret_cast<uint4*>(dst),
+        c->slot_bytes / 16);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
+  return cudaMemcpyAsync(dst, c->host + (size_t)e * c->slot_bytes, c->slot_bytes, cudaMemcpyHostToDevice, s) ==
+                 cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
 moe_status moe_cache_ensure(moe_expert_cache* c, const int32_t* experts, int n, moe_stream_t stream) {
   if (!c) return MOE_ERR_INVALID_ARG;
   std::vector<int32_t> le(c->n_slots), ls(c->n_slots);
@@ -161,24 +221,67 @@ moe_status moe_cache_ensure(moe_expert_cache* c, const int32_t* experts, int n, 
   const moe_status st = plan_loads(c, experts, n, le.data(), ls.data(), &nl);
   if (st != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  int n_sm = 0, dev = 0;
-  if (c->host_dev && (cudaGetDevice(&dev) != cudaSuccess ||
-                      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess))
-    return MOE_ERR_CUDA;
   for (int i = 0; i < nl; ++i) {   // one copy per expert image, in stream order
-    uint8_t* dst = c->dev + (size_t)ls[i] * c->slot_bytes;
-    if (c->host_dev) {
-      image_copy_kernel<<<4 * n_sm, CP_THREADS, 0, s>>>(
-          reinterpret_cast<const uint4*>(c->host_dev + (size_t)le[i] * c->slot_bytes),
-          reinterpret_cast<uint4*>(dst), c->slot_bytes / 16);
-      if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-    } else if (cudaMemcpyAsync(dst, c->host + (size_t)le[i] * c->slot_bytes, c->slot_bytes,
-                               cudaMemcpyHostToDevice, s) != cudaSuccess) {
-      return MOE_ERR_CUDA;
-    }
+    const moe_status cs = copy_image(c, le[i], ls[i], s);
+    if (cs != MOE_OK) return cs;
   }
   Table t;
   for (int e = 0; e < c->n_experts; ++e) t.v[e] = c->expert_slot[e];
+  set_table_kernel<<<1, 256, 0, s>>>(t, c->n_experts, c->dev_table);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+static bool make_event(cudaEvent_t* e) {
+  return *e != nullptr || cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+}
+
+moe_status moe_cache_prefetch(moe_expert_cache* c, const int32_t* experts, int n, moe_stream_t copy_stream) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  std::vector<int32_t> le(c->n_slots), ls(c->n_slots);
+  int nl = 0;
+  const moe_status st = plan_loads(c, experts, n, le.data(), ls.data(), &nl, true);
+  if (st != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)copy_stream;
+  for (int i = 0; i < nl; ++i) {
+    const int slot = ls[i];
+    // the forwards that may still read the slot's previous expert come first
+    if (c->has_released[slot] && cudaStreamWaitEvent(s, c->released[slot], 0) != cudaSuccess) return MOE_ERR_CUDA;
+    const moe_status cs = copy_image(c, le[i], slot, s);
+    if (cs != MOE_OK) return cs;
+    if (!make_event(&c->copied[slot]) || cudaEventRecord(c->copied[slot], s) != cudaSuccess) return MOE_ERR_CUDA;
+    c->has_copied[slot] = 1;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_cache_commit(moe_expert_cache* c, const int32_t* experts, int n, moe_stream_t compute_stream) {
+  if (!c || (!experts && n > 0) || n < 0 || n > c->n_slots) return MOE_ERR_INVALID_ARG;
+  std::vector<char> listed(c->n_experts, 0);
+  for (int i = 0; i < n; ++i) {
+    const int e = experts[i];
+    if (e < 0 || e >= c->n_experts || listed[e] || c->expert_slot[e] < 0) return MOE_ERR_INVALID_ARG;
+    listed[e] = 1;
+  }
+  cudaStream_t s = (cudaStream_t)compute_stream;
+  ++c->tick;
+  for (int i = 0; i < n; ++i) {   // the listed experts' copies land before what follows
+    const int slot = c->expert_slot[experts[i]];
+    c->last_use[slot] = c->tick;
+    if (c->has_copied[slot] && cudaStreamWaitEvent(s, c->copied[slot], 0) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  for (int e = 0; e < c->n_experts; ++e) {   // slots leaving the committed set
+    if (!c->committed[e] || listed[e]) continue;
+    const int slot = c->expert_slot[e];
+    if (slot < 0) continue;
+    if (!make_event(&c->released[slot]) || cudaEventRecord(c->released[slot], s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    c->has_released[slot] = 1;
+  }
+  Table t;
+  for (int e = 0; e < c->n_experts; ++e) {
+    c->committed[e] = listed[e];
+    t.v[e] = listed[e] ? c->expert_slot[e] : -1;
+  }
   set_table_kernel<<<1, 256, 0, s>>>(t, c->n_experts, c->dev_table);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
