@@ -339,6 +339,18 @@ void moe_cache_destroy(moe_expert_cache* cache);
 /* Kernel launches one moe_layer_forward enqueues for these arguments (0 on error). */
 int moe_layer_launch_count(int T, int k, const moe_pool* routed, const moe_pool* shared);
 
+/* Test hook for the failure paths (not for production use; the pages have no
+ * counterpart).  Every wait in the grouped-GEMM kernels is bounded: past its
+ * limit the CTA sets MOE_DEVERR_TIMEOUT in the error word, drains the copies
+ * it issued, waits for its MMAs, frees its tensor memory and returns, so the
+ * context stays usable.  This call makes that path run on purpose: forwards
+ * enqueued afterwards have the gate/up GEMM's producer stop after stop_stage
+ * pipeline stages (-1: never), so its consumers' waits run out, and every
+ * GEMM wait give up after wait_ns (0: the default, 2 s).  Host-side setting,
+ * read when a forward is enqueued; not thread-safe.  moe_debug_gemm_fault(-1,
+ * 0) restores the defaults.  MOE_ERR_INVALID_ARG for stop_stage < -1. */
+moe_status moe_debug_gemm_fault(int stop_stage, unsigned long long wait_ns);
+
 /* Synchronously reads the device error word of a workspace written by
  * moe_permute, moe_grouped_ffn or moe_layer_forward (waits for `stream`).
  * *code = the ORed MOE_DEVERR_* bits; returns MOE_ERR_DEVICE if any bit is set. */

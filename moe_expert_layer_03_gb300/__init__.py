@@ -38,7 +38,7 @@ EXPORTS = ("moe_status_str", "moe_slot_bytes", "moe_prepack_expert", "moe_route_
            "moe_layer_forward_timed", "moe_layer_launch_count", "moe_last_device_error",
            "moe_layer_forward_noalloc", "moe_noalloc_last_device_error", "moe_router_logits", "moe_layer_forward_router",
            "moe_cache_create", "moe_cache_ensure", "moe_cache_plan", "moe_cache_prefetch",
-           "moe_cache_commit", "moe_cache_stats", "moe_cache_destroy")
+           "moe_cache_commit", "moe_cache_stats", "moe_cache_destroy", "moe_debug_gemm_fault")
 
 
 class MoeError(RuntimeError):
@@ -104,6 +104,7 @@ def lib() -> C.CDLL:
                                                   C.POINTER(MoePool), P, P, S, P, P]
             L.moe_layer_launch_count.argtypes = [I, I, C.POINTER(MoePool), C.POINTER(MoePool)]
             L.moe_last_device_error.argtypes = [P, C.POINTER(C.c_int), P]
+            L.moe_debug_gemm_fault.argtypes = [I, C.c_ulonglong]
             _lib = L
     return _lib
 
@@ -272,6 +273,13 @@ def grouped_ffn_workspace_bytes(A: int, pool: PoolView) -> int:
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def debug_gemm_fault(stop_stage: int = -1, wait_ns: int = 0):
+    """Failure-path test hook (moe_debug_gemm_fault): the gate/up GEMM's producer
+    stops after `stop_stage` stages and the GEMMs' waits give up after `wait_ns`;
+    debug_gemm_fault() restores the defaults."""
+    _check(lib().moe_debug_gemm_fault(stop_stage, wait_ns), "moe_debug_gemm_fault")
 
 
 def last_device_error(ws: torch.Tensor, stream=None) -> int:

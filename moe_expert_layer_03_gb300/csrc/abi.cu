@@ -204,8 +204,16 @@ LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* s
   return L;
 }
 
+// Failure-path test hook (moe_debug_gemm_fault): the gate/up GEMM's producer
+// stops after this many stages (-1: never) and the GEMMs' waits give up after
+// this long.  Host globals, read when a forward is enqueued.
+int g_fault_stop_stage = -1;
+unsigned long long g_fault_wait_ns = MOE_WAIT_LIMIT_NS;
+
 GemmArgs base_args(const moe_pool* routed, const moe_pool* shared, int* err) {
   GemmArgs a{};
+  a.wait_ns = g_fault_wait_ns;
+  a.stop_stage = -1;
   a.n_routed = routed->n_experts;
   a.pool_r = (const uint8_t*)routed->pool;
   a.slot_bytes_r = routed->slot_bytes;
@@ -274,6 +282,7 @@ moe_status run_ffn(const uint16_t* x_rows, const float* x_unscale, const int32_t
       g.sk_flags = err + 1;
     }
   }
+  g.stop_stage = g_fault_stop_stage;
   if (launch_grouped_gemm(fmt, true, mx, g, plan_gemm(fmt, true, bn, n_groups, F / TILE_M), grid, s,
                           pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -614,6 +623,13 @@ int moe_layer_launch_count(int T, int k, const moe_pool* routed, const moe_pool*
   if (moe_layer_workspace_bytes(T, k, routed, shared) == 0) return 0;
   // route + permute + gather in one launch for small batches; gate/up, down, combine
   return T <= FUSED_ROUTE_MAX_T ? 4 : 6;
+}
+
+moe_status moe_debug_gemm_fault(int stop_stage, unsigned long long wait_ns) {
+  if (stop_stage < -1) return MOE_ERR_INVALID_ARG;
+  g_fault_stop_stage = stop_stage;
+  g_fault_wait_ns = wait_ns > 0 ? wait_ns : MOE_WAIT_LIMIT_NS;
+  return MOE_OK;
 }
 
 moe_status moe_last_device_error(const void* ws, int* code, moe_stream_t stream) {

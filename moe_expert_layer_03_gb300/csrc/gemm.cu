@@ -233,8 +233,12 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
         const uint8_t* sec = it.slot + p.sec_off;
         bool ok = true;
         for (int kg = g0; kg < g1 && ok; ++kg) {
+          if (issued_b == p.stop_stage) {   // test hook: stop feeding the pipeline
+            ok = false;
+            break;
+          }
           if (INT4) {
-            if (!(ok = mbar_wait(smem_u32(&S.raw_empty[rr.i]), rr.ph ^ 1u, abort_flag, p.err))) break;
+            if (!(ok = mbar_wait(smem_u32(&S.raw_empty[rr.i]), rr.ph ^ 1u, abort_flag, p.err, p.wait_ns))) break;
             const uint32_t bar = smem_u32(&S.raw_full[rr.i]);
             mbar_arrive_expect_tx(bar, RAW_STAGE);
             const uint32_t raw = smem_u32(S.raw_ring + (size_t)rr.i * RAW_STAGE);
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
           for (int h = 0; h < 2 && ok; ++h) {
             const int kstep = 2 * kg + h;
             if (!INT4) {
-              if (!(ok = mbar_wait(smem_u32(&S.a_empty[ra.i]), ra.ph ^ 1u, abort_flag, p.err))) break;
+              if (!(ok = mbar_wait(smem_u32(&S.a_empty[ra.i]), ra.ph ^ 1u, abort_flag, p.err, p.wait_ns))) break;
               const uint32_t bar = smem_u32(&S.a_full[ra.i]);
               mbar_arrive_expect_tx(bar, A_STAGE);
               bulk_g2s_hint(smem_u32(S.a_ring + (size_t)ra.i * A_STAGE),
@@ -265,7 +269,7 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
               ra.next();
               ++issued_a;
             }
-            if (!(ok = mbar_wait(smem_u32(&S.b_empty[rb.i]), rb.ph ^ 1u, abort_flag, p.err))) break;
+            if (!(ok = mbar_wait(smem_u32(&S.b_empty[rb.i]), rb.ph ^ 1u, abort_flag, p.err, p.wait_ns))) break;
             const uint32_t bar = smem_u32(&S.b_full[rb.i]);
             mbar_arrive_expect_tx(bar, B_STAGE);
             tma_load_2d(smem_u32(S.b_ring + (size_t)rb.i * B_STAGE), &tmap_b, kstep * KSTEP, it.r0, bar);
@@ -294,15 +298,15 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
       int g0, g1;
       kgroups(p, it.ks, g0, g1);
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tmem_empty), (it_count & 1u) ^ 1u,
-                                                   abort_flag, p.err))))
+                                                   abort_flag, p.err, p.wait_ns))))
         break;
       tc_fence_after();
       const uint32_t idesc = idesc_f16kind_f32(TILE_M, (uint32_t)((it.n_rows + 15) & ~15), AB_BF16);
       for (int kg = g0; kg < g1 && ok; ++kg) {
         for (int h = 0; h < 2; ++h) {
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.a_full[ra.i]), ra.ph, abort_flag, p.err))))
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.a_full[ra.i]), ra.ph, abort_flag, p.err, p.wait_ns))))
             break;
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.b_full[rb.i]), rb.ph, abort_flag, p.err))))
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.b_full[rb.i]), rb.ph, abort_flag, p.err, p.wait_ns))))
             break;
           tc_fence_after();
           const bool fresh = (kg == g0 && h == 0);
@@ -361,7 +365,7 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
       kgroups(p, it.ks, g0, g1);
       if (INT4) {
         for (int kg = g0; kg < g1 && ok; ++kg) {
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.raw_full[rr.i]), rr.ph, abort_flag, p.err));
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&S.raw_full[rr.i]), rr.ph, abort_flag, p.err, p.wait_ns));
           if (!ok) break;
           const uint8_t* raw = S.raw_ring + (size_t)rr.i * RAW_STAGE;
           const uint8_t* mat = raw + m_own * (F8 ? F8_CODE_BYTES : I4_MAT_BYTES);
@@ -377,7 +381,7 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
           const uint32_t nz_b = *reinterpret_cast<const uint32_t*>(&zb);
           for (int h = 0; h < 2; ++h) {   // K slices of the group: 64 codes of my row each
             ok = __all_sync(0xffffffffu,
-                            mbar_wait(smem_u32(&S.a_empty[ra.i]), ra.ph ^ 1u, abort_flag, p.err));
+                            mbar_wait(smem_u32(&S.a_empty[ra.i]), ra.ph ^ 1u, abort_flag, p.err, p.wait_ns));
             if (!ok) break;
             tc_fence_after();
             const uint32_t ta = tl + a_col0 + (uint32_t)ra.i * A_SLOT;
@@ -414,7 +418,7 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
         if (!ok) break;
       }
       // ---- epilogue: one accumulator per item
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tmem_full), it_count & 1u, abort_flag, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tmem_full), it_count & 1u, abort_flag, p.err, p.wait_ns));
       if (!ok) break;
       tc_fence_after();
       const int half = wr >> 2;
@@ -502,12 +506,12 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
       if (rg == 0 && !INT4) continue;
       if (rg == 1 && INT4) continue;
       for (int q = cons[rg]; q < iss[rg]; ++q)
-        mbar_wait(smem_u32(&fulls[rg][q % ns[rg]]), (uint32_t)((q / ns[rg]) & 1), no_abort, p.err);
+        mbar_wait(smem_u32(&fulls[rg][q % ns[rg]]), (uint32_t)((q / ns[rg]) & 1), no_abort, p.err, p.wait_ns);
     }
   }
   if (warp == 1) {   // every MMA this CTA issued has finished
     mma_commit_elect(smem_u32(S.fin));
-    mbar_wait(smem_u32(S.fin), 0, no_abort, p.err);
+    mbar_wait(smem_u32(S.fin), 0, no_abort, p.err, p.wait_ns);
   }
   tc_fence_before();
   __syncthreads();

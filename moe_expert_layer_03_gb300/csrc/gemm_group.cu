@@ -182,8 +182,9 @@ __device__ __forceinline__ ItemDesc get_item(int i, const GemmArgs& p, const GSh
   return make_item_desc(blockIdx.x + i * gridDim.x, p, S.W);
 }
 
-__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err));
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                         uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err, limit_ns));
 }
 
 // The 8 nibbles of a word as two registers of e4m3 codes q * 2^-9 (a nibble
@@ -376,7 +377,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         const int g0 = it.g0, g1 = it.g1;
         const uint8_t* sec = it.slot + p.sec_off;
         for (int kg = g0; kg < g1; ++kg) {
-          if (!(ok = mbar_wait(smem_u32(&S.empty[rs.i]), rs.ph ^ 1u, abort_flag, p.err))) break;
+          if (issued == p.stop_stage) {   // test hook: stop feeding the pipeline
+            ok = false;
+            break;
+          }
+          if (!(ok = mbar_wait(smem_u32(&S.empty[rs.i]), rs.ph ^ 1u, abort_flag, p.err, p.wait_ns))) break;
           const uint32_t bar = smem_u32(&S.full[rs.i]);
           mbar_arrive_expect_tx(bar, LOADED + B_STAGE);
           const uint32_t raw = smem_u32(S.raw_ring + (size_t)rs.i * RAW_STAGE);
@@ -428,9 +433,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         // int4: the unpacked A slot (which implies its stage has landed); fp8:
         // the stage itself, whose code tiles are the A operand
         if (!(ok = wait_all(F8W ? smem_u32(&S.full[rs.i]) : smem_u32(&S.a_full[ra.i]), F8W ? rs.ph : ra.ph,
-                            abort_flag, p.err)))
+                            abort_flag, p.err, p.wait_ns)))
           break;
-        if (!(ok = wait_all(smem_u32(&S.acc_empty[rc.i]), rc.ph ^ 1u, abort_flag, p.err))) break;
+        if (!(ok = wait_all(smem_u32(&S.acc_empty[rc.i]), rc.ph ^ 1u, abort_flag, p.err, p.wait_ns))) break;
         tc_fence_after();
         // the descriptor's start-address field counts 16-byte units
         const uint64_t bd = bdesc0 + (uint64_t)(((uint32_t)rs.i * B_STAGE) >> 4);
@@ -482,8 +487,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       if (!it.slot) continue;
       const int g0 = it.g0, g1 = it.g1;
       for (int kg = g0; kg < g1 && ok; ++kg) {
-        if (!full_ready && !(ok = wait_all(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err))) break;
-        if (!a_ready && !(ok = wait_all(smem_u32(&S.a_empty[ra.i]), ra.ph ^ 1u, abort_flag, p.err))) break;
+        if (!full_ready && !(ok = wait_all(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err, p.wait_ns))) break;
+        if (!a_ready && !(ok = wait_all(smem_u32(&S.a_empty[ra.i]), ra.ph ^ 1u, abort_flag, p.err, p.wait_ns))) break;
         tc_fence_after();
         const uint8_t* mat = S.raw_ring + (size_t)rs.i * RAW_STAGE + m_own * I4_MAT_BYTES;
         const uint32_t ta = lane_base + (uint32_t)ra.i * A_COLS + (uint32_t)(m_own * 32);
@@ -558,7 +563,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < CW; ++i) acc[m][i] = 0.f;
       for (int kg = g0; kg < g1 && ok; ++kg) {
-        if (!(ok = wait_all(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err))) break;
+        if (!(ok = wait_all(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err, p.wait_ns))) break;
         const uint8_t* raw = S.raw_ring + (size_t)rs.i * RAW_STAGE;
         // per matrix: int4: 2^9 s (the codes are q 2^-9) and s z; fp8: s and 0
         float s9[NM], sz[NM];
@@ -579,7 +584,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         sums_src(p.b_sum, ESZ, p.rows_total, kg, it.r0, off);
         // gate/up: sums; down: (sum, unscale) pairs
         const float* bsum = reinterpret_cast<const float*>(raw + SUMS_OFF) + (off + c0) * (ESZ / 4);
-        if (!(ok = wait_all(smem_u32(&S.acc_full[rc.i]), rc.ph, abort_flag, p.err))) break;
+        if (!(ok = wait_all(smem_u32(&S.acc_full[rc.i]), rc.ph, abort_flag, p.err, p.wait_ns))) break;
         tc_fence_after();
         const uint32_t ta = lane_base + acc0 + (uint32_t)rc.i * SLICE;
 #pragma unroll
@@ -637,7 +642,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
               if (i < nc) part[((m0 + m) * TILE_M + r) * GBN + c0 + i] = acc[m][i];
           __threadfence();
           mbar_arrive(smem_u32(S.sk));   // at most one such segment per CTA: phase 0
-          if (warp == G_FOLD0 && lane == 0 && mbar_wait(smem_u32(S.sk), 0, abort_flag, p.err))
+          if (warp == G_FOLD0 && lane == 0 && mbar_wait(smem_u32(S.sk), 0, abort_flag, p.err, p.wait_ns))
             st_release_gpu(p.sk_flags + blockIdx.x, 1);
           continue;
         }
@@ -647,7 +652,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             const uint64_t t0 = global_timer_ns();
             while (ok && ld_acquire_gpu(flag) == 0) {
               if (*abort_flag) ok = false;
-              else if (global_timer_ns() - t0 > MOE_WAIT_LIMIT_NS) {
+              else if (global_timer_ns() - t0 > p.wait_ns) {
                 *abort_flag = 1;
                 atomicOr(p.err, MOE_DEVERR_TIMEOUT);
                 ok = false;
@@ -693,7 +698,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           if (lane == i) S.red[quad * 32 + c0 + i] = m;
         }
         mbar_arrive(smem_u32(&S.epi[0]));
-        if (!(ok = wait_all(smem_u32(&S.epi[0]), par, abort_flag, p.err))) break;
+        if (!(ok = wait_all(smem_u32(&S.epi[0]), par, abort_flag, p.err, p.wait_ns))) break;
         uint8_t* hq = p.q_out;
         const int f = it.mt * TILE_M + (r & ~7) + k_slot(r & 7);   // stored position of my feature
         float ssum[CW];
@@ -725,7 +730,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           if (lane == i) S.red[128 + quad * 32 + c0 + i] = v;
         }
         mbar_arrive(smem_u32(&S.epi[1]));
-        if (!(ok = wait_all(smem_u32(&S.epi[1]), par, abort_flag, p.err))) break;
+        if (!(ok = wait_all(smem_u32(&S.epi[1]), par, abort_flag, p.err, p.wait_ns))) break;
         if (quad == 0 && lane < nc)   // h's (sum, unscale) pair: the sum
           p.sum_out[2 * ((size_t)it.mt * p.rows_total + it.r0 + c0 + lane)] =
               S.red[128 + c0 + lane] + S.red[160 + c0 + lane] + S.red[192 + c0 + lane] + S.red[224 + c0 + lane];
@@ -752,12 +757,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const int iss = S.misc[3];
     for (int sl = 0; sl < n_st && sl < iss; ++sl) {
       const int q = sl + ((iss - 1 - sl) / n_st) * n_st;
-      mbar_wait(smem_u32(&S.full[sl]), (uint32_t)((q / n_st) & 1), no_abort, p.err);
+      mbar_wait(smem_u32(&S.full[sl]), (uint32_t)((q / n_st) & 1), no_abort, p.err, p.wait_ns);
     }
   }
   if (warp >= 1 && warp < G_UP0) {   // every MMA this CTA issued has finished
     mma_commit_elect(smem_u32(S.fin));
-    mbar_wait(smem_u32(S.fin), 0, no_abort, p.err);
+    mbar_wait(smem_u32(S.fin), 0, no_abort, p.err, p.wait_ns);
   }
   tc_fence_before();
   __syncthreads();

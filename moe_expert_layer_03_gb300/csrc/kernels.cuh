@@ -143,6 +143,9 @@ struct GemmArgs {
   unsigned long long trailer_off;
   int n_a, n_b, n_raw;                  // pipeline depths
   uint32_t tmem_cols;                   // TMEM columns (power of two >= 32)
+  unsigned long long wait_ns;           // limit of every wait (MOE_WAIT_LIMIT_NS unless a test sets it)
+  int stop_stage;                       // test hook: the producer issues no stage at or past this
+                                        // index (-1: off), so that a consumer's wait runs out
 };
 
 struct GemmPlan {

@@ -106,15 +106,17 @@ MOE_DEV bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false (and
-// leaves the pipeline) if the CTA is aborting or the wait ran past its limit.
-MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
+// leaves the pipeline) if the CTA is aborting or the wait ran past its limit
+// (limit_ns of wall time).
+MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                       uint64_t limit_ns = MOE_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_sleep(bar, parity)) return true;
     if ((i & 3u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > MOE_WAIT_LIMIT_NS) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(err, MOE_DEVERR_TIMEOUT);
         return false;

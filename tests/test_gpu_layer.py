@@ -11,7 +11,7 @@ import torch
 import moe_expert_layer_03_gb300 as moe
 import moe_synth as ms
 import oracle
-from layer_setup import HOST_THREADS, GpuLayer, assert_close_rms, chunk_edge_tokens
+from layer_setup import HOST_THREADS, GpuLayer, assert_close_rms, bf16_ulp, chunk_edge_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -170,18 +170,29 @@ def test_slot_trailer_bounds(fmt):
         assert int(B[m]) == int(np.ceil(np.log2(float(L[m]) * (1 + 2.0 ** -7))))
 
 
-def test_combine_with_shared_rows():
-    T, k, d = 5, 3, 256
-    y = torch.randn(T * k, d, device="cuda").to(torch.bfloat16)
-    sh = torch.randn(T, d, device="cuda").to(torch.bfloat16)
-    roa = torch.randperm(T * k, device="cuda").to(torch.int32)
-    w = torch.softmax(torch.randn(T, k, device="cuda"), dim=1)
-    out = moe.combine(y, roa, w, sh).float().cpu().numpy()
+@pytest.mark.parametrize("T,k,d", [(5, 3, 256), (16, 8, 5120), (3, 16, 384)])
+def test_combine_with_shared_rows(T, k, d):
+    """The combine against the oracle's exact sum of the same bf16 rows and fp32
+    weights, held to its own error: half a bf16 ulp of the result (the final
+    rounding) plus the fp32 evaluation of k products and k sums,
+    (2k + 1) 2^-24 sum_j |w_j y_j| + |y_shared| (a weight off by 1% fails)."""
+    g = torch.Generator(device="cuda").manual_seed(T * 1000 + k)
+    y = torch.randn(T * k, d, device="cuda", generator=g).to(torch.bfloat16)
+    sh = torch.randn(T, d, device="cuda", generator=g).to(torch.bfloat16)
+    roa = torch.randperm(T * k, device="cuda", generator=g).to(torch.int32)
+    w = torch.softmax(torch.randn(T, k, device="cuda", generator=g), dim=1)
+    out = moe.combine(y, roa, w, sh).float().cpu().numpy().astype(np.float64)
     yc, shc, roac, wc = y.cpu(), sh.cpu(), roa.cpu().numpy(), w.cpu().numpy()
+    u = 2.0 ** -24
     for t in range(T):
         bits = [yc[roac[t * k + j]].view(torch.int16).numpy().view(np.uint16) for j in range(k)]
         want = oracle.combine_row(bits, wc[t], shc[t].view(torch.int16).numpy().view(np.uint16))
-        assert_close_rms(out[t], want, what=f"token {t}")
+        mag = sum(np.abs(wc[t][j] * yc[roac[t * k + j]].float().numpy().astype(np.float64)) for j in range(k))
+        mag = mag + np.abs(shc[t].float().numpy().astype(np.float64))
+        allowed = 0.5 * bf16_ulp(np.maximum(np.abs(want), np.abs(out[t]))) + (2 * k + 1) * u * mag
+        err = np.abs(out[t] - want)
+        i = int(np.argmax(err / allowed))
+        assert np.all(err <= allowed), f"token {t}: |err| {err[i]:.3e} > {allowed[i]:.3e} at {i}"
 
 
 @pytest.mark.parametrize("name", ["mixtral_decode", "fg125b_decode", "mixtral_decode_fp8"])
