@@ -42,9 +42,9 @@
 //
 //   warp 0       producer (bulk copy + TMA)
 //   warps 1-2    MMA issuers (warp 1 owns TMEM)
-//   warps 3-10   unpack, two per TMEM lane quadrant: in the two-matrix modes
-//                each writes one matrix's codes for its quadrant's rows, in
-//                single down each writes one K half
+//   warps 3-10   unpack: two teams of four (one warp per TMEM lane quadrant)
+//                taking alternate groups; a warp writes all codes of its
+//                quadrant's rows (both matrices in the two-matrix modes)
 //   warps 11-18  fold + epilogue, two per quadrant: every matrix and half the
 //                token columns of its 32 rows
 // Modes: gate/up (SwiGLU epilogue, h written in the e4m3 form the down GEMM
@@ -255,10 +255,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < n_st; ++i) {
       mbar_init(smem_u32(&S.full[i]), 1);
-      mbar_init(smem_u32(&S.empty[i]), ((F8W ? 0 : G_NUP) + G_NFOLD) * 32);
+      mbar_init(smem_u32(&S.empty[i]), ((F8W ? 0 : G_NUP / 2) + G_NFOLD) * 32);   // one unpack team per group
     }
     for (int i = 0; i < G_MAX_NA; ++i) {
-      mbar_init(smem_u32(&S.a_full[i]), G_NUP * 32);
+      mbar_init(smem_u32(&S.a_full[i]), G_NUP / 2 * 32);
       mbar_init(smem_u32(&S.a_empty[i]), 1);
     }
     for (int i = 0; i < G_MAX_NBUF; ++i) {
@@ -470,29 +470,34 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     }
   } else if (warp < G_FOLD0) {
     // ================================================================ unpack
-    // Group gc: wait for its stage and for A slot gc % NA to be free (the
-    // MMAs of group gc - NA are done), both tested one group ahead; write
-    // the codes; hand the slot to the MMA warp; release my reads of the stage.
-    const int wr = warp - G_UP0;
+    // Two teams of four warps (one per TMEM lane quadrant) take alternate
+    // groups, so two groups' stores are in flight at once.  Group gc (team
+    // gc % 2): wait for its stage and for A slot gc % NA to be free (the MMAs
+    // of group gc - NA are done); write all codes of my row (both matrices in
+    // the two-matrix modes); release my reads of the stage; hand the slot to
+    // the MMA warp once the stores have landed.  Ring positions advance by one
+    // per group, owned or not.
+    const int team = (warp - G_UP0) >> 2;
     const int quad = warp & 3;               // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;          // weight row of the tile = TMEM lane
-    const int hw = wr >> 2;                  // which of the quadrant's two unpack warps
-    const int m_own = PAIR ? hw : 0;         // matrix (two-matrix modes) ...
-    const int h_own = PAIR ? 0 : hw;         // ... or K half (single down)
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
     Ring rs{0, 0, n_st}, ra{0, 0, NA > 0 ? NA : 1};
-    bool ok = true, full_ready = false, a_ready = false;
+    bool ok = true;
+    uint32_t gc = 0;
     for (int ii = 0; ii < (F8W ? 0 : n_mine) && ok; ++ii) {   // fp8: nothing to unpack
       const ItemDesc it = get_item(ii, p, S);
       if (!it.slot) continue;
       const int g0 = it.g0, g1 = it.g1;
-      for (int kg = g0; kg < g1 && ok; ++kg) {
-        if (!full_ready && !(ok = wait_all(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err, p.wait_ns))) break;
-        if (!a_ready && !(ok = wait_all(smem_u32(&S.a_empty[ra.i]), ra.ph ^ 1u, abort_flag, p.err, p.wait_ns))) break;
+      for (int kg = g0; kg < g1 && ok; ++kg, ++gc, rs.next(), ra.next()) {
+        if ((int)(gc & 1u) != team) continue;
+        if (!(ok = wait_all(smem_u32(&S.full[rs.i]), rs.ph, abort_flag, p.err, p.wait_ns))) break;
+        if (!(ok = wait_all(smem_u32(&S.a_empty[ra.i]), ra.ph ^ 1u, abort_flag, p.err, p.wait_ns))) break;
         tc_fence_after();
-        const uint8_t* mat = S.raw_ring + (size_t)rs.i * RAW_STAGE + m_own * I4_MAT_BYTES;
-        const uint32_t ta = lane_base + (uint32_t)ra.i * A_COLS + (uint32_t)(m_own * 32);
-        if (PAIR) {   // all 128 codes of my row: column h*16 + j*8 + 2w (+1)
+        const uint8_t* stage = S.raw_ring + (size_t)rs.i * RAW_STAGE;
+        const uint32_t ta = lane_base + (uint32_t)ra.i * A_COLS;
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {   // all 128 codes of my row: column h*16 + j*8 + 2w (+1)
+          const uint8_t* mat = stage + m * I4_MAT_BYTES;
           uint32_t v[32];
 #pragma unroll
           for (int hj = 0; hj < 4; ++hj) {   // quad (h, j) = (hj >> 1, hj & 1)
@@ -502,35 +507,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             e4m3_codes(wq.z, v[hj * 8 + 4], v[hj * 8 + 5]);
             e4m3_codes(wq.w, v[hj * 8 + 6], v[hj * 8 + 7]);
           }
-          tmem_st_32(ta, v);
-        } else {      // my K half: 64 codes of my row
-          uint32_t v[16];
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const uint4 wq = *reinterpret_cast<const uint4*>(mat + ((h_own * 2 + j) * TILE_M + r) * 16);
-            e4m3_codes(wq.x, v[j * 8 + 0], v[j * 8 + 1]);
-            e4m3_codes(wq.y, v[j * 8 + 2], v[j * 8 + 3]);
-            e4m3_codes(wq.z, v[j * 8 + 4], v[j * 8 + 5]);
-            e4m3_codes(wq.w, v[j * 8 + 6], v[j * 8 + 7]);
-          }
-          tmem_st_16(ta + (uint32_t)(h_own * 16), v);
+          tmem_st_32(ta + (uint32_t)(m * 32), v);
         }
         mbar_arrive(smem_u32(&S.empty[rs.i]));   // my reads of the stage are done
-        {   // while the stores drain, test what the next group waits for
-          Ring ns = rs, na = ra;
-          ns.next();
-          na.next();
-          const uint32_t t = __reduce_and_sync(
-              0xffffffffu, mbar_test_wait2(smem_u32(&S.full[ns.i]), ns.ph, smem_u32(&S.a_empty[na.i]),
-                                           na.ph ^ 1u));
-          full_ready = (t & 1u) != 0;
-          a_ready = (t & 2u) != 0;
-        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&S.a_full[ra.i]));
-        rs.next();
-        ra.next();
       }
     }
   } else {
@@ -548,7 +530,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const int c0 = ((warp - G_FOLD0) >> 2) * (GBN / 2);   // my token columns [c0, c0 + CW)
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
     constexpr int CW = GBN / 2;                        // token columns per fold thread
-    constexpr int CH = 8;                              // columns per tcgen05.ld (and per chunk)
+    constexpr int CH = 4;                              // columns per tcgen05.ld (and per chunk): an item
+                                                       // of n rows folds ceil(n / 4) chunks
     Ring rs{0, 0, n_st}, rc{0, 0, NBUF};
     uint32_t it_count = 0;
     bool ok = true;
@@ -594,13 +577,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 #pragma unroll
             for (int m = 0; m < NM; ++m) {
               const uint32_t col = ta + (uint32_t)((m0 + m) * 2 * GBN + c0 + ch * CH);
-              if (CH == 16) {
-                tmem_ld_16(col, *reinterpret_cast<uint32_t(*)[16]>(dv[m]));
-                tmem_ld_16(col + GBN, *reinterpret_cast<uint32_t(*)[16]>(dl[m]));
-              } else {
-                tmem_ld_8(col, *reinterpret_cast<uint32_t(*)[8]>(dv[m]));
-                tmem_ld_8(col + GBN, *reinterpret_cast<uint32_t(*)[8]>(dl[m]));
-              }
+              tmem_ld_4(col, *reinterpret_cast<uint32_t(*)[4]>(dv[m]));
+              tmem_ld_4(col + GBN, *reinterpret_cast<uint32_t(*)[4]>(dl[m]));
             }
             // token factors (shared by the matrices) while the loads are in flight
             float bs[CH], bu[CH];
