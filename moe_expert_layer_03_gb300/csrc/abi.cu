@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "kernels.cuh"
+#include "nvtx_range.h"
 #include "router_dev.cuh"
 
 using namespace moe;
@@ -430,6 +431,7 @@ size_t moe_slot_bytes(int fmt, int d_model, int d_ff) {
 
 moe_status moe_prepack_expert(int fmt, int d_model, int d_ff, const moe_expert_src* src,
                               void* slot_dst, moe_stream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_prepack_expert");
   if (!src || !slot_dst || moe_slot_bytes(fmt, d_model, d_ff) == 0) return MOE_ERR_INVALID_ARG;
   if (d_model > MAX_DIM || d_ff > MAX_DIM) return MOE_ERR_UNSUPPORTED;
   if (!al256(slot_dst)) return MOE_ERR_INVALID_ARG;
@@ -455,6 +457,7 @@ moe_status check_router_args(const uint16_t* x, const uint16_t* w_router, int T,
 
 moe_status moe_router_logits(const uint16_t* x, const uint16_t* w_router, int T, int d, int E,
                              float* logits, moe_stream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_router_logits");
   const moe_status st = check_router_args(x, w_router, T, d, E, logits);
   if (st != MOE_OK) return st;
   return launch_router_logits(x, w_router, T, d, E, logits, sm_count(), (cudaStream_t)stream) ==
@@ -465,6 +468,7 @@ moe_status moe_router_logits(const uint16_t* x, const uint16_t* w_router, int T,
 
 moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* topk_idx,
                           float* topk_w, moe_stream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_route_topk");
   const moe_status st = check_route_args(logits, T, E, k, topk_idx, topk_w);
   if (st != MOE_OK) return st;
   return launch_route_topk(logits, T, E, k, topk_idx, topk_w, nullptr, (cudaStream_t)stream) ==
@@ -479,6 +483,7 @@ moe_status moe_permute(const int32_t* topk_idx, const uint16_t* x, int T, int k,
                        int32_t* counts, int32_t* offsets, int32_t* row_of_assign,
                        int32_t* token_of_row, uint16_t* x_perm, void* ws, size_t ws_bytes,
                        moe_stream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_permute");
   if (!topk_idx || !x || !counts || !offsets || !row_of_assign || !token_of_row || !x_perm || !ws)
     return MOE_ERR_INVALID_ARG;
   if (T < 1 || E < 1 || k < 1 || k > E || d < 128 || d % 128) return MOE_ERR_INVALID_ARG;
@@ -531,6 +536,7 @@ size_t moe_grouped_ffn_workspace_bytes(int A, const moe_pool* pool) {
 moe_status moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int A,
                            const moe_pool* pool, uint16_t* y_perm, void* ws, size_t ws_bytes,
                            moe_stream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_grouped_ffn");
   moe_status st = check_pool(pool, false);
   if (st != MOE_OK) return st;
   if (!x_perm || !offsets || !y_perm || !ws || A < 1) return MOE_ERR_INVALID_ARG;
@@ -572,6 +578,7 @@ moe_status moe_grouped_ffn(const uint16_t* x_perm, const int32_t* offsets, int A
 moe_status moe_combine(const uint16_t* y_perm, const int32_t* row_of_assign, const float* topk_w,
                        const uint16_t* shared_y, int T, int k, int d, uint16_t* out,
                        moe_stream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_combine");
   if (!y_perm || !row_of_assign || !topk_w || !out) return MOE_ERR_INVALID_ARG;
   if (T < 1 || k < 1 || d < 128 || d % 128) return MOE_ERR_INVALID_ARG;
   if (k > MAX_K || (long)T * k > MAX_A || d > MAX_DIM) return MOE_ERR_UNSUPPORTED;
@@ -591,6 +598,7 @@ size_t moe_layer_workspace_bytes(int T, int k, const moe_pool* routed, const moe
 moe_status moe_layer_forward(const uint16_t* x, const float* logits, int T, int k,
                              const moe_pool* routed, const moe_pool* shared, uint16_t* out,
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_layer_forward");
   return layer_forward_impl(x, logits, T, k, routed, shared, out, ws, ws_bytes,
                             (cudaStream_t)stream, nullptr);
 }
@@ -599,6 +607,7 @@ moe_status moe_layer_forward_router(const uint16_t* x, const uint16_t* w_router,
                                     const moe_pool* routed, const moe_pool* shared,
                                     float* logits, uint16_t* out, void* ws, size_t ws_bytes,
                                     moe_stream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_layer_forward_router");
   moe_status st = check_pool(routed, false);
   if (st != MOE_OK) return st;
   if ((st = check_router_args(x, w_router, T, routed->d_model, routed->n_experts, logits)) != MOE_OK)
@@ -615,6 +624,7 @@ moe_status moe_layer_forward_timed(const uint16_t* x, const float* logits, int T
                                    const moe_pool* routed, const moe_pool* shared, uint16_t* out,
                                    void* ws, size_t ws_bytes, moe_stream_t stream,
                                    void* const* stage_events) {
+  const moe::NvtxRange nvtx_range("moe_layer_forward_timed");
   return layer_forward_impl(x, logits, T, k, routed, shared, out, ws, ws_bytes,
                             (cudaStream_t)stream, stage_events);
 }
@@ -715,6 +725,7 @@ extern "C" moe_status moe_layer_forward_noalloc(const uint16_t* x, const float* 
                                                 int k, const moe_pool* routed,
                                                 const moe_pool* shared, uint16_t* out,
                                                 moe_stream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_layer_forward_noalloc");
   const size_t need = moe_layer_workspace_bytes(T, k, routed, shared);
   if (need == 0) return MOE_ERR_INVALID_ARG;
   if (need > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;

@@ -29,6 +29,7 @@
 #include <vector>
 
 #include "kernels.cuh"
+#include "nvtx_range.h"
 
 struct moe_expert_cache {
   int n_experts = 0, n_slots = 0;
@@ -215,6 +216,7 @@ static moe_status copy_image(moe_expert_cache* c, int e, int slot, cudaStream_t 
 }
 
 moe_status moe_cache_ensure(moe_expert_cache* c, const int32_t* experts, int n, moe_stream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_cache_ensure");
   if (!c) return MOE_ERR_INVALID_ARG;
   std::vector<int32_t> le(c->n_slots), ls(c->n_slots);
   int nl = 0;
@@ -236,6 +238,7 @@ static bool make_event(cudaEvent_t* e) {
 }
 
 moe_status moe_cache_prefetch(moe_expert_cache* c, const int32_t* experts, int n, moe_stream_t copy_stream) {
+  const moe::NvtxRange nvtx_range("moe_cache_prefetch");
   if (!c) return MOE_ERR_INVALID_ARG;
   std::vector<int32_t> le(c->n_slots), ls(c->n_slots);
   int nl = 0;
@@ -255,6 +258,7 @@ moe_status moe_cache_prefetch(moe_expert_cache* c, const int32_t* experts, int n
 }
 
 moe_status moe_cache_commit(moe_expert_cache* c, const int32_t* experts, int n, moe_stream_t compute_stream) {
+  const moe::NvtxRange nvtx_range("moe_cache_commit");
   if (!c || (!experts && n > 0) || n < 0 || n > c->n_slots) return MOE_ERR_INVALID_ARG;
   std::vector<char> listed(c->n_experts, 0);
   for (int i = 0; i < n; ++i) {
