@@ -435,7 +435,18 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
         uint32_t acc0[16];
         tmem_ld_16(tl + (uint32_t)(c * 16), acc0);
         const int nv = it.n_rows - c * 16;   // valid token columns of the chunk (> 0)
-        const float* ux_c = p.b_scale + it.r0 + c * 16;
+        // quantised: lane i < 16 works out token i's factors once for the warp
+        // (gate/up: x unscale fx = 2^-ex and fu = 2^-ex * 2^eh for up; down:
+        // 2^-eh), handed to every lane by shuffles
+        float fx = 1.f, fu = 1.f;
+        if constexpr (INT4) {
+          if (lane < 16 && lane < nv) {
+            float inv;
+            fx = __ldg(p.b_scale + it.r0 + c * 16 + lane);
+            fu = fx * h_row_scale(fx, bsum, &inv);
+            if (!GATEUP) fx = inv;
+          }
+        }
         if (GATEUP) {
           const int f = it.mt * TILE_M + r;   // output feature of this thread
           uint32_t acc1[16];
@@ -450,12 +461,10 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
             float g0 = __uint_as_float(acc0[i]), u0 = __uint_as_float(acc1[i]);
             float g1 = __uint_as_float(acc0[i + 1]), u1 = __uint_as_float(acc1[i + 1]);
             if constexpr (INT4) {   // undo x's row scale (exact), apply h's (u * 2^-ex * 2^eh)
-              float inv;
-              const float x0 = i < nv ? __ldg(ux_c + i) : 1.f, x1 = i + 1 < nv ? __ldg(ux_c + i + 1) : 1.f;
-              g0 *= x0;
-              u0 *= x0 * h_row_scale(x0, bsum, &inv);
-              g1 *= x1;
-              u1 *= x1 * h_row_scale(x1, bsum, &inv);
+              g0 *= __shfl_sync(0xffffffffu, fx, i);
+              u0 *= __shfl_sync(0xffffffffu, fu, i);
+              g1 *= __shfl_sync(0xffffffffu, fx, i + 1);
+              u1 *= __shfl_sync(0xffffffffu, fu, i + 1);
             }
             const float h0 = silu_f(g0) * u0, h1 = silu_f(g1) * u1;
             const uint32_t pk = INT4 ? half2_bits_sat(h0, h1) : bf162_bits(h0, h1);
@@ -468,12 +477,7 @@ __global__ void __launch_bounds__((2 + NDQ) * 32, 1)
           if (PAIR) tmem_ld_16(tl + (uint32_t)(p.bn + c * 16), acc1);
           float hu[16];   // quantised: 2^-eh of each token row (h's scale undone), else 1
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            hu[i] = 1.f;
-            if constexpr (INT4) {
-              if (i < nv) h_row_scale(__ldg(ux_c + i), bsum, &hu[i]);
-            }
-          }
+          for (int i = 0; i < 16; ++i) hu[i] = INT4 ? __shfl_sync(0xffffffffu, fx, i) : 1.f;
           tmem_ld_wait();
 #pragma unroll
           for (int m = 0; m < NMAT; ++m) {
