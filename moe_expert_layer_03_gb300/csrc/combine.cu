@@ -101,12 +101,7 @@ __global__ void __launch_bounds__(256)
   float4 acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-  auto add_row = [&](int r, float w) {   // acc += w * y[r], this thread's columns
-    if (r < 0) return;                    // r < 0 only after an index error
-    float4 y[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v)
-      if (cv[v] < d) y[v] = y_from_partials<OVERLAP>(part, n_split, split_stride, r, d, cv[v]);
+  auto add = [&](float4 (&y)[V], float w) {   // acc += w * y, this thread's columns
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       if (cv[v] >= d) continue;
@@ -116,19 +111,73 @@ __global__ void __launch_bounds__(256)
       acc[v].w += w * y[v].w;
     }
   };
+  if (OVERLAP && n_split == 1 && k <= PRE) {
+    // one split (decode with many experts per token): every row's load is in
+    // flight before the first add (the rows are independent; the sum keeps its
+    // order, so the result is the same bits as the loop below)
+    float4 y[PRE + 1][V];
 #pragma unroll
-  for (int j = 0; j < PRE; ++j)
-    if (j < k) add_row(rj[j], wj[j]);
-  for (int j = PRE; j < k; ++j) add_row(row_of_assign[t * k + j], topk_w[t * k + j]);
-  if (shared_row0 >= 0) {
+    for (int j = 0; j < PRE; ++j)
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-      if (cv[v] >= d) continue;
-      const float4 y = y_from_partials<OVERLAP>(part, n_split, split_stride, shared_row0 + t, d, cv[v]);
-      acc[v].x += y.x;
-      acc[v].y += y.y;
-      acc[v].z += y.z;
-      acc[v].w += y.w;
+      for (int v = 0; v < V; ++v)
+        if (j < k && rj[j] >= 0 && cv[v] < d)
+          y[j][v] = __ldg(reinterpret_cast<const float4*>(part + (size_t)rj[j] * d + cv[v]));
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+      if (shared_row0 >= 0 && cv[v] < d)
+        y[PRE][v] = __ldg(reinterpret_cast<const float4*>(part + (size_t)(shared_row0 + t) * d + cv[v]));
+#pragma unroll
+    for (int j = 0; j < PRE; ++j)
+      if (j < k && rj[j] >= 0) add(y[j], wj[j]);   // r < 0 only after an index error
+    if (shared_row0 >= 0) add(y[PRE], 1.f);
+  } else if (OVERLAP && V == 1 && k <= 2 && n_split <= 8 && shared_row0 < 0) {
+    // top-2 with K splits (decode of a few wide experts): both rows' split loads
+    // in flight at once; each row's splits summed in split order, then the
+    // weighted adds in j order -- the same bits as the loop below
+    float4 y[2][8];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (j < k && i < n_split && rj[j] >= 0)
+          y[j][i] = __ldg(reinterpret_cast<const float4*>(part + i * split_stride + (size_t)rj[j] * d + cv[0]));
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (j >= k || rj[j] < 0) continue;   // r < 0 only after an index error
+      float4 sj[V] = {make_float4(0.f, 0.f, 0.f, 0.f)};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i < n_split) {
+          sj[0].x += y[j][i].x;
+          sj[0].y += y[j][i].y;
+          sj[0].z += y[j][i].z;
+          sj[0].w += y[j][i].w;
+        }
+      add(sj, wj[j]);
+    }
+  } else {
+    auto add_row = [&](int r, float w) {   // acc += w * y[r], this thread's columns
+      if (r < 0) return;                    // r < 0 only after an index error
+      float4 y[V];
+#pragma unroll
+      for (int v = 0; v < V; ++v)
+        if (cv[v] < d) y[v] = y_from_partials<OVERLAP>(part, n_split, split_stride, r, d, cv[v]);
+      add(y, w);
+    };
+#pragma unroll
+    for (int j = 0; j < PRE; ++j)
+      if (j < k) add_row(rj[j], wj[j]);
+    for (int j = PRE; j < k; ++j) add_row(row_of_assign[t * k + j], topk_w[t * k + j]);
+    if (shared_row0 >= 0) {
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        if (cv[v] >= d) continue;
+        const float4 y = y_from_partials<OVERLAP>(part, n_split, split_stride, shared_row0 + t, d, cv[v]);
+        acc[v].x += y.x;
+        acc[v].y += y.y;
+        acc[v].z += y.z;
+        acc[v].w += y.w;
+      }
     }
   }
 #pragma unroll
