@@ -689,6 +689,9 @@ def run_ours(args, cfg):
         "gpu_launches": head["gpu_launches"],
         "router_gemm": {"us_per_launch": router_us, "algorithmic_bytes": router_bytes,
                         "achieved_gbs": router_bytes / (router_us / 1e6) / 1e9,
+                        "kernel": ("tensor cores (tcgen05, 8-CTA cluster per 128 tokens)"
+                                   if cfg.E <= 16 and cfg.d % 64 == 0 and cfg.T * max(cfg.E, 8) >= 8192
+                                   else "CUDA cores"),
                         "note": "back-to-back launches in one CUDA graph; x and the router weight stay in L2"},
         "router_step": router_step,
         "expert_streaming": {"h2d_gbs_dma": streaming["dma"], "h2d_gbs_sm": streaming["sm"],

@@ -133,9 +133,13 @@ moe_status moe_prepack_expert(int fmt, int d_model, int d_ff, const moe_expert_s
  *   logits[t][e] = sum_i x[t][i] * w_router[e][i]
  * x bf16 [T][d] and w_router bf16 [E][d], both row-major with the input dim
  * contiguous; logits fp32 [T][E].  Products and sums in fp32 (the order is
- * fixed, so results are reproducible run to run).  Requires d % 8 == 0,
- * 1 <= E <= 256, 16-byte aligned pointers; otherwise MOE_ERR_INVALID_ARG /
- * MOE_ERR_UNSUPPORTED and nothing is launched.  One kernel launch. */
+ * fixed, so results are reproducible run to run).  Long batches
+ * (T * max(E, 8) >= 8192) with E <= 16 and d % 64 == 0 run on the tensor cores
+ * (one cluster of 8 K-slice CTAs per 128 tokens, the slices' fp32 partial sums
+ * added in a fixed order); the rest on CUDA cores.  Requires d % 8 == 0, 1 <= E <= 256, 16-byte
+ * aligned pointers; otherwise MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED and
+ * nothing is launched.  One kernel launch.  Every wait of the tensor-core
+ * kernel is bounded: if one runs out, that tile's logits are NaN. */
 moe_status moe_router_logits(const uint16_t* x, const uint16_t* w_router, int T, int d, int E,
                              float* logits, moe_stream_t stream);
 
@@ -346,7 +350,8 @@ int moe_layer_launch_count(int T, int k, const moe_pool* routed, const moe_pool*
  * context stays usable.  This call makes that path run on purpose: forwards
  * enqueued afterwards have the gate/up GEMM's producer stop after stop_stage
  * pipeline stages (-1: never), so its consumers' waits run out, and every
- * GEMM wait give up after wait_ns (0: the default, 2 s).  Host-side setting,
+ * GEMM wait give up after wait_ns (0: the default, 2 s).  The tensor-core
+ * router kernel (moe_router_logits on long batches) takes the same setting.  Host-side setting,
  * read when a forward is enqueued; not thread-safe.  moe_debug_gemm_fault(-1,
  * 0) restores the defaults.  MOE_ERR_INVALID_ARG for stop_stage < -1. */
 moe_status moe_debug_gemm_fault(int stop_stage, unsigned long long wait_ns);

@@ -211,6 +211,19 @@ LayerLayout layer_layout(int T, int k, const moe_pool* routed, const moe_pool* s
 int g_fault_stop_stage = -1;
 unsigned long long g_fault_wait_ns = MOE_WAIT_LIMIT_NS;
 
+// The router GEMM: tensor cores for long batches of at most 16 experts, else
+// the CUDA-core kernel.
+cudaError_t run_router(const uint16_t* x, const uint16_t* w_router, int T, int d, int E, float* logits,
+                       int* err, cudaStream_t s, bool pdl) {
+  if (router_uses_tensor_cores(T, d, E)) {
+    CUtensorMap tx, tw;
+    if (!make_row_map(&tx, x, T, d, 128, false) || !make_row_map(&tw, w_router, E, d, 16, false))
+      return cudaErrorInvalidValue;
+    return launch_router_logits_tc(tx, tw, T, d, E, logits, err, g_fault_stop_stage, g_fault_wait_ns, s, pdl);
+  }
+  return launch_router_logits(x, w_router, T, d, E, logits, sm_count(), s, pdl);
+}
+
 GemmArgs base_args(const moe_pool* routed, const moe_pool* shared, int* err) {
   GemmArgs a{};
   a.wait_ns = g_fault_wait_ns;
@@ -373,8 +386,7 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
       return MOE_ERR_CUDA;
     if (!rec(MOE_STAGE_PERMUTE) || !rec(MOE_STAGE_GATHER)) return MOE_ERR_CUDA;
   } else {
-    if (w_router && launch_router_logits(x, w_router, T, L.d, E, const_cast<float*>(logits), sm_count(), s) !=
-                        cudaSuccess)
+    if (w_router && run_router(x, w_router, T, L.d, E, const_cast<float*>(logits), nullptr, s, false) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (launch_route_topk(logits, T, E, k, idx, w, nullptr, s, w_router != nullptr && pdl) != cudaSuccess)
       return MOE_ERR_CUDA;
@@ -460,8 +472,7 @@ moe_status moe_router_logits(const uint16_t* x, const uint16_t* w_router, int T,
   const moe::NvtxRange nvtx_range("moe_router_logits");
   const moe_status st = check_router_args(x, w_router, T, d, E, logits);
   if (st != MOE_OK) return st;
-  return launch_router_logits(x, w_router, T, d, E, logits, sm_count(), (cudaStream_t)stream) ==
-                 cudaSuccess
+  return run_router(x, w_router, T, d, E, logits, nullptr, (cudaStream_t)stream, false) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }

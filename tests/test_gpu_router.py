@@ -2,11 +2,19 @@
 fp32 sums) against the oracle's exact fp64 dot products, and of the layer
 forward that starts from the token rows and the router weight.
 
-Tolerance, from the kernel's arithmetic: every logit is one fixed-order fp32
-sum whose longest chain has n = 8 * ceil(d / 2048) + 5 + 8 roundings (a
-thread's FMAs over its K vectors, the 5-step warp butterfly, the 8 warps' sums),
-so |got - exact| <= gamma_n * sum_i |x_i w_i| with gamma_n = n u / (1 - n u),
-u = 2^-24 (the bf16 products themselves are exact in fp32)."""
+Tolerance, from the kernels' arithmetic (the bf16 products are exact in fp32;
+|got - exact| <= gamma_n * sum_i |x_i w_i| with gamma_n = n u / (1 - n u)):
+  CUDA-core kernel (T <= 64, or more than 16 experts): one fixed-order fp32 sum
+  whose longest chain has n = 8 * ceil(d / 2048) + 5 + 8 roundings (a thread's
+  FMAs over its K vectors, the 5-step warp butterfly, the 8 warps' sums),
+  u = 2^-24;
+  tensor-core kernel (T * max(E, 8) >= 8192, at most 16 experts, d % 64 == 0):
+  each of the 8
+  K slices accumulates 4 * ceil(d / 512) MMAs of 16 products into an fp32
+  accumulator, then the 8 slice sums are added in rank order.  The tensor
+  pipe may truncate rather than round when it aligns and adds, so every
+  addition counts with u = 2^-23, and the 16-product block sum inside one MMA
+  as 16 additions: n = 4 * ceil(d / 512) + 16 + 8."""
 import math
 
 import numpy as np
@@ -23,9 +31,16 @@ pytestmark = pytest.mark.gpu
 U = 2.0 ** -24
 
 
-def _gamma(d: int) -> float:
-    n = 8 * math.ceil(d / 2048) + 5 + 8
-    return n * U / (1 - n * U)
+def _tensor_path(T: int, d: int, E: int) -> bool:
+    return E <= 16 and d % 64 == 0 and T * max(E, 8) >= 8192
+
+
+def _gamma(T: int, d: int, E: int) -> float:
+    if _tensor_path(T, d, E):
+        n, u = 4 * math.ceil(d / 512) + 16 + 8, 2.0 ** -23
+    else:
+        n, u = 8 * math.ceil(d / 2048) + 5 + 8, U
+    return n * u / (1 - n * u)
 
 
 def _abs_dot(x: torch.Tensor, w: torch.Tensor) -> np.ndarray:
@@ -44,7 +59,7 @@ def _draw(T, d, E, seed):
 
 def _check_logits(got: torch.Tensor, x: torch.Tensor, w: torch.Tensor, what: str):
     want = oracle.router_logits(x.cpu(), w.cpu())
-    bound = _gamma(x.shape[1]) * _abs_dot(x, w) + 1e-30
+    bound = _gamma(x.shape[0], x.shape[1], w.shape[0]) * _abs_dot(x, w) + 1e-30
     err = np.abs(got.double().cpu().numpy() - want)
     worst = np.unravel_index(np.argmax(err / bound), err.shape)
     assert np.all(err <= bound), f"{what}: |err| {err[worst]:.3e} > bound {bound[worst]:.3e} at {worst}"
@@ -54,7 +69,13 @@ def _check_logits(got: torch.Tensor, x: torch.Tensor, w: torch.Tensor, what: str
 @pytest.mark.parametrize("T,d,E", [
     (16, 4096, 8),      # Mixtral-shaped decode
     (16, 5120, 128),    # 125B-class decode
-    (2048, 4096, 8),    # Mixtral-shaped prefill chunk
+    (2048, 4096, 8),    # Mixtral-shaped prefill chunk (tensor cores)
+    (256, 4096, 16),    # Phi-3.5-MoE-shaped prefill chunk (CUDA cores: below the crossover)
+    (600, 1024, 16),    # tensor cores, N = E = 16, ragged last token tile
+    (4133, 4096, 8),    # tensor cores, more clusters than SMs, ragged last token tile
+    (1100, 64, 3),      # tensor cores: one K step, so seven of the eight K slices are empty
+    (1030, 576, 9),     # tensor cores: 9 K steps over 8 slices, E not a multiple of 4
+    (1024, 1024, 17),   # just past the tensor path (E > 16): the CUDA-core kernel
     (37, 392, 5),       # ragged: T not a tile multiple, d not a multiple of 128, E < 8
     (1, 256, 1),        # one token, one expert
     (301, 1024, 256),   # the largest E, ragged last token tile
@@ -81,8 +102,39 @@ def test_router_logits_reproducible_and_row_independent():
     assert torch.equal(a[17:18], one)
 
 
+def test_tensor_core_router_reproducible_and_row_independent():
+    """The tensor-core router: the same bits twice, and a token's logits do not
+    depend on its row inside the 128-token tile or on the other tokens."""
+    x, w = _draw(1300, 4096, 8, seed=6)
+    xd, wd = x.cuda(), w.cuda()
+    a = moe.router_logits(xd, wd)
+    b = moe.router_logits(xd, wd)
+    tail = moe.router_logits(xd[100:].contiguous(), wd)        # 1200 tokens, shifted by 100 rows
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert torch.equal(a[100:], tail)
+
+
+def test_tensor_core_router_wait_timeout_gives_nan_and_context_stays_usable():
+    """Bounded waits: with the fault hook the router's TMA producer stops after
+    two K steps, the MMA warp's wait runs out after 1 ms and the tiles' logits
+    come out NaN (the call ends, no hang); afterwards the same call is exact."""
+    x, w = _draw(1024, 4096, 8, seed=8)
+    xd, wd = x.cuda(), w.cuda()
+    try:
+        moe.debug_gemm_fault(stop_stage=2, wait_ns=1_000_000)
+        bad = moe.router_logits(xd, wd)
+        torch.cuda.synchronize()
+    finally:
+        moe.debug_gemm_fault()
+    assert torch.isnan(bad).all()
+    got = moe.router_logits(xd, wd)
+    torch.cuda.synchronize()
+    _check_logits(got, x, w, "after the timeout")
+
+
 @pytest.mark.parametrize("name", ["tiny_int4", "int4_shared_perm", "int4_ragged", "fused_route_max",
-                                  "fused_route_bf16", "large_E_decode", "prefill_chunk"])
+                                  "fused_route_bf16", "large_E_decode", "prefill_chunk", "prefill_long"])
 def test_layer_forward_router(name):
     """The layer from x and the router weight: logits within the bound above,
     then every token whose top-k choice is unambiguous under that bound routed as
@@ -92,8 +144,10 @@ def test_layer_forward_router(name):
         # E > 32 and the shared expert on the fused path
         "large_E_decode": ms.LayerConfig("large_E_decode", T=16, d=512, F=256, E=128, k=8, fmt="int4",
                                          logits="zipf", zipf_s=1.1, shared=True, slot_perm=True, seed=71),
-        # more than 64 tokens: the router GEMM as its own launch
+        # more than 64 tokens: the router GEMM as its own launch (CUDA cores)
         "prefill_chunk": ms.LayerConfig("prefill_chunk", T=200, d=384, F=256, E=8, k=2, fmt="int4", seed=72),
+        # a long chunk: the tensor-core router
+        "prefill_long": ms.LayerConfig("prefill_long", T=1100, d=384, F=256, E=8, k=2, fmt="int4", seed=73),
     }
     cfg = SMALL[name] if name in SMALL else extra[name]
     L = GpuLayer(cfg)
