@@ -220,6 +220,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                            ? (512 - NA * (int)A_COLS) / (int)SLICE
                            : G_MAX_NBUF;               // accumulator slices
   static_assert(NA * (int)A_COLS + NBUF * (int)SLICE <= 512, "tensor memory columns");
+  // The two MMA warps and the two unpack teams take alternate groups, and a
+  // barrier polled by parity must never run two phases ahead of a waiter: so
+  // every A slot and every accumulator slice belongs to one MMA warp (and one
+  // unpack team) only, i.e. both counts are multiples of 2.  (With 3 A slots
+  // and 5 slices a warp saw the phase before its own as complete and the
+  // pipeline stalled until the wait limit.)
+  static_assert(G_NMMA == 2 && G_NUP / 4 == 2 && NA % 2 == 0 && NBUF % 2 == 0, "slots per MMA warp");
   const int n_st = p.n_raw;
 
   extern __shared__ uint8_t smem_dyn[];
