@@ -65,6 +65,10 @@ SMALL = {
                                         logits="zipf", zipf_s=1.1, shared=True, slot_perm=True, seed=19),
     "int4_streamk_g32": ms.LayerConfig("int4_streamk_g32", T=24, d=256, F=11136, E=3, k=2, fmt="int4",
                                        seed=20),
+    # more than 256 tokens, top-4 and the shared expert: the combine's
+    # all-rows-in-flight path for one K split at prefill widths
+    "int4_prefill_shared_k4": ms.LayerConfig("int4_prefill_shared_k4", T=300, d=256, F=384, E=8, k=4,
+                                             fmt="int4", shared=True, seed=21),
 }
 
 
