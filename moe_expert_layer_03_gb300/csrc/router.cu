@@ -240,8 +240,11 @@ cudaError_t launch_router_logits_tc(const CUtensorMap& tx, const CUtensorMap& tw
                                     bool pdl) {
   static bool attr_set = false;   // benign race: every caller sets the same value
   if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RTC_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RTC_SMEM);
+    // the whole unified L1 as shared memory, so that two CTAs fit on an SM
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
