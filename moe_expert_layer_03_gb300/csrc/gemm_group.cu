@@ -547,6 +547,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       if (!it.slot) continue;
       const int g0 = it.g0, g1 = it.g1;
       const int nc = max(0, min(CW, it.n_rows - c0));   // my token columns of this item
+      // gate/up: the token rows' unscale factors for the item epilogue, loaded
+      // now so that their latency hides behind the item's groups
+      float ufac[CW];
+#pragma unroll
+      for (int i = 0; i < CW; ++i) ufac[i] = (GATEUP && i < nc) ? __ldg(p.b_scale + it.r0 + c0 + i) : 0.f;
       float acc[NM][CW];
 #pragma unroll
       for (int m = 0; m < NM; ++m)
@@ -666,12 +671,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         // maxima and sums through shared memory (bounded mbarrier hand-offs).
         const uint32_t par = it_count & 1u;
         float hv[CW];
-        const float* ue = p.b_scale + it.r0 + c0;   // the token rows' unscale factors
 #pragma unroll
         for (int i = 0; i < CW; ++i) {
           hv[i] = 0.f;
           if (i < nc) {
-            const float u = __ldg(ue + i);
+            const float u = ufac[i];
             hv[i] = silu_f(acc[0][i] * u) * (acc[1][i] * u);
           }
         }
