@@ -586,10 +586,11 @@ def run_ours(args, cfg):
         lg_np = rg_graph.logits.cpu().numpy()
         router_step = {"us_per_step": q0.elapsed_time(q1) / args.steps * 1e3,
                        "us_per_step_two_calls": q2.elapsed_time(q3) / args.steps * 1e3,
-                       "gpu_launches_per_step": moe.layer_launch_count(cfg.T, cfg.k, routed, shared)
-                                                + (0 if cfg.T <= 64 else 1),
+                       "gpu_launches_per_step": moe.layer_router_launch_count(cfg.T, cfg.k, routed, shared),
                        "gpu_launches_per_step_two_calls": moe.layer_launch_count(cfg.T, cfg.k, routed, shared) + 1,
                        "router_fused_into_routing_launch": cfg.T <= 64,
+                       "topk_fused_into_router_launch": cfg.T > 64 and cfg.E <= 16 and cfg.d % 64 == 0
+                                                        and cfg.T * max(cfg.E, 8) >= 8192,
                        "active_experts": len(needed_experts(cfg, lg_np, list(range(cfg.T))))
                                          + (1 if cfg.shared else 0),
                        "matches_router_then_layer": bool(same),

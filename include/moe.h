@@ -206,7 +206,11 @@ moe_status moe_layer_forward(const uint16_t* x, const float* logits, int T, int 
  * of the gating on the GPU): a cooperative launch of at most one CTA per SM,
  * so the call launches as many kernels as moe_layer_forward; it fails with
  * MOE_ERR_CUDA where a cooperative launch is refused (fewer resident CTAs than
- * its grid).  Larger batches run the router GEMM as its own launch first. */
+ * its grid).  Larger batches run the router GEMM as its own launch first; on
+ * the tensor cores (T * max(E, 8) >= 8192, E <= 16, d_model % 64 == 0) that
+ * launch also does the top-k gating of its rows, with the routing kernel's
+ * selection and arithmetic (the same indices and weights), in place of the
+ * routing launch. */
 moe_status moe_layer_forward_router(const uint16_t* x, const uint16_t* w_router, int T, int k,
                                     const moe_pool* routed, const moe_pool* shared,
                                     float* logits, uint16_t* out, void* ws, size_t ws_bytes,
@@ -342,6 +346,11 @@ void moe_cache_destroy(moe_expert_cache* cache);
 
 /* Kernel launches one moe_layer_forward enqueues for these arguments (0 on error). */
 int moe_layer_launch_count(int T, int k, const moe_pool* routed, const moe_pool* shared);
+/* The same for moe_layer_forward_router: T <= 64, as moe_layer_forward (the
+ * router runs inside the routing launch); longer batches one more (the router
+ * launch), except on the tensor-core router, whose launch also does the top-k
+ * gating (T * max(E, 8) >= 8192, E <= 16). */
+int moe_layer_router_launch_count(int T, int k, const moe_pool* routed, const moe_pool* shared);
 
 /* Test hook for the failure paths (not for production use; the pages have no
  * counterpart).  Every wait in the grouped-GEMM kernels is bounded: past its

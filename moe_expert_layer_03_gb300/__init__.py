@@ -35,7 +35,8 @@ DEVERR = {1: "timeout", 2: "expert index out of range", 4: "slot out of range", 
 EXPORTS = ("moe_status_str", "moe_slot_bytes", "moe_prepack_expert", "moe_route_topk",
            "moe_permute_workspace_bytes", "moe_permute", "moe_grouped_ffn_workspace_bytes",
            "moe_grouped_ffn", "moe_combine", "moe_layer_workspace_bytes", "moe_layer_forward",
-           "moe_layer_forward_timed", "moe_layer_launch_count", "moe_last_device_error",
+           "moe_layer_forward_timed", "moe_layer_launch_count", "moe_layer_router_launch_count",
+           "moe_last_device_error",
            "moe_layer_forward_noalloc", "moe_noalloc_last_device_error", "moe_router_logits", "moe_layer_forward_router",
            "moe_cache_create", "moe_cache_ensure", "moe_cache_plan", "moe_cache_prefetch",
            "moe_cache_commit", "moe_cache_stats", "moe_cache_destroy", "moe_debug_gemm_fault")
@@ -103,6 +104,7 @@ def lib() -> C.CDLL:
             L.moe_layer_forward_timed.argtypes = [P, P, I, I, C.POINTER(MoePool),
                                                   C.POINTER(MoePool), P, P, S, P, P]
             L.moe_layer_launch_count.argtypes = [I, I, C.POINTER(MoePool), C.POINTER(MoePool)]
+            L.moe_layer_router_launch_count.argtypes = [I, I, C.POINTER(MoePool), C.POINTER(MoePool)]
             L.moe_last_device_error.argtypes = [P, C.POINTER(C.c_int), P]
             L.moe_debug_gemm_fault.argtypes = [I, C.c_ulonglong]
             _lib = L
@@ -402,6 +404,11 @@ def layer_forward_router(x: torch.Tensor, w_router: torch.Tensor, k: int, routed
 
 def layer_launch_count(T: int, k: int, routed: PoolView, shared: PoolView | None = None) -> int:
     return lib().moe_layer_launch_count(T, k, routed.ref, shared.ref if shared else None)
+
+
+def layer_router_launch_count(T: int, k: int, routed: PoolView, shared: PoolView | None = None) -> int:
+    """Kernel launches of one layer_forward_router call."""
+    return lib().moe_layer_router_launch_count(T, k, routed.ref, shared.ref if shared else None)
 
 
 class LayerGraph:

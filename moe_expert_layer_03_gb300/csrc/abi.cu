@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "kernels.cuh"
+#include "router_tc.h"
 #include "nvtx_range.h"
 #include "router_dev.cuh"
 
@@ -213,13 +214,19 @@ unsigned long long g_fault_wait_ns = MOE_WAIT_LIMIT_NS;
 
 // The router GEMM: tensor cores for long batches of at most 16 experts, else
 // the CUDA-core kernel.
+// With idx != nullptr the tensor-core kernel also does the top-k gating of its
+// rows (*topk_done = true); the CUDA-core kernel leaves it to the routing kernel.
 cudaError_t run_router(const uint16_t* x, const uint16_t* w_router, int T, int d, int E, float* logits,
-                       int* err, cudaStream_t s, bool pdl) {
+                       int* err, cudaStream_t s, bool pdl, int k = 0, int32_t* idx = nullptr,
+                       float* w = nullptr, bool* topk_done = nullptr) {
+  if (topk_done) *topk_done = false;
   if (router_uses_tensor_cores(T, d, E)) {
     CUtensorMap tx, tw;
     if (!make_row_map(&tx, x, T, d, 128, false) || !make_row_map(&tw, w_router, E, d, 16, false))
       return cudaErrorInvalidValue;
-    return launch_router_logits_tc(tx, tw, T, d, E, logits, err, g_fault_stop_stage, g_fault_wait_ns, s, pdl);
+    if (topk_done) *topk_done = idx != nullptr;
+    return launch_router_topk_tc(tx, tw, T, d, E, logits, idx != nullptr ? k : 0, idx, w, err, g_fault_stop_stage,
+                                 g_fault_wait_ns, s, pdl);
   }
   return launch_router_logits(x, w_router, T, d, E, logits, sm_count(), s, pdl);
 }
@@ -386,9 +393,12 @@ moe_status layer_forward_impl(const uint16_t* x, const float* logits, int T, int
       return MOE_ERR_CUDA;
     if (!rec(MOE_STAGE_PERMUTE) || !rec(MOE_STAGE_GATHER)) return MOE_ERR_CUDA;
   } else {
-    if (w_router && run_router(x, w_router, T, L.d, E, const_cast<float*>(logits), nullptr, s, false) != cudaSuccess)
+    // the router (on the tensor cores: with the top-k gating of its rows fused in)
+    bool topk_done = false;
+    if (w_router && run_router(x, w_router, T, L.d, E, const_cast<float*>(logits), nullptr, s, false, k, idx, w,
+                               &topk_done) != cudaSuccess)
       return MOE_ERR_CUDA;
-    if (launch_route_topk(logits, T, E, k, idx, w, nullptr, s, w_router != nullptr && pdl) != cudaSuccess)
+    if (!topk_done && launch_route_topk(logits, T, E, k, idx, w, nullptr, s, w_router != nullptr && pdl) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (!rec(MOE_STAGE_PERMUTE)) return MOE_ERR_CUDA;
     if (launch_permute_index(idx, T, k, E, L.Tsh, counts, offsets, roa, tor, err, s, pdl) != cudaSuccess)
@@ -644,6 +654,13 @@ int moe_layer_launch_count(int T, int k, const moe_pool* routed, const moe_pool*
   if (moe_layer_workspace_bytes(T, k, routed, shared) == 0) return 0;
   // route + permute + gather in one launch for small batches; gate/up, down, combine
   return T <= FUSED_ROUTE_MAX_T ? 4 : 6;
+}
+
+int moe_layer_router_launch_count(int T, int k, const moe_pool* routed, const moe_pool* shared) {
+  const int n = moe_layer_launch_count(T, k, routed, shared);
+  if (n == 0 || T <= FUSED_ROUTE_MAX_T) return n;   // the router runs inside the routing launch
+  // its own launch; on the tensor cores it also does the top-k (one launch fewer)
+  return router_uses_tensor_cores(T, routed->d_model, routed->n_experts) ? n : n + 1;
 }
 
 moe_status moe_debug_gemm_fault(int stop_stage, unsigned long long wait_ns) {

@@ -14,6 +14,7 @@
 // warp order from shared memory: a fixed order, so the result does not depend
 // on scheduling.
 #include "router_dev.cuh"
+#include "router_tc.h"
 
 namespace moe {
 
@@ -69,7 +70,8 @@ __device__ __forceinline__ bool rtc_wait(uint32_t bar, uint32_t parity, uint64_t
 
 __global__ void __cluster_dims__(1, RTC_SPLIT, 1) __launch_bounds__(128, 2)
     router_tc_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw, int T, int d,
-                     int E, float* __restrict__ logits, int* err, int stop_stage, uint64_t wait_ns) {
+                     int E, float* __restrict__ logits, int k, int32_t* __restrict__ idx, float* __restrict__ w,
+                     int* err, int stop_stage, uint64_t wait_ns) {
   extern __shared__ uint8_t smem_dyn[];
   const uint32_t pad = (1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u;
   uint8_t* base = smem_dyn + pad;
@@ -193,11 +195,12 @@ __global__ void __cluster_dims__(1, RTC_SPLIT, 1) __launch_bounds__(128, 2)
   if ((!good || !in) && err != nullptr && threadIdx.x == 0) atomicOr(err, MOE_DEVERR_TIMEOUT);
   griddep_launch_dependents();
   // this CTA's rows: thread (row, group of 4 experts) adds the slices in rank order
-  if (threadIdx.x < RTC_ROWS * (RTC_N / 4)) {
-    const int row = (int)threadIdx.x / (RTC_N / 4), j = ((int)threadIdx.x % (RTC_N / 4)) * 4;
+  if (threadIdx.x < RTC_ROWS * (RTC_N / 4)) {   // warps 0 and 1, whole: the top-k below shuffles
+    const int jg = (int)threadIdx.x % (RTC_N / 4);
+    const int row = (int)threadIdx.x / (RTC_N / 4), j = jg * 4;
     const int t = tile * RTC_M + rank * RTC_ROWS + row;
-    if (t < T && j < E) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (j < E) {
 #pragma unroll
       for (int r = 0; r < RTC_SPLIT; ++r) {
         const float4 q = *reinterpret_cast<const float4*>(red + ((size_t)r * RTC_ROWS + row) * RTC_LD + j);
@@ -206,8 +209,10 @@ __global__ void __cluster_dims__(1, RTC_SPLIT, 1) __launch_bounds__(128, 2)
         acc.z += q.z;
         acc.w += q.w;
       }
-      if (!in) acc = make_float4(__int_as_float(0x7FC00000), __int_as_float(0x7FC00000), __int_as_float(0x7FC00000),
-                                 __int_as_float(0x7FC00000));
+    }
+    if (!in) acc = make_float4(__int_as_float(0x7FC00000), __int_as_float(0x7FC00000), __int_as_float(0x7FC00000),
+                               __int_as_float(0x7FC00000));
+    if (t < T && j < E) {
       float* out = logits + (size_t)t * E + j;
       if ((E & 3) == 0) {   // 16-byte aligned (the logits buffer is)
         *reinterpret_cast<float4*>(out) = acc;
@@ -216,6 +221,56 @@ __global__ void __cluster_dims__(1, RTC_SPLIT, 1) __launch_bounds__(128, 2)
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           if (j + c < E) out[c] = q[c];
+      }
+    }
+    if (idx != nullptr) {
+      // top-k gating of the row (the same selection and softmax as the routing
+      // kernels, so the same bits): the row's 4 threads hold experts j..j+3;
+      // k rounds of an arg-max on (value desc, index asc) over the 4 lanes,
+      // NaN ranked below every number; weights = softmax over the selected
+      // logits, max-subtracted, summed in selection order
+      float v[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (v[q] != v[q]) v[q] = -INFINITY;
+      uint32_t taken = 0;
+      float sel[RTC_N];
+#pragma unroll
+      for (int sx = 0; sx < RTC_N; ++sx) {
+        if (sx < k) {
+          float bv = -INFINITY;
+          int bi = 0x7FFFFFFF;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int e = j + q;
+            if (e < E && !((taken >> q) & 1u) && (v[q] > bv || (v[q] == bv && e < bi))) {
+              bv = v[q];
+              bi = e;
+            }
+          }
+#pragma unroll
+          for (int off = 1; off < 4; off <<= 1) {   // within the row's 4 lanes
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (ov > bv || (ov == bv && oi < bi)) {
+              bv = ov;
+              bi = oi;
+            }
+          }
+          if ((bi >> 2) == jg) taken |= 1u << (bi & 3);
+          sel[sx] = bv;
+          if (jg == 0 && t < T) idx[(size_t)t * k + sx] = bi;
+        }
+      }
+      if (jg == 0 && t < T) {
+        const float m = sel[0];
+        float den = 0.f;
+#pragma unroll
+        for (int sx = 0; sx < RTC_N; ++sx)
+          if (sx < k) den += expf(sel[sx] - m);
+#pragma unroll
+        for (int sx = 0; sx < RTC_N; ++sx)
+          if (sx < k) w[(size_t)t * k + sx] = expf(sel[sx] - m) / den;
       }
     }
   }
@@ -238,6 +293,12 @@ bool router_uses_tensor_cores(int T, int d, int E) {
 cudaError_t launch_router_logits_tc(const CUtensorMap& tx, const CUtensorMap& tw, int T, int d, int E,
                                     float* logits, int* err, int stop_stage, uint64_t wait_ns, cudaStream_t s,
                                     bool pdl) {
+  return launch_router_topk_tc(tx, tw, T, d, E, logits, 0, nullptr, nullptr, err, stop_stage, wait_ns, s, pdl);
+}
+
+cudaError_t launch_router_topk_tc(const CUtensorMap& tx, const CUtensorMap& tw, int T, int d, int E, float* logits,
+                                  int k, int32_t* idx, float* w, int* err, int stop_stage, uint64_t wait_ns,
+                                  cudaStream_t s, bool pdl) {
   static bool attr_set = false;   // benign race: every caller sets the same value
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RTC_SMEM);
@@ -249,7 +310,7 @@ cudaError_t launch_router_logits_tc(const CUtensorMap& tx, const CUtensorMap& tw
     attr_set = true;
   }
   return launch_kernel(router_tc_kernel, dim3((unsigned)((T + RTC_M - 1) / RTC_M), RTC_SPLIT), dim3(128), RTC_SMEM,
-                       s, pdl, tx, tw, T, d, E, logits, err, stop_stage, wait_ns);
+                       s, pdl, tx, tw, T, d, E, logits, k, idx, w, err, stop_stage, wait_ns);
 }
 
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w_router, int T, int d, int E,

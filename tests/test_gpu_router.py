@@ -134,7 +134,8 @@ def test_tensor_core_router_wait_timeout_gives_nan_and_context_stays_usable():
 
 
 @pytest.mark.parametrize("name", ["tiny_int4", "int4_shared_perm", "int4_ragged", "fused_route_max",
-                                  "fused_route_bf16", "large_E_decode", "prefill_chunk", "prefill_long"])
+                                  "fused_route_bf16", "large_E_decode", "prefill_chunk", "prefill_long",
+                                  "prefill_long_e16"])
 def test_layer_forward_router(name):
     """The layer from x and the router weight: logits within the bound above,
     then every token whose top-k choice is unambiguous under that bound routed as
@@ -146,8 +147,11 @@ def test_layer_forward_router(name):
                                          logits="zipf", zipf_s=1.1, shared=True, slot_perm=True, seed=71),
         # more than 64 tokens: the router GEMM as its own launch (CUDA cores)
         "prefill_chunk": ms.LayerConfig("prefill_chunk", T=200, d=384, F=256, E=8, k=2, fmt="int4", seed=72),
-        # a long chunk: the tensor-core router
+        # a long chunk: the tensor-core router, with the top-k gating in its launch
         "prefill_long": ms.LayerConfig("prefill_long", T=1100, d=384, F=256, E=8, k=2, fmt="int4", seed=73),
+        # the same at N = E = 16, top-4, with the shared expert
+        "prefill_long_e16": ms.LayerConfig("prefill_long_e16", T=600, d=256, F=256, E=16, k=4, fmt="int4",
+                                           shared=True, seed=74),
     }
     cfg = SMALL[name] if name in SMALL else extra[name]
     L = GpuLayer(cfg)
@@ -179,3 +183,17 @@ def test_layer_forward_router(name):
 
     L.logits_np = lg32
     assert_close_rms(out.float().cpu().numpy()[toks], L.oracle_forward(toks), what=name)
+
+
+def test_layer_router_launch_count():
+    """Launches of one layer_forward_router call: the router inside the routing
+    launch for T <= 64; its own launch above; on the tensor cores that launch
+    also does the top-k gating, in place of the routing launch."""
+    cases = [(ms.LayerConfig("lc_decode", T=16, d=256, F=256, E=8, k=2, fmt="int4", seed=75), 0),
+             (ms.LayerConfig("lc_cuda_cores", T=200, d=256, F=256, E=8, k=2, fmt="int4", seed=76), 1),
+             (ms.LayerConfig("lc_tensor", T=1100, d=256, F=256, E=8, k=2, fmt="int4", seed=77), 0),
+             (ms.LayerConfig("lc_wide_E", T=1100, d=256, F=256, E=32, k=2, fmt="int4", seed=78), 1)]
+    for cfg, extra in cases:
+        L = GpuLayer(cfg)
+        n = moe.layer_launch_count(cfg.T, cfg.k, L.routed, L.shared)
+        assert moe.layer_router_launch_count(cfg.T, cfg.k, L.routed, L.shared) == n + extra, cfg.name
