@@ -40,7 +40,11 @@
 //     (fold + epilogue) are separate; two MMA warps take alternate groups and
 //     issue from a converged warp (elect.sync).
 //
-//   warp 0       producer (bulk copy + TMA)
+//   warps 0, 19  producers (bulk copy + TMA), one lane each, alternate groups:
+//                an async-copy instruction costs its thread ~100 cycles of
+//                issue, and one thread issuing every stage paced the
+//                pipeline (Mixtral-shaped step 149.7 -> 148.0 us, 125B-class
+//                143.0 -> 139.7 us)
 //   warps 1-2    MMA issuers (warp 1 owns TMEM)
 //   warps 3-10   unpack: two teams of four (one warp per TMEM lane quadrant)
 //                taking alternate groups; a warp writes all codes of its
@@ -67,13 +71,15 @@ namespace {
 
 constexpr int G_MAX_NBUF = 4;   // accumulator slices (fewer where TMEM is short)
 constexpr int G_MAX_NA = 4;     // A slots in tensor memory
-constexpr int G_MISC = 8;       // [0] tmem [1] abort [2] items [3] stages issued [4] stays 0
+constexpr int G_MISC = 8;       // [0] tmem [1] abort [2] items [3] and [5] the producers' last group + 1
+                                // [4] stays 0
 constexpr int G_NMMA = 2;       // MMA-issuing warps (alternate groups)
 constexpr int G_NUP = 8;        // unpack warps
 constexpr int G_NFOLD = 8;      // fold + epilogue warps
 constexpr int G_UP0 = 1 + G_NMMA;                  // first unpack warp
 constexpr int G_FOLD0 = G_UP0 + G_NUP;             // first fold warp
-constexpr int G_THREADS = (G_FOLD0 + G_NFOLD) * 32;
+constexpr int G_PROD1 = G_FOLD0 + G_NFOLD;          // the second producer warp
+constexpr int G_THREADS = (G_PROD1 + 1) * 32;
 
 enum GroupMode { G_GATEUP = 0, G_DOWN_PAIR = 1, G_DOWN = 2 };
 
@@ -367,15 +373,20 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   const int n_mine = S.misc[2];   // items of this CTA
   const uint32_t acc0 = NA * A_COLS;   // accumulator slices follow the A slots
 
-  if (warp == 0) {
-    // ================================================================ producer
+  if (warp == 0 || warp == G_PROD1) {
+    // ================================================================ producers
     // Per group one stage: the NMAT nibble blocks and the token tile (hi rows
     // at y = r0, lo rows at y = rows_total + r0), on one barrier.  In the
     // paired down mode the item's tile index mt names the output tiles 2mt
-    // and 2mt + 1.
+    // and 2mt + 1.  Two producers take alternate groups; the stage count is
+    // even, so every stage belongs to one of them and each waits only for its
+    // own stages' earlier fills (the consumers take the groups in order, so
+    // neither can wait on a group the other has not issued yet).
     if (lane == 0) {
+      const int pid = warp == 0 ? 0 : 1;   // producer pid feeds the groups gc with gc % 2 == pid
       Ring rs{0, 0, n_st};
-      int issued = 0;
+      int last = 0;
+      uint32_t gc = 0;
       const uint64_t pol = policy_evict_first();
       bool ok = true;
       for (int ii = 0; ii < n_mine && ok && !*abort_flag; ++ii) {
@@ -383,8 +394,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         if (!it.slot) continue;
         const int g0 = it.g0, g1 = it.g1;
         const uint8_t* sec = it.slot + p.sec_off;
-        for (int kg = g0; kg < g1; ++kg) {
-          if (issued == p.stop_stage) {   // test hook: stop feeding the pipeline
+        for (int kg = g0; kg < g1; ++kg, ++gc, rs.next()) {
+          if ((int)(gc & 1u) != pid) continue;
+          if ((int)gc == p.stop_stage) {   // test hook: stop feeding the pipeline
             ok = false;
             break;
           }
@@ -411,11 +423,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           const uint32_t dst = smem_u32(S.b_ring + (size_t)rs.i * B_STAGE);
           tma_load_2d(dst, &tmap_b, kg * QGROUP, it.r0, bar);
           tma_load_2d(dst + B_BOX, &tmap_b, kg * QGROUP, p.rows_total + it.r0, bar);
-          rs.next();
-          ++issued;
+          last = (int)gc + 1;
         }
       }
-      S.misc[3] = issued;
+      S.misc[pid ? 5 : 3] = last;
     }
   } else if (warp < G_UP0) {
     // ================================================================ MMA issuers
@@ -740,11 +751,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   // ------------------------------------------------------------ teardown
   __syncthreads();
   volatile int* no_abort = &S.misc[4];   // stays 0: drain waits are bounded by time only
-  if (warp == 0 && lane == 0 && *abort_flag) {
-    // for each stage, wait (bounded) for the last copies issued into it; an
-    // earlier fill of the same stage had landed before the stage was reused
-    const int iss = S.misc[3];
-    for (int sl = 0; sl < n_st && sl < iss; ++sl) {
+  if ((warp == 0 || warp == G_PROD1) && lane == 0 && *abort_flag) {
+    // for each stage of this producer, wait (bounded) for the last copies issued into it
+    const int pid = warp == 0 ? 0 : 1;
+    const int iss = S.misc[pid ? 5 : 3];
+    for (int sl = pid; sl < n_st && sl < iss; sl += 2) {
       const int q = sl + ((iss - 1 - sl) / n_st) * n_st;
       mbar_wait(smem_u32(&S.full[sl]), (uint32_t)((q / n_st) & 1), no_abort, p.err, p.wait_ns);
     }
@@ -770,6 +781,7 @@ GemmPlan plan_gemm_group(int fmt, bool gateup, int bn, int n_groups, int n_mt) {
   const size_t budget = 227 * 1024 - 1024;
   int n_st = 3;
   while (n_st < 16 && group_carve_bytes(f8w, nmat, bn, gateup, n_st + 1, n_groups) <= budget) ++n_st;
+  n_st &= ~1;   // each stage belongs to one of the two producers
   pl.n_raw = n_st;   // stages (weights + token rows)
   pl.n_b = n_st;
   pl.smem_bytes = group_carve_bytes(f8w, nmat, bn, gateup, n_st, n_groups) + 1024;
