@@ -31,8 +31,8 @@ __global__ void __launch_bounds__(RT_THREADS)
 // For long batches (T * max(E, 8) >= 8192) of at most 16 experts the router is
 // a real (if thin) contraction: D[t][e] = sum_k x[t][k] w[e][k] with M = 128
 // token rows per tile and N = 16 (the experts, the router tile's rows past E
-// read as zeros by the TMA).  One thread-block cluster of RTC_SPLIT CTAs per 128-token
-// tile, CTA r taking the r-th slice of K: TMA loads of the x tile (128 rows x 64
+// read as zeros by the TMA).  One thread-block cluster of RTC_SPLIT CTAs per
+// 128-token tile, CTA r taking the r-th slice of K: TMA loads of the x tile (128 rows x 64
 // K, 128-byte swizzle) and the router tile (16 rows x 64 K) through a ring of
 // stages, tcgen05.mma kind::f16 (bf16 x bf16 -> fp32) into four accumulators
 // of 16 TMEM columns (the 4 MMAs of one 64-wide K step go to different ones, so
@@ -45,8 +45,9 @@ __global__ void __launch_bounds__(RT_THREADS)
 // SM's shared-memory port carries the whole tile.  Nothing is allocated.  Every
 // wait is bounded; a CTA whose pipeline wait runs out contributes NaN, so the
 // tile's logits come out NaN (and the error word, when given, gets
-// MOE_DEVERR_TIMEOUT).  About 100 KB of shared memory, so two CTAs fit on an SM
-// and a launch of 16 clusters (2048 tokens) runs in one wave.
+// MOE_DEVERR_TIMEOUT).  About 100 KB of shared memory, so two CTAs can share an
+// SM (with ~210 KB per CTA a 2048-token launch, 16 clusters, ran in two waves;
+// now its CTAs start within ~0.7 us of each other).
 constexpr int RTC_M = 128;        // token rows per tile (the MMA's M)
 constexpr int RTC_N = 16;         // experts per tile (the MMA's N)
 constexpr int RTC_SPLIT = 8;      // CTAs per cluster = K slices per tile
