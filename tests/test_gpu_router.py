@@ -197,3 +197,32 @@ def test_layer_router_launch_count():
         L = GpuLayer(cfg)
         n = moe.layer_launch_count(cfg.T, cfg.k, L.routed, L.shared)
         assert moe.layer_router_launch_count(cfg.T, cfg.k, L.routed, L.shared) == n + extra, cfg.name
+
+
+@pytest.mark.parametrize("T", [200, 1100])   # CUDA-core router + routing kernel; tensor-core router with its top-k
+def test_router_ties_and_non_finite_rows_match_the_routing_kernel(T):
+    """Duplicate router rows (experts 1 and 2, 3 and 5: equal logits wherever
+    the two sums round alike, and then the lower index must win) and rows whose
+    logits are not finite (an inf in x) must be routed by the same rule on both
+    router paths: the layer output equals moe_layer_forward on the returned
+    logits bit for bit, and the routing of every finite row equals the oracle's
+    on those logits."""
+    cfg = ms.LayerConfig(f"ties_{T}", T=T, d=384, F=256, E=8, k=2, fmt="int4", seed=79)
+    L = GpuLayer(cfg)
+    wr = ms.make_router_weight(cfg)
+    wr[2] = wr[1]
+    wr[5] = wr[3]
+    x = L.x.clone()
+    x[7, 11] = float("inf")
+    x[T - 3, 0] = float("-inf")
+    out, logits, ws = moe.layer_forward_router(x, wr.to(L.dev), cfg.k, L.routed, L.shared)
+    out2, _ = moe.layer_forward(x, logits, cfg.k, L.routed, L.shared)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    lg = logits.cpu().numpy()
+    finite = np.all(np.isfinite(lg), axis=1)
+    assert not finite[7] and not finite[T - 3]
+    idx_gpu, w_gpu = moe.route_topk(logits, cfg.k)
+    idx_ref, w_ref = oracle.route_topk(lg[finite], cfg.k)
+    np.testing.assert_array_equal(idx_gpu.cpu().numpy()[finite], idx_ref)
+    np.testing.assert_allclose(w_gpu.cpu().numpy()[finite], w_ref, rtol=2e-6, atol=0)
