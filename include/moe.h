@@ -357,12 +357,13 @@ int moe_layer_router_launch_count(int T, int k, const moe_pool* routed, const mo
  * limit the CTA sets MOE_DEVERR_TIMEOUT in the error word, drains the copies
  * it issued, waits for its MMAs, frees its tensor memory and returns, so the
  * context stays usable.  This call makes that path run on purpose: forwards
- * enqueued afterwards have the gate/up GEMM's producer stop after stop_stage
- * pipeline stages (-1: never), so its consumers' waits run out, and every
- * GEMM wait give up after wait_ns (0: the default, 2 s).  The tensor-core
- * router kernel (moe_router_logits on long batches) takes the same setting.  Host-side setting,
- * read when a forward is enqueued; not thread-safe.  moe_debug_gemm_fault(-1,
- * 0) restores the defaults.  MOE_ERR_INVALID_ARG for stop_stage < -1. */
+ * enqueued afterwards leave the gate/up GEMM's pipeline stage number
+ * stop_stage of each CTA (counting from 0; -1: none) unissued, so the
+ * consumers' waits for it run out, and every GEMM wait give up after wait_ns
+ * (0: the default, 2 s).  The tensor-core router kernel (moe_router_logits on
+ * long batches) takes the same setting.  Host-side setting, read when a
+ * forward is enqueued; not thread-safe.  moe_debug_gemm_fault(-1, 0) restores
+ * the defaults.  MOE_ERR_INVALID_ARG for stop_stage < -1. */
 moe_status moe_debug_gemm_fault(int stop_stage, unsigned long long wait_ns);
 
 /* Synchronously reads the device error word of a workspace written by
