@@ -290,15 +290,16 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     tmem_alloc(smem_u32(&S.misc[0]), p.tmem_cols);
     tmem_relinquish();
   }
-  // fp8 weights (a pure weight stream): before the dependency wait, prefetch
-  // into L2 the first weight stages of the item this CTA gets if every group
-  // is active with one row chunk (likely when the batch holds at least two
-  // rows per routed expert), so the stream starts while the previous kernel
-  // finishes (the 8-bit Mixtral-shaped decode step: 232 -> 224 us).  Only the
-  // expert-to-slot table is read (an input, not an earlier kernel's output); a
-  // wrong guess costs the prefetched bytes.  The int4 kernel, bound by its
-  // unpack, measured no gain and keeps no such code.
-  if constexpr (F8W && MODE != G_DOWN) {
+  // Before the dependency wait, prefetch into L2 the first weight stages of
+  // the item this CTA gets if every group is active with one row chunk
+  // (likely when the batch holds at least two rows per routed expert), so the
+  // weight stream starts while the previous kernel finishes (Mixtral-shaped
+  // decode step: 8-bit 232 -> 224 us; int4, once its two producers kept the
+  // ring full, 148.7 -> 143.1 us, 125B-class 139.5 -> 137.7 us; 16 stages
+  // instead of 8 measured slower).  Only the expert-to-slot table is read (an
+  // input, not an earlier kernel's output); a wrong guess costs the
+  // prefetched bytes.
+  if constexpr (MODE != G_DOWN) {
     if (warp == 0 && lane == 0 && p.rows_total >= 2 * p.n_routed) {
       const int per_g = p.n_mt * p.ksplit;
       const int g = (int)blockIdx.x / per_g;
