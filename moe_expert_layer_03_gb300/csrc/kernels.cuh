@@ -204,15 +204,6 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 // logits[t][e] = x[t] . w_router[e] (bf16 inputs, fp32 sums; router.cu).
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w_router, int T, int d, int E,
                                  float* logits, int n_sm, cudaStream_t s, bool pdl = false);
-// The same logits on the tensor cores, for long batches of few experts (router.cu):
-// tx = x [T][d] and tw = w_router [E][d] as bf16 row maps with {64 x 128} and
-// {64 x 16} boxes and the 128-byte swizzle.  err (nullable) gets
-// MOE_DEVERR_TIMEOUT if a pipeline wait ran past wait_ns (the tile's logits are
-// then NaN); stop_stage >= 0 is the fault-injection hook (-1 off).
-bool router_uses_tensor_cores(int T, int d, int E);
-cudaError_t launch_router_logits_tc(const CUtensorMap& tx, const CUtensorMap& tw, int T, int d, int E,
-                                    float* logits, int* err, int stop_stage, uint64_t wait_ns, cudaStream_t s,
-                                    bool pdl = false);
 // err_clear (nullable): error word zeroed by the first thread (first launch of a forward).
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                               int* err_clear, cudaStream_t s, bool pdl = false);

@@ -291,12 +291,6 @@ bool router_uses_tensor_cores(int T, int d, int E) {
   return E <= RTC_N && d % 64 == 0 && (long long)T * (E > 8 ? E : 8) >= 8192;
 }
 
-cudaError_t launch_router_logits_tc(const CUtensorMap& tx, const CUtensorMap& tw, int T, int d, int E,
-                                    float* logits, int* err, int stop_stage, uint64_t wait_ns, cudaStream_t s,
-                                    bool pdl) {
-  return launch_router_topk_tc(tx, tw, T, d, E, logits, 0, nullptr, nullptr, err, stop_stage, wait_ns, s, pdl);
-}
-
 cudaError_t launch_router_topk_tc(const CUtensorMap& tx, const CUtensorMap& tw, int T, int d, int E, float* logits,
                                   int k, int32_t* idx, float* w, int* err, int stop_stage, uint64_t wait_ns,
                                   cudaStream_t s, bool pdl) {
